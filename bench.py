@@ -1,0 +1,467 @@
+#!/usr/bin/env python
+"""Benchmark of the selective-SSM forward hot path on GB300.
+
+One step = ssd_fwd on the Mamba-2 SSD workload b=4, L=8192, 80 heads, H=64, S=128, G=1,
+chunk 256, bf16 inputs / fp32 accumulation, h0 ~ N(0, 0.1^2) (4 kernels), followed by
+linscan_fwd on the scalar scan workload 384 rows x 65,536 fp32 (1 kernel).  Inputs are
+seeded synthetic values, resident in HBM before the timed region; L2 (129 MB) is flushed
+by a 256 MiB write before every timed step, outside the timed events.
+
+Prints ONE JSON line (rank 0).  value = SSD forward tokens/s (batch*seqlen per SSD call,
+summed over ranks, divided by the max over ranks of the SSD device time); the scan's GB/s,
+per-kernel times, the roofline of the dominant kernel, clocks, the end-to-end leg through the
+public API with host buffers, and the float64 oracle timed on the host cores ride along.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from selective_state_space_mamba_gb300 import synth  # noqa: E402
+
+METRIC = "SSD fwd tokens/s + % of roofline; linear-scan GB/s vs GB300 HBM peak"
+SSD = synth.SSD_B4_L8192
+SCAN = synth.SCAN_384x65536
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNELS = ("linscan_lookback", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan")
+
+
+# ----------------------------------------------------------------------------------------
+# algorithmic byte / FLOP models (per launch)
+# ----------------------------------------------------------------------------------------
+def ssd_sizes(s):
+    b, L, nh, H, S, G, T = s.batch, s.seqlen, s.nheads, s.headdim, s.dstate, s.ngroups, s.chunk
+    nc = -(-L // T)
+    e = 2 if s.dtype == "bf16" else 4
+    return dict(x=b * L * nh * H * e, dt=b * L * nh * e, BC=b * L * G * S * e, AD=2 * nh * 4,
+                state=b * nh * H * S * 4, chunk_states_f32=b * nc * nh * H * S * 4,
+                hin=b * nc * nh * H * S * e, gd=2 * b * nh * nc * T * 4, y=b * L * nh * H * e)
+
+
+def kernel_bytes(s):
+    z = ssd_sizes(s)
+    return {
+        "ssd_chunk_cumsum": z["dt"] + z["AD"] // 2 + z["gd"],
+        "ssd_chunk_state": z["x"] + z["BC"] + z["gd"] + z["chunk_states_f32"],
+        "ssd_state_passing": z["chunk_states_f32"] + z["state"] + z["hin"] + z["state"],
+        "ssd_chunk_scan": z["x"] + 2 * z["BC"] + z["gd"] + z["hin"] + z["AD"] // 2 + z["y"],
+    }
+
+
+def ssd_model_b_bytes(s):
+    """Inputs once + outputs once + per-chunk fp32 states written once and read once."""
+    z = ssd_sizes(s)
+    return z["x"] + z["dt"] + 2 * z["BC"] + z["AD"] + z["state"] + z["y"] + z["state"] + 2 * z["chunk_states_f32"]
+
+
+def ssd_flops(s):
+    b, L, nh, H, S, G, T = s.batch, s.seqlen, s.nheads, s.headdim, s.dstate, s.ngroups, s.chunk
+    nc = -(-L // T)
+    state = 2 * b * nc * nh * T * H * S                 # X~^T B per (b, c, h)
+    scan = b * nc * nh * (2 * T * T * H + 2 * T * S * H) + b * nc * G * 2 * T * T * S  # CB once per group
+    return {"ssd_chunk_state": state, "ssd_chunk_scan": scan, "total": state + scan}
+
+
+def scan_bytes(rows, length):
+    return 12 * rows * length  # read a, read b, write h
+
+
+# ----------------------------------------------------------------------------------------
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured (MEASURED_PEAKS.json)"
+    return dict(FALLBACK_PEAKS), "fallback (6.8 TB/s, 1.9 PFLOP/s)"
+
+
+def kernel_traffic(kernel):
+    """ncu DRAM bytes per launch from profiles/ncu_traffic.json, if taken on the current source."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d:
+        return None
+    src = os.path.join(ROOT, "selective_state_space_mamba_gb300", "csrc", d["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != d["source_sha"]:
+        return None
+    return d["bytes_per_launch"]
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = ""
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.out.strip().splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------------
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def device_inputs(torch, inp, dtype):
+    out = {}
+    for k, v in inp.items():
+        t = torch.from_numpy(v).cuda()
+        out[k] = t.to(torch.bfloat16) if (dtype == "bf16" and k in ("x", "dt", "B", "C")) else t
+    return out
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import selective_state_space_mamba_gb300 as ssm
+
+    peaks, peak_src = load_peaks()
+    ssd_np = synth.ssd_inputs(SSD)
+    scan_np = synth.scan_inputs(SCAN.rows, SCAN.length, seed=synth.WORKLOAD_SEED[SCAN.name])
+    d = device_inputs(torch, ssd_np, SSD.dtype)
+    a = torch.from_numpy(scan_np["a"]).cuda()
+    bsc = torch.from_numpy(scan_np["b"]).cuda()
+    y = torch.empty_like(d["x"])
+    hf = torch.empty(SSD.batch, SSD.nheads, SSD.headdim, SSD.dstate, dtype=torch.float32, device="cuda")
+    h = torch.empty_like(a)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def ssd_call():
+        ssm.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], chunk=SSD.chunk, y=y, h_final=hf)
+
+    def scan_call():
+        ssm.linscan_fwd(a, bsc, h=h)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        ssd_call()
+        scan_call()
+    torch.cuda.synchronize()
+    if ssm.check_device_status(kind="ssd") or ssm.check_device_status(kind="linscan"):
+        raise RuntimeError("device status error during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks, ssm.KernelTimer(max_launches=8 * args.steps + 8) as kt:
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)
+            ev[i][0].record(stream)
+            ssd_call()
+            ev[i][1].record(stream)
+            scan_call()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    if ssm.check_device_status(kind="ssd") or ssm.check_device_status(kind="linscan"):
+        raise RuntimeError("device status error during the timed region")
+
+    ssd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    scan_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    step_ms = sum(e[0].elapsed_time(e[2]) for e in ev) / args.steps
+    ssd_ms_max = max_over_ranks(world, ssd_ms)
+    scan_ms_max = max_over_ranks(world, scan_ms)
+    step_ms_max = max_over_ranks(world, step_ms)
+    tokens = SSD.batch * SSD.seqlen
+    value = world * tokens / (ssd_ms_max * 1e-3)
+    sbytes = scan_bytes(SCAN.rows, SCAN.length)
+    scan_gbs = world * sbytes / (scan_ms_max * 1e-3) / 1e9
+
+    # per-kernel
+    kb = kernel_bytes(SSD)
+    kb["linscan_lookback"] = sbytes
+    kflops = ssd_flops(SSD)
+    kernels = {}
+    for k in KERNELS:
+        n = kt.launches.get(k, 0)
+        ms = kt.ms.get(k, 0.0) / max(n, 1)
+        gbs = kb[k] / (ms * 1e-3) / 1e9 if ms > 0 else None
+        ent = {"launches": n, "ms_per_launch": round(ms, 5), "alg_bytes": kb[k],
+               "GB/s": round(gbs, 1) if gbs else None,
+               "hbm_frac": round(gbs / peaks["hbm_gbs"], 4) if gbs else None}
+        if k in kflops:
+            tf = kflops[k] / (ms * 1e-3) / 1e12 if ms > 0 else None
+            ent["alg_flops"] = kflops[k]
+            ent["TFLOP/s"] = round(tf, 1) if tf else None
+            ent["tensor_frac"] = round(tf / peaks["bf16_tflops"], 4) if tf else None
+        kernels[k] = ent
+    ssd_kernels = [k for k in KERNELS if k.startswith("ssd_")]
+    dom = max(ssd_kernels, key=lambda k: kt.ms.get(k, 0.0))
+    dk = kernels[dom]
+    tensor_time = kflops.get(dom, 0) / (peaks["bf16_tflops"] * 1e12)
+    hbm_time = kb[dom] / (peaks["hbm_gbs"] * 1e9)
+    if dom in kflops and tensor_time > hbm_time:
+        roof = {"kernel": dom, "bound": "tensor", "achieved": dk["TFLOP/s"], "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": dk["tensor_frac"]}
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": dk["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": dk["hbm_frac"]}
+    tr = kernel_traffic(dom)
+    roof["traffic"] = tr
+    roof["peak_source"] = peak_src + " (burst copy / burst cuBLAS)"
+
+    model_b = ssd_model_b_bytes(SSD)
+    ssd_roof_ms = max(model_b / (peaks["hbm_gbs"] * 1e9), kflops["total"] / (peaks["bf16_tflops"] * 1e12)) * 1e3
+    out = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded numpy PCG64; distributions of the pages' workloads)",
+        "config": {
+            "workload": (f"ssd_fwd b{SSD.batch} L{SSD.seqlen} nh{SSD.nheads} H{SSD.headdim} S{SSD.dstate} "
+                         f"G{SSD.ngroups} chunk{SSD.chunk} bf16/fp32-acc + linscan {SCAN.rows}x{SCAN.length} f32"),
+            "step": "ssd_fwd (4 kernels) then linscan_fwd (1 kernel); value from the ssd_fwd events",
+            "l2": "inputs larger than L2, and L2 flushed by a 256 MiB write before each timed step",
+            "parallelism": f"replicas x{world} (independent problems, no collective)",
+        },
+        "ssd": {"tokens_per_s": round(value, 1), "ms": round(ssd_ms_max, 4), "model_B_bytes": model_b,
+                "roofline_ms": round(ssd_roof_ms, 4), "roofline_frac": round(ssd_roof_ms / ssd_ms_max, 4),
+                "io_only_bytes": model_b - 2 * ssd_sizes(SSD)["chunk_states_f32"]},
+        "linscan": {"value": round(scan_gbs, 1), "unit": "GB/s", "ms": round(scan_ms_max, 4),
+                    "alg_bytes": sbytes, "frac": round(scan_gbs / world / peaks["hbm_gbs"], 4)},
+        "kernels": kernels,
+        "roofline": roof,
+        "gpu_launches": sum(kt.launches.values()),
+        "clocks": clocks.summary(),
+        "wall_s_timed": round(t_wall, 3),
+    }
+    return out, ssd_np, scan_np
+
+
+def run_e2e(args):
+    """Same metric through the public API with pinned host buffers: H2D of the inputs, the call,
+    D2H of y and h_final inside the timed region, every step."""
+    import torch
+    import selective_state_space_mamba_gb300 as ssm
+    inp = synth.ssd_inputs(SSD)
+    host = {}
+    for k, v in inp.items():
+        t = torch.from_numpy(v)
+        if SSD.dtype == "bf16" and k in ("x", "dt", "B", "C"):
+            t = t.to(torch.bfloat16)
+        host[k] = t.pin_memory()
+    dev = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
+    y_host = torch.empty_like(host["x"]).pin_memory()
+    hf_host = torch.empty(SSD.batch, SSD.nheads, SSD.headdim, SSD.dstate, dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        y, hf = ssm.ssd_fwd(dev["x"], dev["dt"], dev["A"], dev["B"], dev["C"], dev["D"], dev["h0"], chunk=SSD.chunk)
+        y_host.copy_(y, non_blocking=True)
+        hf_host.copy_(hf, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(3, min(args.steps, 10))
+    s.record(stream)
+    for _ in range(n):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / n
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = y_host.numel() * y_host.element_size() + hf_host.numel() * 4
+    return {"value": round(SSD.batch * SSD.seqlen / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def oracle_sample(ssd_np, scan_np, budget_s, unit_batch):
+    """Time the float64 C oracle, as it stands, on a bounded sample of the SSD workload (whole
+    (batch, head) units over the full sequence) and of the scan workload (whole rows)."""
+    from oracle import native
+    threads = native.max_threads()
+    total_units = SSD.batch * SSD.nheads
+    done, t_ssd = 0, 0.0
+    order = np.random.default_rng(0).permutation(total_units)
+    while done < total_units and t_ssd < budget_s:
+        units = order[done:done + unit_batch]
+        t0 = time.perf_counter()
+        native.ssd_fwd(ssd_np["x"], ssd_np["dt"], ssd_np["A"], ssd_np["B"], ssd_np["C"], ssd_np["D"], ssd_np["h0"],
+                       units=units)
+        t_ssd += time.perf_counter() - t0
+        done += len(units)
+    ssd_tokens_equiv = done / SSD.nheads * SSD.seqlen  # tokens whose every head was computed
+    rows = min(SCAN.rows, max(threads, 16))
+    t0 = time.perf_counter()
+    native.linscan(scan_np["a"], scan_np["b"], rows=np.arange(rows))
+    t_scan = time.perf_counter() - t0
+    return {
+        "ssd_tokens_per_s": ssd_tokens_equiv / t_ssd, "ssd_units": done, "ssd_s": t_ssd,
+        "scan_gbs": scan_bytes(rows, SCAN.length) / t_scan / 1e9, "scan_rows": rows, "scan_s": t_scan,
+        "cores": threads,
+    }
+
+
+def run_reference(args):
+    """The float64 oracle timed on the host cores, on this bench's workload, metric and unit:
+    each step is a bounded sample (a few whole (batch, head) units of the SSD workload)."""
+    ssd_np = synth.ssd_inputs(SSD)
+    scan_np = synth.scan_inputs(SCAN.rows, SCAN.length, seed=synth.WORKLOAD_SEED[SCAN.name])
+    from oracle import native
+    threads = native.max_threads()
+    per_step = max(1, threads)
+    res = []
+    for i in range(args.warmup + args.steps):
+        units = np.arange(i * per_step, (i + 1) * per_step) % (SSD.batch * SSD.nheads)
+        t0 = time.perf_counter()
+        native.ssd_fwd(ssd_np["x"], ssd_np["dt"], ssd_np["A"], ssd_np["B"], ssd_np["C"], ssd_np["D"], ssd_np["h0"],
+                       units=units)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            res.append(dt)
+    step_s = sum(res) / len(res)
+    tokens_equiv = per_step / SSD.nheads * SSD.seqlen
+    value = tokens_equiv / step_s
+    sample = (f"{per_step} whole (batch, head) units of the SSD workload per step "
+              f"({per_step}/{SSD.batch * SSD.nheads} of the work of one SSD call)")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded numpy PCG64)",
+            "config": {"workload": f"ssd_fwd b{SSD.batch} L{SSD.seqlen} nh{SSD.nheads} H{SSD.headdim} "
+                                   f"S{SSD.dstate} G{SSD.ngroups} (float64 oracle, sampled units)"},
+            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0, help="time budget of the oracle CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return
+        print(json.dumps(run_reference(args)))
+        return
+
+    world, rank, local = dist_setup(args)
+    out, ssd_np, scan_np = run_ours(args, world, rank, local)
+    if not args.no_e2e:
+        e2e = run_e2e(args)
+        e2e["value"] = round(max_over_ranks(world, -e2e["value"]) * -1 * world, 1) if world > 1 else e2e["value"]
+        out["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = oracle_sample(ssd_np, scan_np, args.cpu_budget_s, unit_batch=16)
+        out["cpu_baseline"] = {
+            "value": round(cb["ssd_tokens_per_s"], 1), "unit": "tokens/s", "cores": cb["cores"], "kind": "oracle",
+            "sample": (f"{cb['ssd_units']} of {SSD.batch * SSD.nheads} whole (batch, head) units of the SSD workload "
+                       f"in {cb['ssd_s']:.1f} s; tokens/s counts a token once all its heads are done"),
+            "linscan": {"value": round(cb["scan_gbs"], 2), "unit": "GB/s",
+                        "sample": f"{cb['scan_rows']} of {SCAN.rows} rows in {cb['scan_s']:.2f} s"},
+        }
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

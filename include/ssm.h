@@ -1,0 +1,166 @@
+/*
+ * ssm.h: C ABI of the GB300 (sm_103a) selective state-space forward library.
+ *
+ * Two operations, both forward only, both on one GPU:
+ *
+ *   ssm_ssd_fwd      Mamba-2 chunked SSD forward, (x, dt, A, B, C, D, h0) -> (y, h_final).
+ *                    Definition: "Accelerating Mamba-2 with High-Performance Forward
+ *                    Pass Kernels in NVIDIA CUDA Tile", section "Mamba-2 architecture":
+ *                        h_t = exp(a_t) h_{t-1} + x_t b_t^T,  a_t = A dt_t,  b_t = dt_t B_t
+ *                        y_t = h_t c_t + D x_t
+ *                    with the inclusive output reading (y_t reads the state after token
+ *                    t, as the post's chunked form and its causal mask i >= j do).  The
+ *                    chunked evaluation follows the same section's jump formula
+ *                        h_{t+T} = exp(G_last) h_t + X^T (exp(G_last - G) . B)
+ *                    and chunk output
+ *                        Y = exp(G) C h + (exp(G_i - G_j) . (C B^T) . M) X + D X,
+ *                    run as four kernels (chunk cumsum, chunk state, state passing,
+ *                    chunk scan; the post's "Kernel 1".."Kernel 3" with the chunk loop of
+ *                    Kernel 2 split into a parallel part and a look-back scan).
+ *
+ *   ssm_linscan_fwd  scalar selective scan h[t] = a[t] h[t-1] + b[t], h[-1] = 0, per row.
+ *                    Definition: "Selective-scan CUDA kernels", section "The problem";
+ *                    computed as a single-pass decoupled look-back prefix scan under the
+ *                    pair combine (a1,b1).(a2,b2) = (a1 a2, a2 b1 + b2) (same page, "The
+ *                    five kernels", Level 3c).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library never
+ *     allocates, frees or retains them.  Tensors are dense, row-major (C order), with a
+ *     16-byte aligned base address.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  The call returns once the kernels are enqueued.
+ *   - Host-detectable errors return synchronously, before anything is enqueued.  No
+ *     exception crosses the ABI.  Device-side failures of the bounded look-back waits are
+ *     recorded in a status word inside the workspace and reported by
+ *     ssm_check_device_status().
+ *   - Workspace: caller-owned device memory of at least *_workspace_bytes() bytes, 256-byte
+ *     aligned, ZERO-FILLED BEFORE ITS FIRST USE (e.g. cudaMemset).  Every call leaves it
+ *     ready for the next call.  One workspace must not be used by two calls that can run
+ *     concurrently (different streams without ordering).
+ *   - Not thread-safe per workspace; different workspaces may be used from different host
+ *     threads.
+ */
+#ifndef SSM_GB300_H
+#define SSM_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *ssm_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = 1, /* negative size, NULL required pointer, nheads % ngroups != 0 */
+    SSM_ERR_UNSUPPORTED = 2, /* shape outside what the kernels are built for */
+    SSM_ERR_ALIGNMENT = 3,   /* a tensor or workspace base is not aligned as required */
+    SSM_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than *_workspace_bytes() */
+    SSM_ERR_CUDA = 5,        /* a CUDA runtime call failed (launch, attribute, sync) */
+    SSM_ERR_TIMEOUT = 6      /* a bounded look-back wait gave up (device status word) */
+} ssm_status;
+
+typedef enum {
+    SSM_F32 = 0,  /* x, dt, B, C and y are float32 */
+    SSM_BF16 = 1  /* x, dt, B, C and y are bfloat16; accumulation stays float32 */
+} ssm_dtype;
+
+/* Human-readable name of a status code (static storage; never NULL). */
+SSM_API const char *ssm_status_string(ssm_status status);
+
+/* Library version as "major.minor.patch" (static storage). */
+SSM_API const char *ssm_version(void);
+
+/*
+ * Workspace size in bytes for ssm_ssd_fwd with these sizes (0 when any size is invalid or
+ * unsupported; ssm_ssd_fwd reports the reason).  The workspace holds the per-token decay
+ * cumsums, the per-chunk states and the look-back flags of the state-passing scan.
+ */
+SSM_API size_t ssm_ssd_fwd_workspace_bytes(int64_t batch, int64_t seqlen, int nheads, int headdim,
+                                   int dstate, int ngroups, int chunk, ssm_dtype dtype);
+
+/*
+ * Mamba-2 SSD forward (definition above).
+ *
+ * Inputs (element type `dtype` unless marked f32):
+ *   x   [batch, seqlen, nheads, headdim]
+ *   dt  [batch, seqlen, nheads]          time steps, used as given (already positive)
+ *   A   [nheads] f32                     per-head decay rate (A < 0 for a stable state)
+ *   B   [batch, seqlen, ngroups, dstate] input projection; head h reads group
+ *                                        h / (nheads / ngroups)
+ *   C   [batch, seqlen, ngroups, dstate] output projection, same grouping
+ *   D   [nheads] f32                     skip weight
+ *   h0  [batch, nheads, headdim, dstate] f32 initial state, or NULL for zeros
+ * Outputs:
+ *   y        [batch, seqlen, nheads, headdim], element type `dtype`
+ *   h_final  [batch, nheads, headdim, dstate] f32 state after the last token, or NULL
+ *            (not written).  It can be passed back as h0 of a call on the next segment.
+ * Sizes: batch >= 0, seqlen >= 0 (batch == 0 or seqlen == 0 enqueue only the copy of h0
+ *   into h_final), nheads >= 1, ngroups >= 1 dividing nheads, headdim == 64,
+ *   dstate in {64, 128}, chunk in {64, 128, 256}.  seqlen need not be a multiple of chunk
+ *   (the last chunk is zero-padded, which is exact: dt = 0 gives decay 1 and no input).
+ * Errors: SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_ALIGNMENT (any tensor not
+ *   16-byte aligned, workspace not 256-byte aligned), SSM_ERR_WORKSPACE, SSM_ERR_CUDA.
+ */
+SSM_API ssm_status ssm_ssd_fwd(const void *x, const void *dt, const float *A, const void *B, const void *C,
+                       const float *D, const float *h0, void *y, float *h_final,
+                       int64_t batch, int64_t seqlen, int nheads, int headdim, int dstate,
+                       int ngroups, int chunk, ssm_dtype dtype,
+                       void *workspace, size_t workspace_bytes, ssm_stream_t stream);
+
+/* Workspace size in bytes for ssm_linscan_fwd on rows x len (0 when a size is negative). */
+SSM_API size_t ssm_linscan_workspace_bytes(int64_t rows, int64_t len);
+
+/*
+ * Scalar selective scan (definition above), independently on each row.
+ *   a, b  [rows, len] f32 inputs;  h [rows, len] f32 output (may not alias a or b).
+ * rows >= 0, len >= 0 (either 0: nothing is enqueued).  Rows need not be 16-byte aligned
+ * individually (len may be odd); only the base pointers must be.
+ * Errors: SSM_ERR_INVALID_ARG, SSM_ERR_ALIGNMENT, SSM_ERR_WORKSPACE, SSM_ERR_CUDA.
+ */
+SSM_API ssm_status ssm_linscan_fwd(const float *a, const float *b, float *h, int64_t rows, int64_t len,
+                           void *workspace, size_t workspace_bytes, ssm_stream_t stream);
+
+/*
+ * Synchronizes `stream`, reads the device status word at the start of `workspace` (either
+ * kind), clears it, and returns SSM_OK or the recorded device error (SSM_ERR_TIMEOUT when a
+ * look-back wait exceeded its limit; the outputs of that call are then invalid).
+ */
+SSM_API ssm_status ssm_check_device_status(void *workspace, ssm_stream_t stream);
+
+/*
+ * Test hook for the bounded look-back waits (not needed in normal use).  From the next
+ * call on, the look-back tile with claim index `stall_tile` (-1: none) of every look-back
+ * kernel skips publishing its aggregate and prefix, and every wait gives up after
+ * `spin_limit_ns` nanoseconds (0: the default of 1 s).  The waiting tiles then record
+ * SSM_ERR_TIMEOUT in the status word and return; no kernel waits without a limit.
+ */
+SSM_API void ssm_debug_set_lookback_fault(int64_t stall_tile, uint64_t spin_limit_ns);
+
+/*
+ * Kernel timing (measurement aid; not needed in normal use).  Between ssm_profile_begin()
+ * and ssm_profile_end(), every ssm_ssd_fwd / ssm_linscan_fwd call records a CUDA event on its
+ * own stream before and after each kernel it launches (at most `max_launches` launches are
+ * recorded; later ones are counted but not timed).  ssm_profile_end() synchronizes the
+ * recorded events and writes, for each kernel id below, the summed device time in
+ * milliseconds and the number of launches (arrays of length SSM_PROFILE_KERNELS).
+ * Kernel ids: 0 linscan_lookback, 1 ssd_chunk_cumsum, 2 ssd_chunk_state,
+ * 3 ssd_state_passing, 4 ssd_chunk_scan.  Host-side only; process-global; not thread-safe.
+ */
+#define SSM_PROFILE_KERNELS 5
+SSM_API ssm_status ssm_profile_begin(int max_launches);
+SSM_API ssm_status ssm_profile_end(double *ms_out, int64_t *launches_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSM_GB300_H */

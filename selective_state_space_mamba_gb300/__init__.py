@@ -1,0 +1,214 @@
+"""GB300 (sm_103a) selective state-space forward: Mamba-2 chunked SSD and the scalar scan.
+
+Python entry points with the names of the C ABI (include/ssm.h).  They only marshal torch
+CUDA tensors into the C calls; every step of the computation runs in the library's CUDA
+kernels, enqueued on the current torch stream.  PyTorch supplies device memory and streams.
+
+    y, h_final = ssd_fwd(x, dt, A, B, C, D, h0=None, chunk=256)
+    h = linscan_fwd(a, b)
+
+Importing the package does not load the library; the first call does (and fails loudly if
+it cannot).
+"""
+from __future__ import annotations
+
+from . import _lib
+from ._lib import SSM_BF16, SSM_F32, SsmError
+
+__all__ = ["ssd_fwd", "linscan_fwd", "Workspace", "check_device_status", "ssd_fwd_workspace_bytes",
+           "linscan_workspace_bytes", "SsmError", "version"]
+
+
+def version() -> str:
+    return _lib.load().ssm_version().decode()
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return SSM_F32
+    if t.dtype == torch.bfloat16:
+        return SSM_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _stream_ptr(device):
+    torch = _torch()
+    return ctypes_void(torch.cuda.current_stream(device).cuda_stream)
+
+
+def ctypes_void(v):
+    import ctypes
+    return ctypes.c_void_p(v) if v else None
+
+
+def _ptr(t):
+    return ctypes_void(t.data_ptr()) if t is not None else None
+
+
+class Workspace:
+    """Zero-initialised device scratch buffer for the C calls, grown on demand.
+
+    The library leaves a workspace ready for reuse after every call.  One Workspace must not
+    serve two calls that can run concurrently on different streams.
+    """
+
+    def __init__(self, device=None, nbytes: int = 0):
+        torch = _torch()
+        self.device = torch.device(device if device is not None else "cuda")
+        self.buf = None
+        if nbytes:
+            self.ensure(nbytes)
+
+    def ensure(self, nbytes: int):
+        torch = _torch()
+        if self.buf is None or self.buf.numel() < nbytes:
+            # round up so that small growth does not reallocate every call
+            n = max(int(nbytes), 1 << 20)
+            self.buf = torch.zeros(n, dtype=torch.uint8, device=self.device)
+        return self.buf
+
+    @property
+    def nbytes(self) -> int:
+        return 0 if self.buf is None else self.buf.numel()
+
+    def ptr(self):
+        return _ptr(self.buf)
+
+
+_default_ws = {}
+
+
+def _workspace(kind: str, device, nbytes: int) -> Workspace:
+    torch = _torch()
+    key = (kind, torch.device(device).index)
+    ws = _default_ws.get(key)
+    if ws is None:
+        ws = _default_ws[key] = Workspace(device)
+    ws.ensure(nbytes)
+    return ws
+
+
+def ssd_fwd_workspace_bytes(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype_code) -> int:
+    return int(_lib.load().ssm_ssd_fwd_workspace_bytes(batch, seqlen, nheads, headdim, dstate, ngroups, chunk,
+                                                       dtype_code))
+
+
+def linscan_workspace_bytes(rows, length) -> int:
+    return int(_lib.load().ssm_linscan_workspace_bytes(rows, length))
+
+
+def _require(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def ssd_fwd(x, dt, A, B, C, D, h0=None, chunk: int = 256, *, y=None, h_final=None, return_final_state=True,
+            workspace: Workspace | None = None):
+    """Mamba-2 chunked SSD forward on one GPU (see include/ssm.h, ssm_ssd_fwd).
+
+    x [b, L, nh, H], dt [b, L, nh], B/C [b, L, G, S] (all float32 or all bfloat16);
+    A, D [nh] float32; h0 [b, nh, H, S] float32 or None.  Returns (y, h_final) with y like x
+    and h_final float32 [b, nh, H, S] (None when return_final_state is False).
+    """
+    torch = _torch()
+    lib = _lib.load()
+    code = _dtype_code(x)
+    _require(x.dim() == 4 and dt.dim() == 3 and B.dim() == 4 and C.dim() == 4, "bad ranks")
+    b, L, nh, H = x.shape
+    G, S = B.shape[2], B.shape[3]
+    _require(tuple(dt.shape) == (b, L, nh), "dt must be [b, L, nh]")
+    _require(tuple(B.shape) == (b, L, G, S) and tuple(C.shape) == (b, L, G, S), "B, C must be [b, L, G, S]")
+    _require(tuple(A.shape) == (nh,) and tuple(D.shape) == (nh,), "A, D must be [nh]")
+    for name, t in (("dt", dt), ("B", B), ("C", C)):
+        _require(t.dtype == x.dtype, f"{name} must have x's dtype")
+    _require(A.dtype == torch.float32 and D.dtype == torch.float32, "A, D must be float32")
+    ts = [x, dt, A, B, C, D] + ([h0] if h0 is not None else [])
+    for t in ts:
+        _require(t.is_cuda and t.is_contiguous(), "all tensors must be contiguous CUDA tensors")
+    if h0 is not None:
+        _require(tuple(h0.shape) == (b, nh, H, S) and h0.dtype == torch.float32, "h0 must be f32 [b, nh, H, S]")
+    if y is None:
+        y = torch.empty_like(x)
+    if return_final_state and h_final is None:
+        h_final = torch.empty((b, nh, H, S), dtype=torch.float32, device=x.device)
+    if not return_final_state:
+        h_final = None
+    need = lib.ssm_ssd_fwd_workspace_bytes(b, L, nh, H, S, G, chunk, code)
+    ws = workspace if workspace is not None else _workspace("ssd", x.device, max(need, 1))
+    if workspace is not None:
+        ws.ensure(need)
+    st = lib.ssm_ssd_fwd(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(h0), _ptr(y),
+                         _ptr(h_final), b, L, nh, H, S, G, chunk, code, ws.ptr(), ws.nbytes, _stream_ptr(x.device))
+    _lib.check(st, "ssm_ssd_fwd")
+    return y, h_final
+
+
+def linscan_fwd(a, b, *, h=None, workspace: Workspace | None = None):
+    """Scalar selective scan h[t] = a[t] h[t-1] + b[t] per row of [rows, L] float32 tensors."""
+    torch = _torch()
+    lib = _lib.load()
+    _require(a.shape == b.shape and a.dim() == 2, "a, b must be [rows, L] and equal")
+    _require(a.dtype == torch.float32 and b.dtype == torch.float32, "a, b must be float32")
+    _require(a.is_cuda and b.is_cuda and a.is_contiguous() and b.is_contiguous(), "contiguous CUDA tensors")
+    rows, L = a.shape
+    if h is None:
+        h = torch.empty_like(a)
+    need = lib.ssm_linscan_workspace_bytes(rows, L)
+    ws = workspace if workspace is not None else _workspace("linscan", a.device, max(need, 1))
+    if workspace is not None:
+        ws.ensure(need)
+    st = lib.ssm_linscan_fwd(_ptr(a), _ptr(b), _ptr(h), rows, L, ws.ptr(), ws.nbytes, _stream_ptr(a.device))
+    _lib.check(st, "ssm_linscan_fwd")
+    return h
+
+
+def check_device_status(workspace: Workspace | None = None, kind: str = "ssd", device=None) -> int:
+    """Synchronise and return (and clear) the device status word of a workspace (0 = OK)."""
+    torch = _torch()
+    lib = _lib.load()
+    if workspace is None:
+        dev = torch.device(device if device is not None else "cuda")
+        workspace = _default_ws.get((kind, dev.index if dev.index is not None else torch.cuda.current_device()))
+        if workspace is None:
+            return 0
+    return int(lib.ssm_check_device_status(workspace.ptr(), _stream_ptr(workspace.device)))
+
+
+def debug_set_lookback_fault(stall_tile: int = -1, spin_limit_ns: int = 0) -> None:
+    """Test hook: see ssm_debug_set_lookback_fault in include/ssm.h."""
+    _lib.load().ssm_debug_set_lookback_fault(int(stall_tile), int(spin_limit_ns))
+
+
+class KernelTimer:
+    """Per-kernel device times of the library's launches inside a ``with`` block.
+
+    Uses the library's own CUDA events, recorded on the stream of each launch
+    (ssm_profile_begin / ssm_profile_end in include/ssm.h).  After the block, ``ms`` maps kernel
+    name -> summed milliseconds and ``launches`` kernel name -> launch count.
+    """
+
+    def __init__(self, max_launches: int = 4096):
+        self.max_launches = max_launches
+        self.ms = {}
+        self.launches = {}
+
+    def __enter__(self):
+        _lib.check(_lib.load().ssm_profile_begin(self.max_launches), "ssm_profile_begin")
+        return self
+
+    def __exit__(self, *exc):
+        import ctypes
+        n = len(_lib.PROFILE_KERNELS)
+        ms = (ctypes.c_double * n)()
+        cnt = (ctypes.c_int64 * n)()
+        _lib.check(_lib.load().ssm_profile_end(ctypes.cast(ms, ctypes.c_void_p), ctypes.cast(cnt, ctypes.c_void_p)),
+                   "ssm_profile_end")
+        self.ms = {k: float(ms[i]) for i, k in enumerate(_lib.PROFILE_KERNELS)}
+        self.launches = {k: int(cnt[i]) for i, k in enumerate(_lib.PROFILE_KERNELS)}
+        return False

@@ -1,0 +1,321 @@
+// Host side of the C ABI declared in include/ssm.h: argument validation, workspace layout,
+// and the launch sequence of each operation on the caller's stream.
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "ssm_internal.cuh"
+
+namespace ssm {
+
+cudaError_t launch_ssd_chunk_state_simt(const void* x, const void* B, const SsdDims& d, const SsdWorkspace& ws,
+                                        cudaStream_t s);
+cudaError_t launch_ssd_chunk_scan_simt(const void* x, const void* B, const void* C, const float* D, void* y,
+                                       const SsdDims& d, const SsdWorkspace& ws, cudaStream_t s);
+bool ssd_tc_supported(const SsdDims& d);
+cudaError_t launch_ssd_chunk_state_tc(const void* x, const void* B, const SsdDims& d, const SsdWorkspace& ws,
+                                      cudaStream_t s);
+cudaError_t launch_ssd_chunk_scan_tc(const void* x, const void* B, const void* C, const float* D, void* y,
+                                     const SsdDims& d, const SsdWorkspace& ws, cudaStream_t s);
+
+namespace {
+
+std::atomic<uint32_t> g_epoch{0};
+std::atomic<int64_t> g_stall_tile{-1};
+std::atomic<uint64_t> g_spin_limit_ns{0};
+constexpr uint64_t kDefaultSpinLimitNs = 1000000000ull;  // 1 s per wait
+
+// ---- optional per-kernel timing (ssm_profile_begin / ssm_profile_end) ----
+struct ProfRecord {
+  int kernel;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+int g_prof_max = 0;
+std::vector<ProfRecord> g_prof_records;
+std::vector<cudaEvent_t> g_prof_pool;
+int64_t g_prof_counts[SSM_PROFILE_KERNELS] = {0};
+
+// Wraps one launch: records events around it on `s` while profiling is enabled.
+template <typename F>
+cudaError_t timed_launch(int kernel, cudaStream_t s, F&& launch) {
+  ProfRecord rec{kernel, nullptr, nullptr};
+  bool timed = false;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (g_prof_on) {
+      g_prof_counts[kernel]++;
+      if ((int)g_prof_records.size() < g_prof_max && g_prof_pool.size() >= 2) {
+        rec.start = g_prof_pool.back();
+        g_prof_pool.pop_back();
+        rec.stop = g_prof_pool.back();
+        g_prof_pool.pop_back();
+        timed = true;
+      }
+    }
+  }
+  if (timed && cudaEventRecord(rec.start, s) != cudaSuccess) return cudaErrorUnknown;
+  const cudaError_t e = launch();
+  if (timed) {
+    if (cudaEventRecord(rec.stop, s) != cudaSuccess) return cudaErrorUnknown;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof_records.push_back(rec);
+  }
+  return e;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+ssm_status check_ssd_dims(int64_t batch, int64_t seqlen, int nheads, int headdim, int dstate, int ngroups,
+                          int chunk, ssm_dtype dtype) {
+  if (batch < 0 || seqlen < 0 || nheads < 1 || headdim < 1 || dstate < 1 || ngroups < 1 || chunk < 1)
+    return SSM_ERR_INVALID_ARG;
+  if (nheads % ngroups != 0) return SSM_ERR_INVALID_ARG;
+  if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
+  if (headdim != 64) return SSM_ERR_UNSUPPORTED;
+  if (dstate != 64 && dstate != 128) return SSM_ERR_UNSUPPORTED;
+  if (chunk != 64 && chunk != 128 && chunk != 256) return SSM_ERR_UNSUPPORTED;
+  // grid limits: chunks and batch go to grid.x / grid.z of some kernels
+  const int64_t nchunks = (seqlen + chunk - 1) / chunk;
+  if (nchunks * (chunk / 64) > 0x7fffffffLL || batch > 65535 || nheads > 65535) return SSM_ERR_UNSUPPORTED;
+  return SSM_OK;
+}
+
+SsdDims make_dims(int64_t batch, int64_t seqlen, int nheads, int headdim, int dstate, int ngroups, int chunk,
+                  ssm_dtype dtype) {
+  SsdDims d;
+  d.batch = batch;
+  d.seqlen = seqlen;
+  d.nheads = nheads;
+  d.headdim = headdim;
+  d.dstate = dstate;
+  d.ngroups = ngroups;
+  d.chunk = chunk;
+  d.nchunks = (seqlen + chunk - 1) / chunk;
+  d.lpad = d.nchunks * chunk;
+  d.dtype = dtype;
+  return d;
+}
+
+}  // namespace
+
+LookbackCtl next_lookback_ctl() {
+  LookbackCtl c;
+  uint32_t e;
+  do {
+    e = (g_epoch.fetch_add(1, std::memory_order_relaxed) + 1) & 0x3fffffffu;
+  } while (e == 0);
+  c.epoch = e;
+  c.stall_tile = g_stall_tile.load(std::memory_order_relaxed);
+  const uint64_t lim = g_spin_limit_ns.load(std::memory_order_relaxed);
+  c.spin_limit_ns = lim ? lim : kDefaultSpinLimitNs;
+  return c;
+}
+
+SsdWorkspace ssd_workspace_layout(const SsdDims& d, void* base) {
+  SsdWorkspace w{};
+  char* p = static_cast<char*>(base);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char* r = p ? p + off : nullptr;
+    off = align_up(off + bytes, 256);
+    return r;
+  };
+  const int64_t bh = d.batch * d.nheads;
+  const int64_t HS = (int64_t)d.headdim * d.dstate;
+  const size_t hin_elem = d.dtype == SSM_BF16 ? 2 : 4;
+  w.sp_chains = bh * (HS / kSpElems);
+  w.sp_ctiles = (d.nchunks + kSpChunks - 1) / kSpChunks;
+  w.sp_tiles = w.sp_chains * w.sp_ctiles;
+  w.hdr = reinterpret_cast<WsHeader*>(take(kHeaderBytes));
+  w.flags = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * w.sp_tiles));
+  w.G = reinterpret_cast<float*>(take(sizeof(float) * bh * d.lpad));
+  w.dtT = reinterpret_cast<float*>(take(sizeof(float) * bh * d.lpad));
+  w.Sc = reinterpret_cast<float*>(take(sizeof(float) * d.batch * d.nchunks * d.nheads * HS));
+  w.hin = take(hin_elem * d.batch * d.nchunks * d.nheads * HS);
+  w.agg = reinterpret_cast<float*>(take(sizeof(float) * w.sp_tiles * kSpElems));
+  w.inc = reinterpret_cast<float*>(take(sizeof(float) * w.sp_tiles * kSpElems));
+  w.total_bytes = off;
+  return w;
+}
+
+LinscanWorkspace linscan_workspace_layout(int64_t n, void* base) {
+  LinscanWorkspace w{};
+  char* p = static_cast<char*>(base);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char* r = p ? p + off : nullptr;
+    off = align_up(off + bytes, 256);
+    return r;
+  };
+  w.tiles = (n + kLsTile - 1) / kLsTile;
+  w.hdr = reinterpret_cast<WsHeader*>(take(kHeaderBytes));
+  w.flags = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * w.tiles));
+  w.agg = reinterpret_cast<float2*>(take(sizeof(float2) * w.tiles));
+  w.inc = reinterpret_cast<float2*>(take(sizeof(float2) * w.tiles));
+  w.total_bytes = off;
+  return w;
+}
+
+}  // namespace ssm
+
+using namespace ssm;
+
+extern "C" {
+
+const char* ssm_status_string(ssm_status status) {
+  switch (status) {
+    case SSM_OK: return "SSM_OK";
+    case SSM_ERR_INVALID_ARG: return "SSM_ERR_INVALID_ARG: invalid argument";
+    case SSM_ERR_UNSUPPORTED: return "SSM_ERR_UNSUPPORTED: shape not supported by the kernels";
+    case SSM_ERR_ALIGNMENT: return "SSM_ERR_ALIGNMENT: pointer not aligned as required";
+    case SSM_ERR_WORKSPACE: return "SSM_ERR_WORKSPACE: workspace missing or too small";
+    case SSM_ERR_CUDA: return "SSM_ERR_CUDA: CUDA runtime error";
+    case SSM_ERR_TIMEOUT: return "SSM_ERR_TIMEOUT: a look-back wait exceeded its limit";
+  }
+  return "unknown ssm_status";
+}
+
+const char* ssm_version(void) { return "0.1.0"; }
+
+size_t ssm_ssd_fwd_workspace_bytes(int64_t batch, int64_t seqlen, int nheads, int headdim, int dstate, int ngroups,
+                                   int chunk, ssm_dtype dtype) {
+  if (check_ssd_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype) != SSM_OK) return 0;
+  return ssd_workspace_layout(make_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype), nullptr)
+      .total_bytes;
+}
+
+ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void* B, const void* C, const float* D,
+                       const float* h0, void* y, float* h_final, int64_t batch, int64_t seqlen, int nheads,
+                       int headdim, int dstate, int ngroups, int chunk, ssm_dtype dtype, void* workspace,
+                       size_t workspace_bytes, ssm_stream_t stream) {
+  ssm_status st = check_ssd_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype);
+  if (st != SSM_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const SsdDims d = make_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype);
+  const size_t state_bytes = sizeof(float) * (size_t)batch * nheads * headdim * dstate;
+  if (batch == 0 || seqlen == 0) {
+    // no tokens: y is empty and the final state is the initial state
+    if (h_final && state_bytes) {
+      if (h0 && !aligned(h0, 16)) return SSM_ERR_ALIGNMENT;
+      cudaError_t e = h0 ? cudaMemcpyAsync(h_final, h0, state_bytes, cudaMemcpyDeviceToDevice, s)
+                         : cudaMemsetAsync(h_final, 0, state_bytes, s);
+      if (e != cudaSuccess) return SSM_ERR_CUDA;
+    }
+    return SSM_OK;
+  }
+  if (!x || !dt || !A || !B || !C || !D || !y) return SSM_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, dt, A, B, C, D, y};
+  for (const void* p : ptrs)
+    if (!aligned(p, 16)) return SSM_ERR_ALIGNMENT;
+  if ((h0 && !aligned(h0, 16)) || (h_final && !aligned(h_final, 16))) return SSM_ERR_ALIGNMENT;
+  const SsdWorkspace need = ssd_workspace_layout(d, nullptr);
+  if (!workspace || workspace_bytes < need.total_bytes) return SSM_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return SSM_ERR_ALIGNMENT;
+  const SsdWorkspace ws = ssd_workspace_layout(d, workspace);
+  const LookbackCtl ctl = next_lookback_ctl();
+
+  const bool tc = ssd_tc_supported(d);
+  if (timed_launch(1, s, [&] { return launch_ssd_chunk_cumsum(dt, A, d, ws, s); }) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  if (timed_launch(2, s, [&] {
+        return tc ? launch_ssd_chunk_state_tc(x, B, d, ws, s) : launch_ssd_chunk_state_simt(x, B, d, ws, s);
+      }) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  if (timed_launch(3, s, [&] { return launch_ssd_state_passing(h0, h_final, d, ws, ctl, s); }) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  if (timed_launch(4, s, [&] {
+        return tc ? launch_ssd_chunk_scan_tc(x, B, C, D, y, d, ws, s)
+                  : launch_ssd_chunk_scan_simt(x, B, C, D, y, d, ws, s);
+      }) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  return SSM_OK;
+}
+
+size_t ssm_linscan_workspace_bytes(int64_t rows, int64_t len) {
+  if (rows < 0 || len < 0) return 0;
+  return linscan_workspace_layout(rows * len, nullptr).total_bytes;
+}
+
+ssm_status ssm_linscan_fwd(const float* a, const float* b, float* h, int64_t rows, int64_t len, void* workspace,
+                           size_t workspace_bytes, ssm_stream_t stream) {
+  if (rows < 0 || len < 0) return SSM_ERR_INVALID_ARG;
+  if (rows == 0 || len == 0) return SSM_OK;
+  if (!a || !b || !h) return SSM_ERR_INVALID_ARG;
+  if (!aligned(a, 16) || !aligned(b, 16) || !aligned(h, 16)) return SSM_ERR_ALIGNMENT;
+  const int64_t n = rows * len;
+  if (n / len != rows) return SSM_ERR_INVALID_ARG;
+  const LinscanWorkspace need = linscan_workspace_layout(n, nullptr);
+  if (need.tiles > 0x7fffffffLL) return SSM_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < need.total_bytes) return SSM_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return SSM_ERR_ALIGNMENT;
+  const LinscanWorkspace ws = linscan_workspace_layout(n, workspace);
+  const LookbackCtl ctl = next_lookback_ctl();
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (timed_launch(0, s, [&] { return launch_linscan(a, b, h, rows, len, ws, ctl, s); }) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  return SSM_OK;
+}
+
+ssm_status ssm_check_device_status(void* workspace, ssm_stream_t stream) {
+  if (!workspace) return SSM_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SSM_ERR_CUDA;
+  unsigned long long word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return SSM_ERR_CUDA;
+  if (word == 0) return SSM_OK;
+  const unsigned long long zero = 0;
+  if (cudaMemcpy(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SSM_ERR_CUDA;
+  const uint32_t code = (uint32_t)(word & 0xffffffffu);
+  return code == 0 ? SSM_ERR_CUDA : static_cast<ssm_status>(code);
+}
+
+ssm_status ssm_profile_begin(int max_launches) {
+  if (max_launches < 0) return SSM_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (auto& r : g_prof_records) {
+    g_prof_pool.push_back(r.start);
+    g_prof_pool.push_back(r.stop);
+  }
+  g_prof_records.clear();
+  while ((int)g_prof_pool.size() < 2 * max_launches) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return SSM_ERR_CUDA;
+    g_prof_pool.push_back(e);
+  }
+  for (auto& c : g_prof_counts) c = 0;
+  g_prof_max = max_launches;
+  g_prof_on = true;
+  return SSM_OK;
+}
+
+ssm_status ssm_profile_end(double* ms_out, int64_t* launches_out) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = false;
+  double ms[SSM_PROFILE_KERNELS] = {0};
+  ssm_status st = SSM_OK;
+  for (auto& r : g_prof_records) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess)
+      st = SSM_ERR_CUDA;
+    ms[r.kernel] += t;
+    g_prof_pool.push_back(r.start);
+    g_prof_pool.push_back(r.stop);
+  }
+  g_prof_records.clear();
+  for (int k = 0; k < SSM_PROFILE_KERNELS; ++k) {
+    if (ms_out) ms_out[k] = ms[k];
+    if (launches_out) launches_out[k] = g_prof_counts[k];
+  }
+  return st;
+}
+
+void ssm_debug_set_lookback_fault(int64_t stall_tile, uint64_t spin_limit_ns) {
+  g_stall_tile.store(stall_tile < 0 ? -1 : stall_tile, std::memory_order_relaxed);
+  g_spin_limit_ns.store(spin_limit_ns, std::memory_order_relaxed);
+}
+
+}  // extern "C"

@@ -1,0 +1,97 @@
+// ssd_chunk_cumsum: per-chunk inclusive cumulative sums of a_t = A[h] dt[b,t,h], scaled by
+// log2(e) so that every later decay is an exp2 ("Accelerating Mamba-2 with High-Performance
+// Forward Pass Kernels in NVIDIA CUDA Tile", "Kernel 1: Computing cumulative sums").  The
+// decay matrix of a chunk is then L[i,j] = exp(sum_{k=j+1..i} a_k) = 2^(G_i - G_j), j <= i.
+//
+// Output layout is [batch, head, token] (the post's "GMEM layout" optimisation): the later
+// kernels read one head's G and dt as contiguous runs.  dt is written out transposed as f32
+// at the same time, with 0 in the padding of the last chunk (decay 1, no input: exact).
+//
+// One CTA per (chunk, block of 32 heads, batch): the dt tile [chunk, 32 heads] is staged
+// through shared memory so both the read (heads contiguous) and the write (tokens
+// contiguous) are coalesced; each warp then scans whole head rows.
+#include "ssm_internal.cuh"
+
+namespace ssm {
+namespace {
+
+constexpr int kCsHeads = 32;
+constexpr int kCsThreads = 256;
+
+template <typename DtT>
+__global__ void __launch_bounds__(kCsThreads) ssd_chunk_cumsum_kernel(const DtT* __restrict__ dt,
+                                                                       const float* __restrict__ A, SsdDims d,
+                                                                       float* __restrict__ G, float* __restrict__ dtT,
+                                                                       WsHeader* hdr) {
+  extern __shared__ float s_dt[];  // [chunk][kCsHeads + 1]
+  const int c = blockIdx.x, hblk = blockIdx.y;
+  const int64_t bi = blockIdx.z;
+  const int T = d.chunk, nh = d.nheads;
+  const int h0 = hblk * kCsHeads;
+  const int nhb = min(kCsHeads, nh - h0);
+  const int64_t t0 = (int64_t)c * T;
+
+  if (c == 0 && hblk == 0 && bi == 0 && threadIdx.x == 0) {
+    // the state-passing kernel runs after this one on the same stream: start its claims at 0
+    hdr->counter = 0u;
+    hdr->done = 0u;
+  }
+
+  for (int idx = threadIdx.x; idx < T * kCsHeads; idx += kCsThreads) {
+    const int t = idx / kCsHeads, hh = idx % kCsHeads;
+    float v = 0.f;
+    if (hh < nhb && t0 + t < d.seqlen) v = to_f32(dt[((bi * d.seqlen) + t0 + t) * nh + h0 + hh]);
+    s_dt[t * (kCsHeads + 1) + hh] = v;
+  }
+  __syncthreads();
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per_lane = T / 32;  // chunk is a multiple of 64
+  for (int hh = warp; hh < nhb; hh += kCsThreads / 32) {
+    const float Ah = A[h0 + hh];
+    float run = 0.f;
+    float vals[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k < per_lane) {
+        run += Ah * s_dt[(lane * per_lane + k) * (kCsHeads + 1) + hh];
+        vals[k] = run;
+      }
+    }
+    // exclusive prefix of the lane totals
+    float incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    const float excl = incl - run;
+    const int64_t row = (bi * nh + h0 + hh) * d.lpad + t0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k < per_lane) {
+        const int t = lane * per_lane + k;
+        G[row + t] = (excl + vals[k]) * kLog2e;
+        dtT[row + t] = s_dt[t * (kCsHeads + 1) + hh];
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_ssd_chunk_cumsum(const void* dt, const float* A, const SsdDims& d, const SsdWorkspace& ws,
+                                    cudaStream_t s) {
+  dim3 grid((unsigned)d.nchunks, (unsigned)((d.nheads + kCsHeads - 1) / kCsHeads), (unsigned)d.batch);
+  const size_t smem = sizeof(float) * d.chunk * (kCsHeads + 1);
+  if (d.dtype == SSM_BF16) {
+    ssd_chunk_cumsum_kernel<__nv_bfloat16><<<grid, kCsThreads, smem, s>>>(
+        static_cast<const __nv_bfloat16*>(dt), A, d, ws.G, ws.dtT, ws.hdr);
+  } else {
+    ssd_chunk_cumsum_kernel<float><<<grid, kCsThreads, smem, s>>>(static_cast<const float*>(dt), A, d, ws.G,
+                                                                   ws.dtT, ws.hdr);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace ssm

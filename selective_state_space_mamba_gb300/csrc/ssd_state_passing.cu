@@ -1,0 +1,196 @@
+// ssd_state_passing: the inter-chunk scan of the Mamba-2 SSD forward.
+//
+// With S_c the state increment of chunk c (computed in parallel by ssd_chunk_state) and
+// d_c = exp(sum of a over chunk c) = 2^(G_last of chunk c), the chunk-initial states are
+//     h_in[0] = h0,   h_in[c+1] = d_c h_in[c] + S_c,   h_final = h_in[nchunks]
+// ("Accelerating Mamba-2 with High-Performance Forward Pass Kernels in NVIDIA CUDA Tile",
+// "Kernel 2: fwd_pass_state": the jump h_{t+T} = exp(G_last) h_t + X^T(exp(G_last - G) B),
+// whose chunk loop runs sequentially inside one program there).
+//
+// Here the loop over chunks is a scan under the same affine pair combine as the scalar scan
+// ("Selective-scan CUDA kernels", "The problem"), run as a decoupled look-back: each tile is
+// kSpElems state entries of one (batch, head) across up to kSpChunks chunks.  A tile
+// publishes its aggregate state vector (flag A), looks back over predecessor tiles of the
+// same chain (a warp inspects 32 flags at once, atomic claim order guarantees progress),
+// publishes its inclusive state (flag P), then writes h_in for each of its chunks.  The
+// decay of an aggregate is not published: every tile recomputes it from G.
+#include "ssm_internal.cuh"
+
+namespace ssm {
+namespace {
+
+__device__ __forceinline__ float4 f4_fma(float s, float4 x, float4 y) {
+  return make_float4(fmaf(s, x.x, y.x), fmaf(s, x.y, y.y), fmaf(s, x.z, y.z), fmaf(s, x.w, y.w));
+}
+
+template <typename T> __device__ __forceinline__ void store4(T* p, float4 v);
+template <> __device__ __forceinline__ void store4<float>(float* p, float4 v) {
+  *reinterpret_cast<float4*>(p) = v;
+}
+template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
+  __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&lo);
+  u.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+template <typename HinT>
+__global__ void __launch_bounds__(kSpThreads) ssd_state_passing_kernel(const float* __restrict__ h0,
+                                                                        float* __restrict__ h_final, SsdDims d,
+                                                                        SsdWorkspace ws, LookbackCtl ctl) {
+  __shared__ uint32_t s_tile;
+  __shared__ int s_last, s_found;
+
+  if (threadIdx.x == 0) s_tile = claim_tile(ws.hdr);
+  __syncthreads();
+  const int64_t tile = s_tile;
+  if (tile >= ws.sp_tiles) {  // claim counter not reset: refuse rather than index past the workspace
+    if (threadIdx.x == 0) {
+      record_error(ws.hdr, ctl.epoch, SSM_ERR_WORKSPACE);
+      retire_tile(ws.hdr, (uint32_t)ws.sp_tiles);
+    }
+    return;
+  }
+  const int64_t chain = tile % ws.sp_chains;
+  const int64_t ctile = tile / ws.sp_chains;
+  const int HS = d.headdim * d.dstate;
+  const int nslices = HS / kSpElems;
+  const int64_t bh = chain / nslices;  // bi * nheads + h
+  const int slice = (int)(chain % nslices);
+  const int64_t bi = bh / d.nheads;
+  const int h = (int)(bh % d.nheads);
+  const int64_t nc = d.nchunks;
+  const int64_t c0 = ctile * kSpChunks;
+  const int nk = (int)(nc - c0 < kSpChunks ? nc - c0 : kSpChunks);
+  const int e = slice * kSpElems + threadIdx.x * 4;
+  const float* Grow = ws.G + bh * d.lpad + (d.chunk - 1);  // G_last of chunk c at Grow[c * chunk]
+
+  // ---- load this tile's chunk increments and decays ----
+  float4 sc[kSpChunks];
+  float lg[kSpChunks];
+#pragma unroll
+  for (int k = 0; k < kSpChunks; ++k) {
+    if (k < nk) {
+      const int64_t c = c0 + k;
+      sc[k] = __ldcs(reinterpret_cast<const float4*>(ws.Sc + ((bi * nc + c) * d.nheads + h) * HS + e));
+      lg[k] = Grow[c * d.chunk];
+    }
+  }
+  float4 agg = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lg_tile = 0.f;
+#pragma unroll
+  for (int k = 0; k < kSpChunks; ++k) {
+    if (k < nk) {
+      agg = f4_fma(exp2f(lg[k]), agg, sc[k]);
+      lg_tile += lg[k];
+    }
+  }
+
+  const bool stalled = (int64_t)tile == ctl.stall_tile;
+  float* my_agg = ws.agg + tile * kSpElems + threadIdx.x * 4;
+  float* my_inc = ws.inc + tile * kSpElems + threadIdx.x * 4;
+  float4 X;  // state entering the tile's first chunk
+  if (ctile == 0) {
+    X = h0 ? *reinterpret_cast<const float4*>(h0 + bh * HS + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!stalled) {
+      *reinterpret_cast<float4*>(my_inc) = f4_fma(exp2f(lg_tile), X, agg);
+      __threadfence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !stalled) st_release_u64(&ws.flags[tile], make_flag(ctl.epoch, kFlagPrefix));
+  } else {
+    if (!stalled) {
+      *reinterpret_cast<float4*>(my_agg) = agg;
+      __threadfence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !stalled) st_release_u64(&ws.flags[tile], make_flag(ctl.epoch, kFlagAggregate));
+
+    // ---- look-back: compose predecessors newest to oldest until a published prefix ----
+    float4 acc_b = make_float4(0.f, 0.f, 0.f, 0.f);  // map h -> 2^acc_lg h + acc_b
+    float acc_lg = 0.f;
+    int64_t newest = ctile - 1;
+    while (true) {
+      if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const int64_t ct = newest - lane;
+        uint32_t kind = kFlagPrefix;
+        if (ct >= 0) {
+          kind = wait_flag(&ws.flags[ct * ws.sp_chains + chain], ws.hdr, ctl);
+          if (kind == 0) kind = 3;  // gave up: use as a (poisoned) prefix
+        }
+        const unsigned pmask = __ballot_sync(0xffffffffu, kind != kFlagAggregate);
+        const int last = pmask ? (__ffs(pmask) - 1) : 31;  // lanes 0..last are composed
+        const uint32_t kind_last = __shfl_sync(0xffffffffu, kind, last);
+        if (lane == 0) {
+          s_last = last;
+          s_found = pmask ? (int)kind_last : 0;
+        }
+      }
+      __syncthreads();
+      const int last = s_last;
+      const int found = s_found;  // 0: all 32 were aggregates, 2: prefix, 3: gave up
+      __threadfence();
+      for (int l = 0; l <= last; ++l) {
+        const int64_t ct = newest - l;
+        const int64_t t = ct * ws.sp_chains + chain;
+        if (l == last && found != 0) {
+          float4 v;
+          if (found == kFlagPrefix) {
+            v = ld_relaxed_f4(reinterpret_cast<const float4*>(ws.inc + t * kSpElems + threadIdx.x * 4));
+          } else {
+            const float nan = __int_as_float(0x7fc00000);
+            v = make_float4(nan, nan, nan, nan);
+          }
+          acc_b = f4_fma(exp2f(acc_lg), v, acc_b);
+        } else {
+          const float4 v = ld_relaxed_f4(reinterpret_cast<const float4*>(ws.agg + t * kSpElems + threadIdx.x * 4));
+          acc_b = f4_fma(exp2f(acc_lg), v, acc_b);
+          float lq = 0.f;
+          const int64_t cb = ct * kSpChunks;
+          const int nq = (int)(nc - cb < kSpChunks ? nc - cb : kSpChunks);
+          for (int k = 0; k < nq; ++k) lq += Grow[(cb + k) * d.chunk];
+          acc_lg += lq;
+        }
+      }
+      if (found != 0) break;
+      newest -= 32;
+      __syncthreads();  // warp 0 rewrites s_last / s_found
+    }
+    X = acc_b;
+    if (!stalled) {
+      *reinterpret_cast<float4*>(my_inc) = f4_fma(exp2f(lg_tile), X, agg);
+      __threadfence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !stalled) st_release_u64(&ws.flags[tile], make_flag(ctl.epoch, kFlagPrefix));
+  }
+
+  // ---- chunk-initial states of this tile, then the final state ----
+  HinT* hin = static_cast<HinT*>(ws.hin);
+#pragma unroll
+  for (int k = 0; k < kSpChunks; ++k) {
+    if (k < nk) {
+      const int64_t c = c0 + k;
+      store4<HinT>(hin + ((bi * nc + c) * d.nheads + h) * HS + e, X);
+      X = f4_fma(exp2f(lg[k]), X, sc[k]);
+    }
+  }
+  if (h_final && c0 + nk == nc) *reinterpret_cast<float4*>(h_final + bh * HS + e) = X;
+  if (threadIdx.x == 0) retire_tile(ws.hdr, (uint32_t)ws.sp_tiles);
+}
+
+}  // namespace
+
+cudaError_t launch_ssd_state_passing(const float* h0, float* h_final, const SsdDims& d, const SsdWorkspace& ws,
+                                     const LookbackCtl& ctl, cudaStream_t s) {
+  if (d.dtype == SSM_BF16) {
+    ssd_state_passing_kernel<__nv_bfloat16><<<(unsigned)ws.sp_tiles, kSpThreads, 0, s>>>(h0, h_final, d, ws, ctl);
+  } else {
+    ssd_state_passing_kernel<float><<<(unsigned)ws.sp_tiles, kSpThreads, 0, s>>>(h0, h_final, d, ws, ctl);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace ssm

@@ -1,0 +1,67 @@
+"""Shared helpers of the GPU parity tests: device transfer and the tolerance rules.
+
+Tolerances (fixed for this method, written here once):
+  float32 workloads: max |GPU - oracle| <= 1e-4 * max |oracle|, per output tensor (the scan:
+    per row).  Relative error is undefined at zero crossings, so "max relative error 1e-4"
+    is read normwise.
+  bf16-input workloads (float32 accumulation): max |dy| <= 2e-2 * RMS(y_oracle) and
+    max |dh_final| <= 1e-2 * RMS(h_final_oracle).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+F32_RTOL = 1e-4
+BF16_Y_RMS = 2e-2
+BF16_H_RMS = 1e-2
+
+
+def to_dev(arr, dtype="f32", device="cuda"):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32)).to(device)
+    return t.to(torch.bfloat16) if dtype == "bf16" else t
+
+
+def to_np(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def err_report(got, ref):
+    d = np.abs(np.asarray(got, np.float64) - ref)
+    i = np.unravel_index(int(np.argmax(d)), d.shape) if d.size else ()
+    return d, i
+
+
+def assert_f32_close(got, ref, what):
+    if ref.size == 0:
+        return
+    d, i = err_report(got, ref)
+    scale = float(np.max(np.abs(ref)))
+    assert d[i] <= F32_RTOL * scale or d[i] == 0.0, (
+        f"{what}: max|d|={d[i]:.3e} at {i} (gpu {np.asarray(got)[i]!r}, oracle {ref[i]!r}) > 1e-4*{scale:.3e}")
+
+
+def assert_rows_close(got, ref, what):
+    """Per-row normwise float32 rule for the scan."""
+    for r in range(ref.shape[0]):
+        assert_f32_close(got[r], ref[r], f"{what} row {r}")
+
+
+def assert_bf16_close(got, ref, what, rms_tol):
+    if ref.size == 0:
+        return
+    d, i = err_report(got, ref)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    assert d[i] <= rms_tol * rms, (
+        f"{what}: max|d|={d[i]:.3e} at {i} (gpu {np.asarray(got)[i]!r}, oracle {ref[i]!r}) > {rms_tol}*RMS {rms:.3e}")
+
+
+def assert_ssd_close(dtype, y, y_ref, hf, hf_ref, what):
+    if dtype == "f32":
+        assert_f32_close(y, y_ref, f"{what} y")
+        if hf_ref is not None:
+            assert_f32_close(hf, hf_ref, f"{what} h_final")
+    else:
+        assert_bf16_close(y, y_ref, f"{what} y", BF16_Y_RMS)
+        if hf_ref is not None:
+            assert_bf16_close(hf, hf_ref, f"{what} h_final", BF16_H_RMS)

@@ -1,0 +1,114 @@
+"""CPU tests of the C ABI: the library builds, loads, exports every symbol include/ssm.h declares,
+and rejects bad arguments on the host before anything is enqueued (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from selective_state_space_mamba_gb300 import _build, _lib
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "ssm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"SSM_API\s+[\w\s\*]*?\b(ssm_\w+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    assert declared_symbols() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    out = os.popen(f"nm -D --defined-only {_build.LIB}").read()
+    exported = set(re.findall(r"\bT (ssm_\w+)", out))
+    assert set(declared_symbols()) <= exported
+    assert all(s.startswith("ssm_") for s in exported), "only the C ABI is exported"
+
+
+def test_library_targets_sm103a():
+    assert "arch=compute_103a,code=sm_103a" in " ".join(_build.ARCH)
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = _lib.status_string(code)
+        assert s.startswith("SSM_")
+    assert _lib.status_string(99) == "unknown ssm_status"
+    assert lib.ssm_version().decode().count(".") == 2
+
+
+def test_workspace_sizes(lib):
+    # 0 for invalid / unsupported shapes
+    assert lib.ssm_ssd_fwd_workspace_bytes(1, 256, 2, 32, 64, 1, 64, 0) == 0   # headdim 32
+    assert lib.ssm_ssd_fwd_workspace_bytes(1, 256, 3, 64, 64, 2, 64, 0) == 0   # nh % G
+    assert lib.ssm_ssd_fwd_workspace_bytes(1, 256, 2, 64, 64, 1, 100, 0) == 0  # chunk
+    assert lib.ssm_linscan_workspace_bytes(-1, 5) == 0
+    # grows with the problem and holds at least the per-chunk states
+    w3 = lib.ssm_ssd_fwd_workspace_bytes(4, 8192, 80, 64, 128, 1, 256, 1)
+    states = 4 * 32 * 80 * 64 * 128
+    assert w3 >= states * 4 + states * 2
+    assert w3 % 256 == 0
+    assert lib.ssm_linscan_workspace_bytes(384, 65536) >= 256 + (384 * 65536 // 4096) * 24
+
+
+FAKE = 0x10000  # never dereferenced: every call below fails validation first
+
+
+def _ssd(lib, **kw):
+    args = dict(x=FAKE, dt=FAKE, A=FAKE, B=FAKE, C=FAKE, D=FAKE, h0=None, y=FAKE, hf=None, batch=1, L=256, nh=2,
+                H=64, S=64, G=1, T=64, dtype=0, ws=FAKE, wsb=1 << 40)
+    args.update(kw)
+    return lib.ssm_ssd_fwd(args["x"], args["dt"], args["A"], args["B"], args["C"], args["D"], args["h0"], args["y"],
+                           args["hf"], args["batch"], args["L"], args["nh"], args["H"], args["S"], args["G"],
+                           args["T"], args["dtype"], args["ws"], args["wsb"], None)
+
+
+def test_ssd_host_validation(lib):
+    assert _ssd(lib, H=32) == _lib.SSM_ERR_UNSUPPORTED
+    assert _ssd(lib, S=96) == _lib.SSM_ERR_UNSUPPORTED
+    assert _ssd(lib, T=32) == _lib.SSM_ERR_UNSUPPORTED
+    assert _ssd(lib, nh=3, G=2) == _lib.SSM_ERR_INVALID_ARG
+    assert _ssd(lib, batch=-1) == _lib.SSM_ERR_INVALID_ARG
+    assert _ssd(lib, L=-5) == _lib.SSM_ERR_INVALID_ARG
+    assert _ssd(lib, dtype=7) == _lib.SSM_ERR_INVALID_ARG
+    assert _ssd(lib, x=None) == _lib.SSM_ERR_INVALID_ARG
+    assert _ssd(lib, x=FAKE + 4) == _lib.SSM_ERR_ALIGNMENT
+    assert _ssd(lib, h0=FAKE + 8) == _lib.SSM_ERR_ALIGNMENT
+    assert _ssd(lib, ws=None) == _lib.SSM_ERR_WORKSPACE
+    assert _ssd(lib, wsb=1024) == _lib.SSM_ERR_WORKSPACE
+    assert _ssd(lib, ws=FAKE + 16) == _lib.SSM_ERR_ALIGNMENT
+    # no tokens and no final state requested: nothing to enqueue
+    assert _ssd(lib, L=0, hf=None) == _lib.SSM_OK
+    assert _ssd(lib, batch=0, hf=None) == _lib.SSM_OK
+
+
+def test_linscan_host_validation(lib):
+    f = lib.ssm_linscan_fwd
+    assert f(FAKE, FAKE, FAKE, -1, 10, FAKE, 1 << 30, None) == _lib.SSM_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, 3, -1, FAKE, 1 << 30, None) == _lib.SSM_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, 0, 10, None, 0, None) == _lib.SSM_OK   # empty: nothing enqueued
+    assert f(FAKE, FAKE, FAKE, 10, 0, None, 0, None) == _lib.SSM_OK
+    assert f(None, FAKE, FAKE, 3, 10, FAKE, 1 << 30, None) == _lib.SSM_ERR_INVALID_ARG
+    assert f(FAKE + 4, FAKE, FAKE, 3, 10, FAKE, 1 << 30, None) == _lib.SSM_ERR_ALIGNMENT
+    assert f(FAKE, FAKE, FAKE, 3, 10, FAKE, 16, None) == _lib.SSM_ERR_WORKSPACE
+    assert f(FAKE, FAKE, FAKE, 3, 10, FAKE + 128, 1 << 30, None) == _lib.SSM_ERR_ALIGNMENT
+
+
+def test_product_package_does_not_import_oracle():
+    pkg = os.path.dirname(_lib.__file__)
+    for root, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith(".py"):
+                text = open(os.path.join(root, fn)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), fn
+            if fn.endswith((".cu", ".cuh", ".h")):
+                assert "ssm_oracle" not in open(os.path.join(root, fn)).read(), fn

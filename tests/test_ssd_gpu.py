@@ -1,0 +1,181 @@
+"""GPU parity of the SSD forward (through the C ABI) against the float64 oracle.
+
+Full-size bf16 workloads are compared on sampled (batch, head) units, which the C oracle
+computes over the whole sequence; small workloads (several chunks, ragged tails, every chunk
+size, both state sizes, grouped B/C, with and without h0) are compared on every output.
+"""
+import zlib
+
+import numpy as np
+import pytest
+
+import parity as P
+from oracle import native
+from oracle import ssd as ossd
+from selective_state_space_mamba_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_ssd(inp, shape, h0=True, final=True, stream=None):
+    import torch
+    import selective_state_space_mamba_gb300 as ssm
+    dt_ = shape.dtype
+    x, dt, B, C = (P.to_dev(inp[k], dt_) for k in ("x", "dt", "B", "C"))
+    A, D = P.to_dev(inp["A"]), P.to_dev(inp["D"])
+    h0_t = P.to_dev(inp["h0"]) if h0 else None
+    ctx = torch.cuda.stream(stream) if stream is not None else torch.cuda.stream(torch.cuda.current_stream())
+    with ctx:
+        y, hf = ssm.ssd_fwd(x, dt, A, B, C, D, h0_t, chunk=shape.chunk, return_final_state=final)
+    torch.cuda.synchronize()
+    assert ssm.check_device_status(kind="ssd") == 0
+    return P.to_np(y), (P.to_np(hf) if hf is not None else None)
+
+
+def oracle_units(inp, units, h0=True):
+    return native.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                          inp["h0"] if h0 else None, units=np.asarray(units))
+
+
+def sample_units(shape, n, seed=0):
+    rng = np.random.default_rng(seed)
+    total = shape.batch * shape.nheads
+    units = {0, total - 1}
+    while len(units) < min(n, total):
+        units.add(int(rng.integers(total)))
+    return sorted(units)
+
+
+def compare_units(shape, inp, y, hf, units, what):
+    y_ref, hf_ref = oracle_units(inp, units)
+    nh = shape.nheads
+    yu = np.stack([y[u // nh, :, u % nh] for u in units])
+    hu = np.stack([hf[u // nh, u % nh] for u in units])
+    P.assert_ssd_close(shape.dtype, yu, y_ref, hu, hf_ref, what)
+
+
+def test_small_f32_workload_all_outputs(cuda_lib):
+    shape = synth.SSD_SMALL_F32
+    inp = synth.ssd_inputs(shape)
+    y, hf = gpu_ssd(inp, shape)
+    y_ref, hf_ref = ossd.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"])
+    P.assert_ssd_close("f32", y, y_ref, hf, hf_ref, shape.name)
+
+
+@pytest.mark.parametrize("shape,n_units", [(synth.SSD_B8_L2048, 12), (synth.SSD_B4_L8192, 10),
+                                           (synth.SSD_B1_L131072, 4)], ids=lambda v: getattr(v, "name", str(v)))
+def test_full_bf16_workloads_sampled(cuda_lib, shape, n_units):
+    inp = synth.ssd_inputs(shape)
+    y, hf = gpu_ssd(inp, shape)
+    assert np.isfinite(y).all() and np.isfinite(hf).all()
+    compare_units(shape, inp, y, hf, sample_units(shape, n_units), shape.name)
+
+
+SMALL = []
+for dtype in ("f32", "bf16"):
+    for (L, T) in [(1, 64), (63, 64), (64, 64), (65, 64), (300, 128), (1000, 256), (777, 64)]:
+        for S, G, nh in [(64, 1, 2), (128, 2, 4)]:
+            SMALL.append(synth.SSDShape(f"{dtype}_L{L}_T{T}_S{S}_G{G}", 2, L, nh, 64, S, G, T, dtype, h0=True))
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: s.name)
+def test_small_shapes_all_outputs(cuda_lib, shape):
+    inp = synth.ssd_inputs(shape, seed=zlib.crc32(shape.name.encode()))
+    y, hf = gpu_ssd(inp, shape)
+    y_ref, hf_ref = ossd.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"])
+    P.assert_ssd_close(shape.dtype, y, y_ref, hf, hf_ref, shape.name)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_long_state_chain(cuda_lib, dtype):
+    """Many chunks through the look-back state passing (nc = 200 chunks -> 13 chunk tiles)."""
+    shape = synth.SSDShape(f"chain_{dtype}", 1, 200 * 64 - 5, 2, 64, 128, 1, 64, dtype, dt_shift=4.0, h0=True)
+    inp = synth.ssd_inputs(shape, seed=77)
+    y, hf = gpu_ssd(inp, shape)
+    y_ref, hf_ref = native.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"])
+    y_ref = y_ref.reshape(1, 2, -1, 64).transpose(0, 2, 1, 3)
+    P.assert_ssd_close(dtype, y, y_ref, hf, hf_ref.reshape(hf.shape), shape.name)
+
+
+def test_no_h0_and_no_final_state(cuda_lib):
+    shape = synth.SSDShape("noh0", 2, 200, 2, 64, 64, 1, 64, "f32")
+    inp = synth.ssd_inputs(shape, seed=4)
+    y, hf = gpu_ssd(inp, shape, h0=False, final=False)
+    assert hf is None
+    y_ref, _ = ossd.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], None)
+    P.assert_f32_close(y, y_ref, "no h0")
+
+
+def test_zero_length_copies_h0(cuda_lib):
+    import torch
+    import selective_state_space_mamba_gb300 as ssm
+    h0 = torch.randn(2, 3, 64, 64, device="cuda")
+    x = torch.zeros(2, 0, 3, 64, device="cuda")
+    y, hf = ssm.ssd_fwd(x, torch.zeros(2, 0, 3, device="cuda"), torch.zeros(3, device="cuda"),
+                        torch.zeros(2, 0, 1, 64, device="cuda"), torch.zeros(2, 0, 1, 64, device="cuda"),
+                        torch.zeros(3, device="cuda"), h0, chunk=64)
+    assert y.shape == x.shape and torch.equal(hf, h0)
+
+
+def test_output_is_inclusive_not_exclusive(cuda_lib):
+    """y_t reads the state after token t; the exclusive reading (state before t) is far off."""
+    shape = synth.SSDShape("incl", 1, 130, 2, 64, 64, 1, 64, "f32", h0=True)
+    inp = synth.ssd_inputs(shape, seed=8)
+    y, _ = gpu_ssd(inp, shape)
+    x, dt, A, B, C, D, h0 = (inp[k].astype(np.float64) for k in ("x", "dt", "A", "B", "C", "D", "h0"))
+    state = h0.copy()
+    y_excl = np.empty_like(y)
+    for t in range(shape.seqlen):
+        y_excl[:, t] = np.einsum("bnps,bs->bnp", state, C[:, t, 0]) + D[None, :, None] * x[:, t]
+        state = np.exp(A[None] * dt[:, t])[..., None, None] * state + x[:, t][..., None] * (
+            dt[:, t][..., None] * B[:, t, 0][:, None, :])[:, :, None, :]
+    assert np.max(np.abs(y - y_excl)) > 100 * 1e-4 * np.max(np.abs(y_excl))
+
+
+@pytest.mark.parametrize("split", [128, 150])
+def test_state_carry_split_equals_full(cuda_lib, split):
+    shape = synth.SSDShape("carry", 1, 320, 2, 64, 64, 1, 64, "f32", h0=True)
+    inp = synth.ssd_inputs(shape, seed=21)
+    y, hf = gpu_ssd(inp, shape)
+    first = {k: (v[:, :split] if k in ("x", "dt", "B", "C") else v) for k, v in inp.items()}
+    second = {k: (v[:, split:] if k in ("x", "dt", "B", "C") else v) for k, v in inp.items()}
+    y1, h1 = gpu_ssd(first, shape.replace(seqlen=split))
+    second["h0"] = h1.astype(np.float32)
+    y2, h2 = gpu_ssd(second, shape.replace(seqlen=shape.seqlen - split))
+    P.assert_f32_close(np.concatenate([y1, y2], axis=1), y, "split y")
+    P.assert_f32_close(h2, hf, "split h_final")
+
+
+def test_side_stream(cuda_lib):
+    import torch
+    shape = synth.SSDShape("stream", 1, 500, 4, 64, 128, 2, 128, "bf16", h0=True)
+    inp = synth.ssd_inputs(shape, seed=5)
+    y, hf = gpu_ssd(inp, shape, stream=torch.cuda.Stream())
+    y_ref, hf_ref = ossd.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"])
+    P.assert_ssd_close("bf16", y, y_ref, hf, hf_ref, "side stream")
+
+
+def test_state_passing_bounded_wait_timeout(cuda_lib):
+    import selective_state_space_mamba_gb300 as ssm
+    from selective_state_space_mamba_gb300 import _lib
+    shape = synth.SSDShape("timeout", 1, 64 * 64, 1, 64, 64, 1, 64, "f32")
+    inp = synth.ssd_inputs(shape, seed=2)
+    # 4 chains (state slices) x 4 chunk tiles; claim index 5 is chunk tile 1 of chain 1
+    try:
+        ssm.debug_set_lookback_fault(stall_tile=5, spin_limit_ns=20_000_000)
+        gpu_ssd_status = _run_raw(inp, shape)
+        assert gpu_ssd_status == _lib.SSM_ERR_TIMEOUT
+    finally:
+        ssm.debug_set_lookback_fault(-1, 0)
+    y, hf = gpu_ssd(inp, shape)
+    y_ref, hf_ref = ossd.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"])
+    P.assert_ssd_close("f32", y, y_ref, hf, hf_ref, "after timeout")
+
+
+def _run_raw(inp, shape):
+    import torch
+    import selective_state_space_mamba_gb300 as ssm
+    x, dt, B, C = (P.to_dev(inp[k], shape.dtype) for k in ("x", "dt", "B", "C"))
+    ssm.ssd_fwd(x, dt, P.to_dev(inp["A"]), B, C, P.to_dev(inp["D"]), P.to_dev(inp["h0"]), chunk=shape.chunk)
+    torch.cuda.synchronize()
+    return ssm.check_device_status(kind="ssd")
