@@ -104,9 +104,10 @@ def kernel_traffic(kernel):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock / throttle sampling (every 20 ms); summary() keeps the samples taken
+    inside [t0, t1] (host wall-clock bounds of the timed region)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -118,7 +119,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -134,23 +135,32 @@ class ClockSampler:
                 self.out, _ = self.proc.communicate()
         return False
 
-    def summary(self):
-        sm, mx, reasons = [], 0.0, set()
+    def summary(self, t0=None, t1=None):
+        import datetime
+        sm, mx, reasons, power = [], 0.0, set(), []
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for line in self.out.strip().splitlines():
             f = [v.strip() for v in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = max(mx, float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None
+            if t0 is not None and ts is not None and not (t0 - 0.025 <= ts <= t1 + 0.025):
+                continue
+            try:
+                sm.append(float(f[2]))
+                mx = max(mx, float(f[3]))
+                power.append(float(f[4]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+            for n, v in zip(names, f[6:10]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
 
 
 # ----------------------------------------------------------------------------------------
@@ -226,6 +236,8 @@ def run_ours(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks, ssm.KernelTimer(max_launches=8 * args.steps + 8) as kt:
+        time.sleep(0.1)  # let the sampler start
+        t_wall0 = time.time()
         t_wall = time.perf_counter()
         for i in range(args.steps):
             flush.fill_(i & 0xff)
@@ -236,6 +248,8 @@ def run_ours(args, world, rank, local):
             ev[i][2].record(stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
+        t_wall1 = time.time()
+        time.sleep(0.05)
     barrier(world)
     if ssm.check_device_status(kind="ssd") or ssm.check_device_status(kind="linscan"):
         raise RuntimeError("device status error during the timed region")
@@ -314,7 +328,7 @@ def run_ours(args, world, rank, local):
         "kernels": kernels,
         "roofline": roof,
         "gpu_launches": sum(kt.launches.values()),
-        "clocks": clocks.summary(),
+        "clocks": clocks.summary(t_wall0, t_wall1),
         "wall_s_timed": round(t_wall, 3),
     }
     return out, ssd_np, scan_np
@@ -424,7 +438,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0, help="time budget of the oracle CPU baseline")

@@ -132,8 +132,9 @@ SSM_API ssm_status ssm_linscan_fwd(const float *a, const float *b, float *h, int
 
 /*
  * Synchronizes `stream`, reads the device status word at the start of `workspace` (either
- * kind), clears it, and returns SSM_OK or the recorded device error (SSM_ERR_TIMEOUT when a
- * look-back wait exceeded its limit; the outputs of that call are then invalid).
+ * kind) and returns SSM_OK or the recorded device error (SSM_ERR_TIMEOUT when a bounded wait
+ * exceeded its limit; the outputs of that call are then invalid).  After an error it also
+ * resets the workspace's claim counters, so the workspace is usable again.
  */
 SSM_API ssm_status ssm_check_device_status(void *workspace, ssm_stream_t stream);
 

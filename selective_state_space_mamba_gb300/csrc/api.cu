@@ -153,11 +153,33 @@ LinscanWorkspace linscan_workspace_layout(int64_t n, void* base) {
   };
   w.tiles = (n + kLsTile - 1) / kLsTile;
   w.hdr = reinterpret_cast<WsHeader*>(take(kHeaderBytes));
-  w.flags = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * w.tiles));
-  w.agg = reinterpret_cast<float2*>(take(sizeof(float2) * w.tiles));
-  w.inc = reinterpret_cast<float2*>(take(sizeof(float2) * w.tiles));
+  w.desc = reinterpret_cast<LsDesc*>(take(sizeof(LsDesc) * w.tiles));
   w.total_bytes = off;
   return w;
+}
+
+cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                                 uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                                 CUtensorMapSwizzle swizzle) {
+  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorUnknown;
+    encode = reinterpret_cast<EncodeFn>(fn);
+  }
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace ssm
@@ -267,7 +289,8 @@ ssm_status ssm_check_device_status(void* workspace, ssm_stream_t stream) {
   unsigned long long word = 0;
   if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return SSM_ERR_CUDA;
   if (word == 0) return SSM_OK;
-  const unsigned long long zero = 0;
+  // a failed call may also have left the claim counters set: clear the whole header
+  const WsHeader zero{};
   if (cudaMemcpy(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SSM_ERR_CUDA;
   const uint32_t code = (uint32_t)(word & 0xffffffffu);
   return code == 0 ? SSM_ERR_CUDA : static_cast<ssm_status>(code);

@@ -4,14 +4,29 @@
 // aggregates published with flag A and inclusive prefixes with flag P, a whole warp
 // inspecting 32 predecessors at once, several items per thread scanned in registers).
 //
-// GB300 layout choices (not on the page):
-//   * all rows are scanned as ONE flattened sequence of rows*len elements, with a reset at
-//     every row start.  Tiles then never straddle a misaligned row base, every load and
-//     store is a 16-byte vector, and a tile that contains a row start publishes its prefix
-//     immediately (its aggregate is absolute), which cuts the look-back chains at rows.
-//   * within a tile, warp w owns 512 consecutive elements as 4 runs of 128; in each run lane
-//     i owns 4 consecutive elements, so every float4 load/store instruction of a warp covers
-//     512 contiguous bytes.
+// GB300 design choices (not on the page):
+//   * all rows are scanned as ONE flattened sequence of rows*len elements, viewed as a 2-D
+//     tensor of 128-byte lines (32 floats), with a reset at every row start.  A tile is
+//     kLsLines consecutive lines; each consumer thread owns kLsElems consecutive elements of
+//     one line, so a thread scans sequentially in registers and a warp needs one shuffle
+//     scan per tile.
+//   * tiles move by TMA: the producer warp loads a and b with 2-D tensor copies in 128-byte
+//     swizzle mode (a thread reading its own line then hits 8 different bank groups per
+//     quarter-warp: conflict-free), and h goes back to the same swizzled buffer and out with
+//     a TMA tensor store.  Loads and stores are fully coalesced and asynchronous.
+//   * persistent, warp-specialised CTAs: one producer warp claims tiles (atomic counter) and
+//     fills a ring of shared-memory stages ("full" / "empty" mbarriers); the consumer warps
+//     scan; one look-back warp resolves tile i's prefix while the consumers already run the
+//     first pass of tile i+1 (the second pass re-reads tile i from its stage), so the
+//     look-back latency is off the consumers' path; one store warp issues the TMA store of
+//     each finished tile and hands its stage back to the producer once the store has read it.  Claims stay in counter order and each CTA consumes its
+//     claims in order, so the page's forward-progress argument holds: the smallest
+//     unfinished tile is always some CTA's current tile (its data arrives without waiting on
+//     anything) and it waits only on smaller tiles.
+//   * a tile's flag and value share one 16-byte descriptor (no fence between value and flag),
+//     and the look-back stops at the nearest published prefix instead of waiting for all 32
+//     inspected predecessors.  A tile holding a row start publishes its prefix at once (its
+//     aggregate is absolute), which cuts look-back chains at rows.
 //   * a reset is an element whose decay is replaced by 0, and the combine SELECTS the later
 //     operand's b when its decay is 0 instead of multiplying by 0, so an overflowed
 //     predecessor can never turn a fresh row into NaN.
@@ -46,176 +61,407 @@ __device__ __forceinline__ Pair shfl(Pair p, int src) {
   return r;
 }
 
-__global__ void __launch_bounds__(kLsThreads) linscan_lookback_kernel(
-    const float* __restrict__ a, const float* __restrict__ b, float* __restrict__ h, int64_t n, int64_t len,
-    LinscanWorkspace ws, LookbackCtl ctl) {
-  __shared__ uint32_t s_tile;
-  __shared__ Pair s_warp[kLsThreads / 32];
-  __shared__ Pair s_prefix;
+struct LsStage {  // two [kLsLines x 32] float boxes in 128-byte swizzled layout
+  float a[kLsTile];
+  float b[kLsTile];  // h is written back over a
+};
+static_assert(kLsRow % (4 * kLsSplit) == 0, "a thread owns whole 16-byte chunks");
+struct LsJob {        // consumer -> look-back warp, double-buffered by tile parity
+  int64_t tile;      // >= tiles: stop
+  int64_t r0;
+  Pair agg;          // tile aggregate
+  float prefix;      // look-back warp -> consumers: state before the tile
+  int absolute;
+};
+struct LsShared {
+  LsStage stage[kLsStages];   // first member: 1024-byte aligned (swizzle atom)
+  uint64_t full[kLsStages];   // producer -> consumers: tile id written, data landed
+  uint64_t empty[kLsStages];  // consumers -> producer: stage read and stored, may be refilled
+  uint64_t lb_req[2];         // consumers -> look-back warp: job posted
+  uint64_t lb_done[2];        // look-back warp -> consumers: prefix posted
+  uint64_t st_req[kLsStages]; // consumers -> store warp: stage holds a finished tile (or stop)
+  int64_t st_line0[kLsStages];// first line of that tile (< 0: stop)
+  int64_t tile[kLsStages];
+  int64_t r0[kLsStages];      // position of the tile's first element within its row
+  LsJob job[2];
+  Pair warp_agg[2][kLsThreads / 32];
+};
+static_assert(sizeof(LsStage) % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 
+constexpr int kLsBlock = kLsThreads + 96;  // consumer warps + producer, look-back and store warps
+constexpr uint32_t kLsConsumerBar = 1;      // named barrier of the consumer warps
+
+struct LsArgs {
+  const float* a;
+  const float* b;
+  float* h;
+  int64_t n;      // rows * len
+  int64_t len;
+  int64_t lines;  // n / 32: full 128-byte lines covered by the tensor maps (0: no TMA)
+};
+
+// Shared-memory word index of 16-byte chunk `chunk` (0..7) of line `line` in the 128-byte
+// swizzled box.  The eight lanes of a quarter-warp read eight different bank groups.
+__device__ __forceinline__ int swz(int line, int chunk) { return line * kLsRow + ((chunk ^ (line & 7)) << 2); }
+
+// Producer (one thread): claim tiles in counter order and fill the stage ring; it ends after
+// the first claim past the last tile, which it hands on as a sentinel.
+__device__ void ls_producer(LsShared& sh, const LsArgs& p, const CUtensorMap* map_a, const CUtensorMap* map_b,
+                            const LinscanWorkspace& ws, const LookbackCtl& ctl) {
+  for (int i = 0;; ++i) {
+    const int st = i % kLsStages;
+    const int use = i / kLsStages;
+    if (use > 0 && !mbar_wait(&sh.empty[st], (uint32_t)(use - 1) & 1u, ctl.spin_limit_ns)) {
+      record_error(ws.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
+      return;  // the consumers give up on their own bounded wait
+    }
+    const int64_t tile = claim_tile(ws.hdr);
+    sh.tile[st] = tile;
+    if (tile >= ws.tiles) {
+      mbar_arrive(&sh.full[st]);  // sentinel, no data
+      return;
+    }
+    sh.r0[st] = (tile * kLsTile) % p.len;
+    const int64_t line0 = tile * kLsLines;
+    if (line0 < p.lines) {
+      // the whole box counts toward the transaction, rows past the tensor are zero-filled
+      mbar_arrive_expect_tx(&sh.full[st], 2u * (uint32_t)sizeof(float) * kLsTile);
+      tma_load_2d(sh.stage[st].a, map_a, 0, (int)line0, &sh.full[st]);
+      tma_load_2d(sh.stage[st].b, map_b, 0, (int)line0, &sh.full[st]);
+    } else {
+      mbar_arrive(&sh.full[st]);  // only the ragged tail: consumers read it directly
+    }
+  }
+}
+
+// Consumer warp 0: state just before `tile`, by decoupled look-back.  Lanes poll the
+// descriptors of 32 predecessors; the window is complete once every lane up to the nearest
+// published prefix (P) is valid, so a tile never waits on predecessors older than that P.
+// Without a P in a complete window the 32 aggregates are folded in and the window moves
+// back.  Bounded: past the limit it records SSM_ERR_TIMEOUT and yields NaN.
+__device__ __forceinline__ float lookback(int64_t tile, const LinscanWorkspace& ws, const LookbackCtl& ctl,
+                                          int lane) {
+  Pair acc{1.f, 0.f};  // composition of the predecessors folded so far (newest last)
+  int64_t newest = tile - 1;
+  uint64_t t0 = 0;
+  uint32_t polls = 0;
+  const unsigned long long want = make_flag(ctl.epoch, 0);
+  while (true) {
+    const int64_t idx = newest - lane;
+    bool valid = true, is_p = true;  // lanes before tile 0 count as a published zero prefix
+    Pair v{0.f, 0.f};
+    if (idx >= 0) {
+      unsigned long long f;
+      float va, vb;
+      ld_relaxed_desc(&ws.desc[idx], f, va, vb);
+      valid = (f & ~3ull) == want && (f & 3ull) != 0ull;
+      is_p = valid && (f & 3ull) == kFlagPrefix;
+      v = is_p ? Pair{0.f, vb} : Pair{va, vb};
+    }
+    const unsigned invalid = __ballot_sync(0xffffffffu, !valid);
+    const unsigned pmask = __ballot_sync(0xffffffffu, is_p);
+    const int first_invalid = invalid ? __ffs(invalid) - 1 : 32;
+    const int first_p = pmask ? __ffs(pmask) - 1 : 32;
+    if (first_p < first_invalid || invalid == 0u) {
+      const int last = first_p < 32 ? first_p : 31;  // lanes 0..last are folded
+      Pair win{1.f, 0.f};
+      for (int l = last; l >= 0; --l) win = combine(win, shfl(v, l));
+      acc = combine(win, acc);
+      if (first_p < 32) return acc.b;
+      newest -= 32;
+      polls = 0;
+      continue;
+    }
+    // a predecessor before the nearest prefix has not published yet: poll again (bounded)
+    if (++polls == 1) t0 = global_timer_ns();
+    if ((polls & 31u) == 0u) {
+      const bool aborted = call_aborted(ws.hdr, ctl.epoch);
+      const bool late = global_timer_ns() - t0 > ctl.spin_limit_ns;
+      if (__any_sync(0xffffffffu, late) && lane == 0) record_error(ws.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
+      if (__any_sync(0xffffffffu, aborted || late)) return __int_as_float(0x7fc00000);
+    }
+    if (polls > 64) __nanosleep(64);
+  }
+}
+
+// Look-back warp: serve the consumers' jobs in order until the stop job.
+__device__ void ls_lookback_warp(LsShared& sh, const LinscanWorkspace& ws, const LookbackCtl& ctl, int lane) {
+  for (int j = 0;; ++j) {
+    if (!mbar_wait(&sh.lb_req[j & 1], (uint32_t)(j >> 1) & 1u, ctl.spin_limit_ns)) {
+      if (lane == 0) record_error(ws.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
+      return;
+    }
+    LsJob& job = sh.job[j & 1];
+    const int64_t tile = job.tile;
+    if (tile >= ws.tiles) return;
+    const bool need_prefix = (tile != 0) && (job.r0 != 0);
+    const float x = need_prefix ? lookback(tile, ws, ctl, lane) : 0.f;
+    if (lane == 0) {
+      if (tile != ctl.stall_tile && !job.absolute)
+        st_relaxed_desc(&ws.desc[tile], make_flag(ctl.epoch, kFlagPrefix), 0.f, apply(job.agg, x));
+      job.prefix = x;
+      mbar_arrive(&sh.lb_done[j & 1]);
+    }
+    __syncwarp();
+  }
+}
+
+// Store warp (one thread): in tile order, TMA-store each finished stage, wait until the store
+// has read it, and hand the stage back to the producer; stops at the stop job.
+__device__ void ls_store_warp(LsShared& sh, const CUtensorMap* map_h, const LinscanWorkspace& ws,
+                              const LookbackCtl& ctl) {
+  for (int j = 0;; ++j) {
+    const int st = j % kLsStages;
+    if (!mbar_wait(&sh.st_req[st], (uint32_t)(j / kLsStages) & 1u, ctl.spin_limit_ns)) {
+      record_error(ws.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
+      break;
+    }
+    const int64_t line0 = sh.st_line0[st];
+    if (line0 < 0) break;
+    if (line0 < (int64_t)0x7fffffff && line0 >= 0) {
+      tma_store_2d(map_h, sh.stage[st].a, 0, (int)line0);
+      bulk_commit();
+      bulk_wait_read<0>();
+    }
+    mbar_arrive(&sh.empty[st]);
+  }
+  bulk_wait<0>();  // every store of this CTA has completed
+}
+
+__global__ void __launch_bounds__(kLsBlock, SSM_LS_MIN_BLOCKS)
+    linscan_lookback_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                            const __grid_constant__ CUtensorMap map_h, LsArgs p, LinscanWorkspace ws,
+                            LookbackCtl ctl) {
+  extern __shared__ unsigned char ls_smem_raw[];
+  // align the stage ring to the 1024-byte swizzle atom (the launch adds 1 KB of slack)
+  const uint32_t raw = smem_addr(ls_smem_raw);
+  LsShared& sh = *reinterpret_cast<LsShared*>(ls_smem_raw + ((1024u - (raw & 1023u)) & 1023u));
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  if (threadIdx.x == 0) s_tile = claim_tile(ws.hdr);
-  __syncthreads();
-  const int64_t tile = s_tile;
-  if (tile >= ws.tiles) {  // claim counter not reset (workspace not zero-filled): refuse
-    if (threadIdx.x == 0) {
-      record_error(ws.hdr, ctl.epoch, SSM_ERR_WORKSPACE);
-      retire_tile(ws.hdr, (uint32_t)ws.tiles);
+  const int t = threadIdx.x;                           // consumer thread
+  const int my_line = t / kLsSplit;                    // line within the tile
+  const int my_chunk0 = (t % kLsSplit) * (kLsElems / 4);  // first 16-byte chunk of the line
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kLsStages; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], 1);
     }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sh.lb_req[s], 1);
+      mbar_init(&sh.lb_done[s], 1);
+    }
+    for (int s = 0; s < kLsStages; ++s) mbar_init(&sh.st_req[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == kLsThreads / 32) {  // producer warp
+    if (lane == 0) ls_producer(sh, p, &map_a, &map_b, ws, ctl);
     return;
   }
-  const int64_t tile_base = tile * kLsTile;
+  if (warp == kLsThreads / 32 + 1) {  // look-back warp
+    ls_lookback_warp(sh, ws, ctl, lane);
+    return;
+  }
+  if (warp == kLsThreads / 32 + 2) {  // store warp
+    if (lane == 0) ls_store_warp(sh, &map_h, ws, ctl);
+    return;
+  }
 
-  // ---- load 4 runs of 4 consecutive elements (16-byte vectors, coalesced per warp) ----
-  float va[kLsRuns][4], vb[kLsRuns][4];
-#pragma unroll
-  for (int k = 0; k < kLsRuns; ++k) {
-    const int64_t e0 = tile_base + warp * 512 + k * 128 + lane * 4;
-    if (e0 + 3 < n) {
-      const float4 fa = __ldcs(reinterpret_cast<const float4*>(a + e0));
-      const float4 fb = __ldcs(reinterpret_cast<const float4*>(b + e0));
-      va[k][0] = fa.x; va[k][1] = fa.y; va[k][2] = fa.z; va[k][3] = fa.w;
-      vb[k][0] = fb.x; vb[k][1] = fb.y; vb[k][2] = fb.z; vb[k][3] = fb.w;
-    } else {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const bool in = e0 + j < n;
-        va[k][j] = in ? a[e0 + j] : 1.f;  // identity beyond the end
-        vb[k][j] = in ? b[e0 + j] : 0.f;
-      }
+  // per-thread results of pass 1 of the previous tile, consumed by its pass 2
+  Pair prev_excl{1.f, 0.f}, prev_wp{1.f, 0.f};
+  int64_t prev_tile = -1, prev_r0 = 0;
+  for (int it = 0;; ++it) {
+    const int st = it % kLsStages;
+    int64_t tile = ws.tiles;  // stop unless a tile arrives
+    if (mbar_wait(&sh.full[st], (uint32_t)(it / kLsStages) & 1u, ctl.spin_limit_ns)) {
+      tile = sh.tile[st];
+    } else if (threadIdx.x == 0) {
+      record_error(ws.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
     }
-  }
+    const bool valid = tile < ws.tiles;  // uniform across the consumers
+    Pair cur_excl{1.f, 0.f}, cur_wp{1.f, 0.f};
+    int64_t cur_r0 = 0;
 
-  // ---- row starts become resets; per-lane inclusive scan of each run ----
-  Pair ex[kLsRuns][4];  // element prefixes, relative to the start of the lane's run
-  Pair lane_tot[kLsRuns];
+    // ================= pass 1 of this tile: aggregate, publish, post the look-back job =====
+    if (valid) {
+      cur_r0 = sh.r0[st];
+      const int64_t tile_base = tile * kLsTile;
+      const bool in_map = tile * kLsLines + my_line < p.lines;
+      const int e0 = t * kLsElems;
+      const int nv = (int)min(int64_t(kLsTile), p.n - tile_base);
+      const float* sa = sh.stage[st].a;
+      const float* sb = sh.stage[st].b;
+      Pair tot{1.f, 0.f};
+      int64_t m = (cur_r0 + e0) % p.len;  // position of my first element within its row
 #pragma unroll
-  for (int k = 0; k < kLsRuns; ++k) {
-    const int64_t e0 = tile_base + warp * 512 + k * 128 + lane * 4;
-    int64_t m = e0 % len;  // position of the first element within its row
-    Pair acc{1.f, 0.f};
+      for (int c = 0; c < kLsElems / 4; ++c) {
+        float va[4], vb[4];
+        if (in_map) {
+          const float4 fa = *reinterpret_cast<const float4*>(&sa[swz(my_line, my_chunk0 + c)]);
+          const float4 fb = *reinterpret_cast<const float4*>(&sb[swz(my_line, my_chunk0 + c)]);
+          va[0] = fa.x; va[1] = fa.y; va[2] = fa.z; va[3] = fa.w;
+          vb[0] = fb.x; vb[1] = fb.y; vb[2] = fb.z; vb[3] = fb.w;
+        } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      Pair q{m == 0 ? 0.f : va[k][j], vb[k][j]};
-      acc = (j == 0) ? q : combine(acc, q);
-      ex[k][j] = acc;
-      if (++m == len) m = 0;
-    }
-    lane_tot[k] = acc;
-  }
-
-  // ---- warp scan of each run, chained across the 4 runs ----
-  Pair carry{1.f, 0.f};  // composition of the warp's earlier runs
-#pragma unroll
-  for (int k = 0; k < kLsRuns; ++k) {
-    Pair inc = lane_tot[k];
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      Pair o = shfl_up(inc, d);
-      if (lane >= d) inc = combine(o, inc);
-    }
-    Pair excl = shfl_up(inc, 1);
-    if (lane == 0) excl = Pair{1.f, 0.f};
-    const Pair lane_prefix = combine(carry, excl);  // everything in the warp before this lane's run
-#pragma unroll
-    for (int j = 0; j < 4; ++j) ex[k][j] = combine(lane_prefix, ex[k][j]);
-    carry = combine(carry, shfl(inc, 31));
-  }
-  if (lane == 0) s_warp[warp] = carry;
-  __syncthreads();
-
-  // ---- block scan of warp aggregates; thread 0 publishes the tile aggregate ----
-  Pair warp_prefix{1.f, 0.f};
-  Pair tile_agg{1.f, 0.f};
-#pragma unroll
-  for (int w = 0; w < kLsThreads / 32; ++w) {
-    if (w == warp) warp_prefix = tile_agg;
-    tile_agg = combine(tile_agg, s_warp[w]);
-  }
-  const bool stalled = (int64_t)tile == ctl.stall_tile;
-  const bool absolute = (tile == 0) || (tile_agg.a == 0.f);
-  if (threadIdx.x == 0 && !stalled) {
-    if (absolute) {
-      ws.inc[tile] = float2{0.f, tile_agg.b};
-    } else {
-      ws.agg[tile] = float2{tile_agg.a, tile_agg.b};
-    }
-    __threadfence();
-    st_release_u64(&ws.flags[tile], make_flag(ctl.epoch, absolute ? kFlagPrefix : kFlagAggregate));
-  }
-
-  // ---- decoupled look-back by warp 0 (32 predecessors per step) ----
-  // The first element of a tile that starts a row needs no prefix; neither does tile 0.
-  const bool need_prefix = (tile != 0) && (tile_base % len != 0);
-  if (warp == 0) {
-    Pair acc{1.f, 0.f};  // composition of the predecessors inspected so far (newest last)
-    if (need_prefix) {
-      int64_t newest = tile - 1;
-      while (true) {
-        const int64_t idx = newest - lane;
-        uint32_t kind = kFlagPrefix;
-        Pair v{0.f, 0.f};
-        if (idx >= 0) {
-          kind = wait_flag(&ws.flags[idx], ws.hdr, ctl);
-          if (kind == kFlagPrefix) {
-            float2 f = ld_relaxed_f2(&ws.inc[idx]);
-            v = Pair{0.f, f.y};
-          } else if (kind == kFlagAggregate) {
-            float2 f = ld_relaxed_f2(&ws.agg[idx]);
-            v = Pair{f.x, f.y};
-          } else {
-            v = Pair{0.f, __int_as_float(0x7fc00000)};  // gave up: poison, flagged in status
-            kind = kFlagPrefix;
+          for (int j = 0; j < 4; ++j) {
+            const int e = e0 + 4 * c + j;
+            va[j] = e < nv ? p.a[tile_base + e] : 1.f;  // identity past the end
+            vb[j] = e < nv ? p.b[tile_base + e] : 0.f;
           }
         }
-        const unsigned pmask = __ballot_sync(0xffffffffu, kind == kFlagPrefix);
-        const int last = pmask ? (__ffs(pmask) - 1) : 31;  // lanes 0..last are used
-        // Fold lanes last..0 (oldest first) into the accumulated composition.
-        Pair win{1.f, 0.f};
-        for (int l = last; l >= 0; --l) win = combine(win, shfl(v, l));
-        acc = combine(win, acc);
-        if (pmask) break;
-        newest -= 32;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const Pair q{m == 0 ? 0.f : va[j], vb[j]};
+          tot = (c == 0 && j == 0) ? q : combine(tot, q);
+          if (++m == p.len) m = 0;
+        }
       }
-    }
-    if (lane == 0) {
-      s_prefix = acc;
-      if (!stalled && !absolute) {
-        const Pair incl = combine(acc, tile_agg);
-        ws.inc[tile] = float2{0.f, incl.b};
-        __threadfence();
-        st_release_u64(&ws.flags[tile], make_flag(ctl.epoch, kFlagPrefix));
+      Pair inc = tot;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const Pair o = shfl_up(inc, d);
+        if (lane >= d) inc = combine(o, inc);
       }
+      cur_excl = shfl_up(inc, 1);
+      if (lane == 0) cur_excl = Pair{1.f, 0.f};
+      if (lane == 31) sh.warp_agg[it & 1][warp] = inc;
+      named_bar_sync(kLsConsumerBar, kLsThreads);
+      Pair tile_agg{1.f, 0.f};
+#pragma unroll
+      for (int w = 0; w < kLsThreads / 32; ++w) {
+        if (w == warp) cur_wp = tile_agg;
+        tile_agg = combine(tile_agg, sh.warp_agg[it & 1][w]);
+      }
+      if (threadIdx.x == 0) {
+        const bool absolute = (tile == 0) || (tile_agg.a == 0.f);
+        if (tile != ctl.stall_tile)
+          st_relaxed_desc(&ws.desc[tile], make_flag(ctl.epoch, absolute ? kFlagPrefix : kFlagAggregate),
+                          absolute ? 0.f : tile_agg.a, tile_agg.b);
+        LsJob& job = sh.job[it & 1];
+        job.tile = tile;
+        job.r0 = cur_r0;
+        job.agg = tile_agg;
+        job.absolute = absolute;
+        mbar_arrive(&sh.lb_req[it & 1]);
+      }
+    } else if (threadIdx.x == 0) {
+      sh.job[it & 1].tile = ws.tiles;  // stop the look-back warp
+      mbar_arrive(&sh.lb_req[it & 1]);
     }
-  }
-  __syncthreads();
-  const float h_in = s_prefix.b;  // state just before the tile (unused where not needed)
 
-  // ---- apply and store ----
+    // ================= pass 2 of the previous tile: apply its prefix, store ================
+    if (prev_tile >= 0) {
+      const int ps = (it - 1) % kLsStages;
+      const int pj = (it - 1) & 1;
+      float x = __int_as_float(0x7fc00000);
+      if (mbar_wait(&sh.lb_done[pj], (uint32_t)((it - 1) >> 1) & 1u, ctl.spin_limit_ns)) {
+        x = sh.job[pj].prefix;
+      } else if (threadIdx.x == 0) {
+        record_error(ws.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
+      }
+      const int64_t tile_base = prev_tile * kLsTile;
+      const int64_t line0 = prev_tile * kLsLines;
+      const bool in_map = line0 + my_line < p.lines;
+      const int e0 = t * kLsElems;
+      const int nv = (int)min(int64_t(kLsTile), p.n - tile_base);
+      float* sa = sh.stage[ps].a;
+      const float* sb = sh.stage[ps].b;
+      float hcur = apply(prev_excl, apply(prev_wp, x));  // state before my line
+      int64_t m = (prev_r0 + e0) % p.len;
 #pragma unroll
-  for (int k = 0; k < kLsRuns; ++k) {
-    const int64_t e0 = tile_base + warp * 512 + k * 128 + lane * 4;
-    float o[4];
+      for (int c = 0; c < kLsElems / 4; ++c) {
+        float va[4], vb[4];
+        if (in_map) {
+          const float4 fa = *reinterpret_cast<const float4*>(&sa[swz(my_line, my_chunk0 + c)]);
+          const float4 fb = *reinterpret_cast<const float4*>(&sb[swz(my_line, my_chunk0 + c)]);
+          va[0] = fa.x; va[1] = fa.y; va[2] = fa.z; va[3] = fa.w;
+          vb[0] = fb.x; vb[1] = fb.y; vb[2] = fb.z; vb[3] = fb.w;
+        } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) o[j] = apply(combine(warp_prefix, ex[k][j]), h_in);
-    if (e0 + 3 < n) {
-      __stcs(reinterpret_cast<float4*>(h + e0), make_float4(o[0], o[1], o[2], o[3]));
-    } else {
+          for (int j = 0; j < 4; ++j) {
+            const int e = e0 + 4 * c + j;
+            va[j] = e < nv ? p.a[tile_base + e] : 1.f;
+            vb[j] = e < nv ? p.b[tile_base + e] : 0.f;
+          }
+        }
+        float o[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if (e0 + j < n) h[e0 + j] = o[j];
+        for (int j = 0; j < 4; ++j) {
+          hcur = (m == 0) ? vb[j] : fmaf(va[j], hcur, vb[j]);
+          o[j] = hcur;
+          if (++m == p.len) m = 0;
+        }
+        if (in_map) {
+          *reinterpret_cast<float4*>(&sa[swz(my_line, my_chunk0 + c)]) = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (e0 + 4 * c + j < nv) p.h[tile_base + e0 + 4 * c + j] = o[j];
+        }
+      }
+      if (in_map) fence_proxy_async_smem();
+      named_bar_sync(kLsConsumerBar, kLsThreads);
+      if (threadIdx.x == 0) {  // hand the stage to the store warp (no store for the tail-only tile)
+        sh.st_line0[ps] = line0 < p.lines ? line0 : (int64_t)0x7fffffff;
+        mbar_arrive(&sh.st_req[ps]);
+      }
     }
+    if (!valid) {
+      if (threadIdx.x == 0) {  // stop the store warp through the (dataless) sentinel stage
+        sh.st_line0[st] = -1;
+        mbar_arrive(&sh.st_req[st]);
+      }
+      break;
+    }
+    prev_tile = tile;
+    prev_r0 = cur_r0;
+    prev_excl = cur_excl;
+    prev_wp = cur_wp;
   }
-  if (threadIdx.x == 0) retire_tile(ws.hdr, (uint32_t)ws.tiles);
+  if (threadIdx.x == 0) retire_tile(ws.hdr, gridDim.x);
 }
+
+int g_ls_grid[64] = {0};
 
 }  // namespace
 
 cudaError_t launch_linscan(const float* a, const float* b, float* h, int64_t rows, int64_t len,
                            const LinscanWorkspace& ws, const LookbackCtl& ctl, cudaStream_t s) {
-  const int64_t n = rows * len;
-  linscan_lookback_kernel<<<(unsigned)ws.tiles, kLsThreads, 0, s>>>(a, b, h, n, len, ws, ctl);
+  LsArgs p{a, b, h, rows * len, len, (rows * len) / kLsRow};
+  if (p.lines > 0x7fffffffLL) return cudaErrorInvalidValue;  // TMA coordinates are 32-bit
+  CUtensorMap map_a{}, map_b{}, map_h{};
+  if (p.lines > 0) {
+    cudaError_t e;
+    const uint64_t row_bytes = kLsRow * sizeof(float);
+    if ((e = encode_tensor_map_2d(&map_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a, kLsRow, p.lines, row_bytes, kLsRow,
+                                  kLsLines, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+      return e;
+    if ((e = encode_tensor_map_2d(&map_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, b, kLsRow, p.lines, row_bytes, kLsRow,
+                                  kLsLines, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+      return e;
+    if ((e = encode_tensor_map_2d(&map_h, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, h, kLsRow, p.lines, row_bytes, kLsRow,
+                                  kLsLines, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+      return e;
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64) return cudaErrorInvalidDevice;
+  const size_t smem = sizeof(LsShared) + 1024;  // + alignment slack
+  if (g_ls_grid[dev] == 0) {
+    e = cudaFuncSetAttribute(linscan_lookback_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int sms = 0, per_sm = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, linscan_lookback_kernel, kLsBlock, smem)) !=
+        cudaSuccess)
+      return e;
+    g_ls_grid[dev] = sms * (per_sm > 0 ? per_sm : 1);
+  }
+  const int64_t cap = g_ls_grid[dev];
+  const unsigned grid = (unsigned)(ws.tiles < cap ? ws.tiles : cap);
+  linscan_lookback_kernel<<<grid, kLsBlock, smem, s>>>(map_a, map_b, map_h, p, ws, ctl);
   return cudaGetLastError();
 }
 

@@ -1,6 +1,7 @@
 // Internal declarations shared by the CUDA sources of the library (not part of the ABI).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap and its enums (types only; the driver is reached through the runtime)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -40,6 +41,14 @@ __host__ __device__ __forceinline__ unsigned long long make_flag(uint32_t epoch,
   return ((unsigned long long)epoch << 32) | (kFlagMagic | kind);
 }
 
+// Scalar-scan tile descriptor: flag word and value in ONE 16-byte word, written and read
+// with single 16-byte accesses, so a reader that sees the flag sees its value and the
+// publisher needs no fence.  kind A: (a, b) = tile aggregate; kind P: b = inclusive prefix.
+struct __align__(16) LsDesc {
+  unsigned long long flag;
+  float a, b;
+};
+
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
   unsigned long long v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -65,6 +74,16 @@ __device__ __forceinline__ float4 ld_relaxed_f4(const float4* p) {
                : "l"(p)
                : "memory");
   return v;
+}
+__device__ __forceinline__ void st_relaxed_desc(LsDesc* p, unsigned long long flag, float a, float b) {
+  const unsigned long long hi = ((unsigned long long)__float_as_uint(b) << 32) | __float_as_uint(a);
+  asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(flag), "l"(hi) : "memory");
+}
+__device__ __forceinline__ void ld_relaxed_desc(const LsDesc* p, unsigned long long& flag, float& a, float& b) {
+  unsigned long long hi;
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(flag), "=l"(hi) : "l"(p) : "memory");
+  a = __uint_as_float((uint32_t)(hi & 0xffffffffull));
+  b = __uint_as_float((uint32_t)(hi >> 32));
 }
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
@@ -101,6 +120,91 @@ __device__ __forceinline__ uint32_t wait_flag(const unsigned long long* flag, Ws
     if (spins > 8) __nanosleep(spins > 256 ? 256 : 32);
   }
 }
+
+// ---- mbarrier + bulk-copy (TMA engine) helpers -----------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+// Named barrier over `count` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for a phase of an mbarrier; false when the limit passed.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16), completing
+// `bytes` of transaction count on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+
+// ---- TMA tensor copies (cp.async.bulk.tensor), 2-D tiles -------------------------------
+// Load box at (x = c0 inner, y = c1 outer) into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+      : "memory");
+}
+// Store a shared-memory box to (c0, c1); elements outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_addr(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's bulk groups still READ shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// Wait until at most N of this thread's bulk groups are incomplete (writes done).
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+// Make this thread's generic-proxy shared-memory writes visible to the async proxy (TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Host: encode a 2-D tiled tensor map (inner dimension contiguous); returns a CUDA error code.
+cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                                 uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                                 CUtensorMapSwizzle swizzle);
 
 // Claim the next look-back tile (thread 0 only).
 __device__ __forceinline__ uint32_t claim_tile(WsHeader* hdr) { return atomicAdd(&hdr->counter, 1u); }
@@ -159,15 +263,29 @@ SsdWorkspace ssd_workspace_layout(const SsdDims& d, void* base);
 
 struct LinscanWorkspace {
   WsHeader* hdr;
-  unsigned long long* flags;  // [tiles]
-  float2* agg;      // [tiles]
-  float2* inc;      // [tiles]
+  LsDesc* desc;     // [tiles]
   int64_t tiles;
   size_t total_bytes;
 };
-constexpr int kLsThreads = 256;
-constexpr int kLsRuns = 4;                            // float4 runs per thread
-constexpr int kLsTile = kLsThreads * 4 * kLsRuns;     // 4096 elements per tile
+#ifndef SSM_LS_LINES
+#define SSM_LS_LINES 128
+#endif
+#ifndef SSM_LS_SPLIT
+#define SSM_LS_SPLIT 2
+#endif
+#ifndef SSM_LS_STAGES
+#define SSM_LS_STAGES 3
+#endif
+#ifndef SSM_LS_MIN_BLOCKS
+#define SSM_LS_MIN_BLOCKS 2
+#endif
+constexpr int kLsLines = SSM_LS_LINES;                // 128-byte lines (32 floats) per tile
+constexpr int kLsRow = 32;                            // elements per line
+constexpr int kLsSplit = SSM_LS_SPLIT;                // consumer threads per line
+constexpr int kLsElems = kLsRow / kLsSplit;           // consecutive elements per consumer thread
+constexpr int kLsThreads = kLsLines * kLsSplit;       // consumer threads
+constexpr int kLsTile = kLsLines * kLsRow;            // elements per tile
+constexpr int kLsStages = SSM_LS_STAGES;              // shared-memory stages of the producer ring
 LinscanWorkspace linscan_workspace_layout(int64_t n, void* base);
 
 // Launchers (return a CUDA error code; 0 = success).

@@ -57,7 +57,8 @@ def test_workspace_sizes(lib):
     states = 4 * 32 * 80 * 64 * 128
     assert w3 >= states * 4 + states * 2
     assert w3 % 256 == 0
-    assert lib.ssm_linscan_workspace_bytes(384, 65536) >= 256 + (384 * 65536 // 4096) * 24
+    # header + one 16-byte descriptor per 4096-element tile
+    assert lib.ssm_linscan_workspace_bytes(384, 65536) >= 256 + (384 * 65536 // 4096) * 16
 
 
 FAKE = 0x10000  # never dereferenced: every call below fails validation first
