@@ -131,6 +131,32 @@ SSM_API ssm_status ssm_linscan_fwd(const float *a, const float *b, float *h, int
                            void *workspace, size_t workspace_bytes, ssm_stream_t stream);
 
 /*
+ * Scalar selective scan for callers that cannot allocate device memory (the pages have no
+ * counterpart; this is a convenience of this library).  Some callers must not allocate once
+ * they are running: a framework that reserves its device memory up front and forbids later
+ * allocation, a real-time loop that cannot afford the implicit device synchronisation of
+ * cudaMalloc / cudaFree, or a host that simply has no allocator to hand out a workspace.
+ * This entry point takes the same a, b, h, rows and len as ssm_linscan_fwd (same layout,
+ * alignment and results, same kernel) but no workspace: the scan's scratch lives in a fixed
+ * device array inside the library, sized for rows * len <= 2^26 elements (67,108,864),
+ * 262,400 bytes that every GPU which loads the library keeps until the process exits.
+ *   - Larger scans return SSM_ERR_UNSUPPORTED without enqueuing anything; use
+ *     ssm_linscan_fwd with a workspace for them.
+ *   - It allocates nothing: no cudaMalloc, cudaFree or allocating library routine.  It
+ *     enqueues a 16-byte cudaMemsetAsync that clears the scratch header, then the kernel.
+ *   - The first call on each device looks up the device address of the scratch array (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the one scratch array, which keeps the previous call's contents.  Calls
+ *     that may overlap on the GPU (different streams without ordering) race and must not be
+ *     issued.
+ *   - Device-side look-back timeouts are not reported by this entry point (there is no
+ *     workspace to pass to ssm_check_device_status); the output of such a call is invalid.
+ * Errors: SSM_ERR_INVALID_ARG, SSM_ERR_ALIGNMENT, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA.
+ */
+SSM_API ssm_status ssm_linscan_fwd_noalloc(const float *a, const float *b, float *h, int64_t rows, int64_t len,
+                                           ssm_stream_t stream);
+
+/*
  * Synchronizes `stream`, reads the device status word at the start of `workspace` (either
  * kind) and returns SSM_OK or the recorded device error (SSM_ERR_TIMEOUT when a bounded wait
  * exceeded its limit; the outputs of that call are then invalid).  After an error it also

@@ -18,7 +18,7 @@ SSM_F32, SSM_BF16 = 0, 1
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ("ssm_status_string", "ssm_version", "ssm_ssd_fwd_workspace_bytes", "ssm_ssd_fwd",
            "ssm_linscan_workspace_bytes", "ssm_linscan_fwd", "ssm_check_device_status",
-           "ssm_debug_set_lookback_fault", "ssm_profile_begin", "ssm_profile_end")
+           "ssm_debug_set_lookback_fault", "ssm_profile_begin", "ssm_profile_end", "ssm_linscan_fwd_noalloc")
 PROFILE_KERNELS = ("linscan_lookback", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan")
 
 _lib = None
@@ -49,6 +49,8 @@ def _declare(lib):
     lib.ssm_check_device_status.restype = i32
     lib.ssm_debug_set_lookback_fault.argtypes = [i64, u64]
     lib.ssm_debug_set_lookback_fault.restype = None
+    lib.ssm_linscan_fwd_noalloc.argtypes = [vp, vp, vp, i64, i64, vp]
+    lib.ssm_linscan_fwd_noalloc.restype = i32
     lib.ssm_profile_begin.argtypes = [i32]
     lib.ssm_profile_begin.restype = i32
     lib.ssm_profile_end.argtypes = [vp, vp]
