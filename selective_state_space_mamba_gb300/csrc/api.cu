@@ -15,7 +15,7 @@ cudaError_t launch_ssd_chunk_scan_simt(const void* x, const void* B, const void*
                                        const SsdDims& d, const SsdWorkspace& ws, cudaStream_t s);
 bool ssd_tc_supported(const SsdDims& d);
 cudaError_t launch_ssd_chunk_state_tc(const void* x, const void* B, const SsdDims& d, const SsdWorkspace& ws,
-                                      cudaStream_t s);
+                                      const LookbackCtl& ctl, cudaStream_t s);
 cudaError_t launch_ssd_chunk_scan_tc(const void* x, const void* B, const void* C, const float* D, void* y,
                                      const SsdDims& d, const SsdWorkspace& ws, cudaStream_t s);
 
@@ -158,12 +158,11 @@ LinscanWorkspace linscan_workspace_layout(int64_t n, void* base) {
   return w;
 }
 
-cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
-                                 uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
-                                 CUtensorMapSwizzle swizzle) {
-  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+namespace {
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+cudaError_t get_encoder(EncodeFn* out) {
   static EncodeFn encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -172,6 +171,31 @@ cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, co
     if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorUnknown;
     encode = reinterpret_cast<EncodeFn>(fn);
   }
+  *out = encode;
+  return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, const uint64_t dims[3],
+                                 const uint64_t strides_bytes[2], const uint32_t box[3], CUtensorMapSwizzle swizzle) {
+  EncodeFn encode;
+  const cudaError_t e = get_encoder(&encode);
+  if (e != cudaSuccess) return e;
+  const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  const cuuint64_t st[2] = {strides_bytes[0], strides_bytes[1]};
+  const cuuint32_t bx[3] = {box[0], box[1], box[2]};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = encode(map, dtype, 3, const_cast<void*>(base), d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                                 uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                                 CUtensorMapSwizzle swizzle) {
+  EncodeFn encode;
+  const cudaError_t ge = get_encoder(&encode);
+  if (ge != cudaSuccess) return ge;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {row_stride_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
@@ -240,17 +264,18 @@ ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void
   const SsdWorkspace ws = ssd_workspace_layout(d, workspace);
   const LookbackCtl ctl = next_lookback_ctl();
 
-  const bool tc = ssd_tc_supported(d);
+  const bool state_tc = ssd_tc_supported(d);
+  const bool scan_tc = false;
   if (timed_launch(1, s, [&] { return launch_ssd_chunk_cumsum(dt, A, d, ws, s); }) != cudaSuccess)
     return SSM_ERR_CUDA;
   if (timed_launch(2, s, [&] {
-        return tc ? launch_ssd_chunk_state_tc(x, B, d, ws, s) : launch_ssd_chunk_state_simt(x, B, d, ws, s);
+        return state_tc ? launch_ssd_chunk_state_tc(x, B, d, ws, ctl, s) : launch_ssd_chunk_state_simt(x, B, d, ws, s);
       }) != cudaSuccess)
     return SSM_ERR_CUDA;
   if (timed_launch(3, s, [&] { return launch_ssd_state_passing(h0, h_final, d, ws, ctl, s); }) != cudaSuccess)
     return SSM_ERR_CUDA;
   if (timed_launch(4, s, [&] {
-        return tc ? launch_ssd_chunk_scan_tc(x, B, C, D, y, d, ws, s)
+        return scan_tc ? launch_ssd_chunk_scan_tc(x, B, C, D, y, d, ws, s)
                   : launch_ssd_chunk_scan_simt(x, B, C, D, y, d, ws, s);
       }) != cudaSuccess)
     return SSM_ERR_CUDA;

@@ -1,13 +1,317 @@
-// Tensor-core (tcgen05 / TMEM / TMA) kernels for the bf16 chunk contractions.
-#include "ssm_internal.cuh"
+// Tensor-core (tcgen05 / TMEM / TMA) kernels for the bf16 chunk contractions of the Mamba-2
+// SSD forward.
+//
+// ssd_chunk_state_tc: the decayed jump term of "Accelerating Mamba-2 with High-Performance
+// Forward Pass Kernels in NVIDIA CUDA Tile", "Kernel 2: fwd_pass_state":
+//     S_c = X^T (w . B),  w_t = dt_t 2^(G_last - G_t)          (H x S per batch, chunk, head)
+// computed per chunk in parallel (the chunk loop of the post's kernel becomes the separate
+// state-passing scan).  The weighted X is split into bf16 hi + lo parts (lo = the rounding
+// remainder) and both are multiplied, so the weighting costs no bf16 rounding (2^-18 instead of
+// 2^-9 relative): the chunk states feed h_final, whose tolerance a single bf16 rounding of
+// x * w exceeds.  One MMA tile covers TWO heads of the same B/C group: M = 128 rows
+// (64 p-values of each head), N = S = 128, K = the chunk's tokens.  Both operands are
+// MN-major in shared memory, exactly as TMA lands them in 128-byte swizzle: A = X (p
+// contiguous), B = the group's B (s contiguous).  The per-token weight is applied to X in
+// shared memory (the post scales B instead; B is shared by the heads of a group here, so the
+// per-head weight goes on X — the "swap A/B" idea of the post's optimisation section read the
+// other way round).
+//
+// CTA = (batch, chunk, group, run of head pairs), warp-specialised:
+//   warp 0      TMA producer: B once, then X of each head pair, in 128-token halves, into a
+//               2-stage ring
+//   warp 1      TMEM owner and MMA issuer (one thread): K/16 MMAs per pair into one of two
+//               128-column f32 accumulators, tcgen05.commit to free the stage and hand the
+//               accumulator to the epilogue
+//   warps 2-5   scale X in shared memory by w (per head and token) into hi + lo parts, then
+//               release them to the MMA
+//   warps 6-9   epilogue: TMEM -> registers -> S_c (f32), then free the accumulator
+// Every wait is bounded; on expiry the CTA records SSM_ERR_TIMEOUT, drains, frees its TMEM
+// and returns.
+#include "tc_common.cuh"
 
 namespace ssm {
+namespace {
 
-bool ssd_tc_supported(const SsdDims&) { return false; }
+constexpr int kCsWarps = 10;
+constexpr int kCsThreads = kCsWarps * 32;
+constexpr int kCsMaxT = 256;
+constexpr int kCsKH = 128;        // tokens per stage (a chunk of 256 takes two stages)
+constexpr int kCsRowBytes = 128;  // 64 bf16 per swizzled row
+constexpr uint32_t kCsScaleBar = 1, kCsEpiBar = 2;
+constexpr uint32_t kCsTmemCols = 256;  // two 128-column accumulators
 
-cudaError_t launch_ssd_chunk_state_tc(const void*, const void*, const SsdDims&, const SsdWorkspace&, cudaStream_t) {
-  return cudaErrorNotSupported;
+struct CsParams {
+  const float* G;
+  const float* dtT;
+  float* Sc;
+  WsHeader* hdr;
+  int64_t lpad, nchunks;
+  int nheads, ngroups, chunk;
+  int pairs_per_item, items_per_group;
+};
+
+// Shared-memory layout (offsets from a 1024-byte aligned base), chunk size T, stage tokens KH:
+//   stage[2] = { hi[2 heads][KH rows][128 B], lo[2 heads][KH rows][128 B] }   swizzled
+//   bm[s block][T rows][128 B]                                                 swizzled
+//   w[stage][2 heads][KH] f32, barriers, TMEM base, abort flag
+struct CsLayout {
+  uint32_t kh, stage_bytes, half_bytes, bm0, w0, bars, total;
+  __host__ __device__ explicit CsLayout(int T) {
+    kh = T < kCsKH ? T : kCsKH;
+    half_bytes = 2u * kh * kCsRowBytes;  // one of hi / lo for the two heads
+    stage_bytes = 2u * half_bytes;
+    bm0 = 2u * stage_bytes;
+    w0 = bm0 + 2u * T * kCsRowBytes;
+    bars = w0 + 2u * 2u * kh * 4u;
+    total = bars + 16 * 8 + 16;
+  }
+};
+enum CsBar { kBFull = 0, kXFull = 1, kXScaled = 3, kXEmpty = 5, kAccFull = 7, kAccEmpty = 9, kDone = 11, kNumBars = 12 };
+
+__global__ void __launch_bounds__(kCsThreads, 1)
+    ssd_chunk_state_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_b,
+                              CsParams p, LookbackCtl ctl) {
+  extern __shared__ unsigned char cs_raw[];
+  const uint32_t raw = smem_addr(cs_raw);
+  unsigned char* base = cs_raw + ((1024u - (raw & 1023u)) & 1023u);
+  const int T = p.chunk;
+  const CsLayout L(T);
+  const int KH = (int)L.kh;
+  const int nk = T / KH;  // stages per head pair
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.bars + kNumBars * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.bars + kNumBars * 8 + 4);
+  float* wbuf = reinterpret_cast<float*>(base + L.w0);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // work item -> (batch, chunk, group, first pair)
+  int64_t item = blockIdx.x;
+  const int k_item = (int)(item % p.items_per_group);
+  item /= p.items_per_group;
+  const int g = (int)(item % p.ngroups);
+  item /= p.ngroups;
+  const int64_t c = item % p.nchunks;
+  const int64_t bi = item / p.nchunks;
+  const int hpg = p.nheads / p.ngroups;
+  const int ppg = hpg / 2;
+  const int q0 = k_item * p.pairs_per_item;
+  const int nq = min(p.pairs_per_item, ppg - q0);
+  const int nsteps = nq * nk;  // (pair, token half) steps through the stage ring
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);  // every barrier has one arriving thread
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, kCsTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  auto fail = [&](void) {
+    record_error(p.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------------------
+    if (lane == 0 && nsteps > 0) {
+      mbar_arrive_expect_tx(&bars[kBFull], 2u * T * kCsRowBytes);
+      for (int sb = 0; sb < 2; ++sb)
+        tc::tma_load_3d(base + L.bm0 + sb * T * kCsRowBytes, &map_b, g * 128 + sb * 64, (int)(c * T), (int)bi,
+                        &bars[kBFull]);
+      int issued = 0;
+      for (int i = 0; i < nsteps && !*abort_flag; ++i) {
+        const int st = i & 1;
+        if (i >= 2 && !mbar_wait(&bars[kXEmpty + st], (uint32_t)((i >> 1) - 1) & 1u, ctl.spin_limit_ns)) {
+          fail();
+          break;
+        }
+        const int q = i / nk, kh = i % nk;
+        const int h = g * hpg + 2 * (q0 + q);
+        mbar_arrive_expect_tx(&bars[kXFull + st], L.half_bytes);
+        for (int hh = 0; hh < 2; ++hh)
+          tc::tma_load_3d(base + st * L.stage_bytes + hh * KH * kCsRowBytes, &map_x, (h + hh) * 64,
+                          (int)(c * T + kh * KH), (int)bi, &bars[kXFull + st]);
+        issued = i + 1;
+      }
+      // leave no copy in flight: the last loads of each stage have landed (bounded)
+      for (int i = max(0, issued - 2); i < issued; ++i)
+        mbar_wait(&bars[kXFull + (i & 1)], (uint32_t)(i >> 1) & 1u, ctl.spin_limit_ns);
+      mbar_wait(&bars[kBFull], 0, ctl.spin_limit_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ---------------------------------------------
+    if (lane == 0 && nsteps > 0) {
+      const uint32_t idesc = tc::idesc_bf16_f32(128, 128, /*a_mn=*/true, /*b_mn=*/true);
+      const uint32_t a_lbo = KH * kCsRowBytes;  // head 0 block -> head 1 block (MN blocks)
+      const uint32_t b_lbo = T * kCsRowBytes;   // s 0..63 block -> s 64..127 block
+      const uint32_t sbo = 8 * kCsRowBytes;     // next 8-token group
+      bool ok = mbar_wait(&bars[kBFull], 0, ctl.spin_limit_ns);
+      if (!ok) fail();
+      for (int i = 0; i < nsteps && ok && !*abort_flag; ++i) {
+        const int st = i & 1;
+        const int q = i / nk, kh = i % nk, acc = q & 1;
+        if (!mbar_wait(&bars[kXScaled + st], (uint32_t)(i >> 1) & 1u, ctl.spin_limit_ns) ||
+            (kh == 0 && q >= 2 && !mbar_wait(&bars[kAccEmpty + acc], (uint32_t)((q >> 1) - 1) & 1u, ctl.spin_limit_ns))) {
+          fail();
+          break;
+        }
+        tc::fence_after_sync();
+        const uint32_t hi0 = smem_addr(base + st * L.stage_bytes);
+        const uint32_t lo0 = hi0 + L.half_bytes;
+        const uint32_t b0 = smem_addr(base + L.bm0) + kh * KH * kCsRowBytes;
+        for (int ks = 0; ks < KH / 16; ++ks) {
+          const uint32_t koff = ks * 16 * kCsRowBytes;  // 16 tokens = two 8-row groups
+          const uint64_t bdesc = tc::sdesc_sw128(b0 + koff, b_lbo, sbo);
+          tc::mma_bf16(tmem + acc * 128, tc::sdesc_sw128(hi0 + koff, a_lbo, sbo), bdesc, idesc, kh > 0 || ks > 0);
+          tc::mma_bf16(tmem + acc * 128, tc::sdesc_sw128(lo0 + koff, a_lbo, sbo), bdesc, idesc, true);
+        }
+        tc::mma_commit(&bars[kXEmpty + st]);                   // the stage may be refilled
+        if (kh == nk - 1) tc::mma_commit(&bars[kAccFull + acc]);  // the accumulator is ready
+      }
+      tc::mma_commit(&bars[kDone]);
+      mbar_wait(&bars[kDone], 0, ctl.spin_limit_ns);  // every MMA has completed
+    }
+  } else if (warp < 6) {
+    // ---------------- scale X by w, split into bf16 hi + lo parts --------------------------
+    const int t = threadIdx.x - 64;  // 0..127
+    const int64_t bh0 = bi * p.nheads;
+    for (int i = 0; i < nsteps; ++i) {
+      const int st = i & 1;
+      const int q = i / nk, kh = i % nk;
+      const int h = g * hpg + 2 * (q0 + q);
+      // weights of the pair's two heads for these tokens: w_t = dt_t 2^(G_last - G_t)
+      float* w = wbuf + st * 2 * KH;
+      for (int j = t; j < 2 * KH; j += 128) {
+        const int hh = j / KH, tok = kh * KH + j % KH;
+        const int64_t row = (bh0 + h + hh) * p.lpad + c * T;
+        w[j] = p.dtT[row + tok] * exp2f(p.G[row + T - 1] - p.G[row + tok]);
+      }
+      if (!mbar_wait(&bars[kXFull + st], (uint32_t)(i >> 1) & 1u, ctl.spin_limit_ns)) {
+        if (t == 0) fail();
+        break;
+      }
+      named_bar_sync(kCsScaleBar, 128);  // w complete
+      // every 16-byte chunk holds 8 p-values of one token row of one head
+      uint4* hi = reinterpret_cast<uint4*>(base + st * L.stage_bytes);
+      uint4* lo = reinterpret_cast<uint4*>(base + st * L.stage_bytes + L.half_bytes);
+      const int nchunk = 2 * KH * 8;
+      for (int j = t; j < nchunk; j += 128) {
+        const float wv = w[j >> 3];  // row = head * KH + token
+        uint4 v = hi[j], r;
+        __nv_bfloat162* e = reinterpret_cast<__nv_bfloat162*>(&v);
+        __nv_bfloat162* f = reinterpret_cast<__nv_bfloat162*>(&r);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 xv = __bfloat1622float2(e[k]);
+          const float2 s = make_float2(xv.x * wv, xv.y * wv);
+          e[k] = __floats2bfloat162_rn(s.x, s.y);
+          const float2 sh = __bfloat1622float2(e[k]);
+          f[k] = __floats2bfloat162_rn(s.x - sh.x, s.y - sh.y);
+        }
+        hi[j] = v;
+        lo[j] = r;
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kCsScaleBar, 128);
+      if (t == 0) mbar_arrive(&bars[kXScaled + st]);
+    }
+  } else {
+    // ------------------------------ epilogue: TMEM -> S_c ----------------------------------
+    const int quad = warp & 3;       // TMEM lanes 32*quad .. +31
+    const int m = quad * 32 + lane;  // accumulator row
+    const int hh = m >> 6, pp = m & 63;
+    const int S = 128;
+    for (int q = 0; q < nq; ++q) {
+      const int acc = q & 1;
+      if (!mbar_wait(&bars[kAccFull + acc], (uint32_t)(q >> 1) & 1u, ctl.spin_limit_ns)) {
+        if (threadIdx.x == 192) fail();
+        break;
+      }
+      tc::fence_after_sync();
+      const int h = g * hpg + 2 * (q0 + q) + hh;
+      float* out = p.Sc + ((((bi * p.nchunks + c) * p.nheads + h) * 64 + pp) * (int64_t)S);
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t r[32];
+        tc::tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + acc * 128 + cb * 32, r);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          reinterpret_cast<float4*>(out + cb * 32)[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                                    __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+      }
+      tc::fence_before_sync();
+      named_bar_sync(kCsEpiBar, 128);
+      if (threadIdx.x == 192) mbar_arrive(&bars[kAccEmpty + acc]);
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kCsTmemCols);
+  }
 }
+
+}  // namespace
+
+bool ssd_tc_supported(const SsdDims& d) {
+  return d.dtype == SSM_BF16 && d.headdim == 64 && d.dstate == 128 && (d.nheads / d.ngroups) % 2 == 0 &&
+         d.chunk <= kCsMaxT;
+}
+
+cudaError_t launch_ssd_chunk_state_tc(const void* x, const void* B, const SsdDims& d, const SsdWorkspace& ws,
+                                      const LookbackCtl& ctl, cudaStream_t s) {
+  CUtensorMap map_x, map_b;
+  const uint64_t xd[3] = {(uint64_t)d.nheads * 64, (uint64_t)d.seqlen, (uint64_t)d.batch};
+  const uint64_t xs[2] = {(uint64_t)d.nheads * 64 * 2, (uint64_t)d.seqlen * d.nheads * 64 * 2};
+  const uint64_t bd[3] = {(uint64_t)d.ngroups * 128, (uint64_t)d.seqlen, (uint64_t)d.batch};
+  const uint64_t bs[2] = {(uint64_t)d.ngroups * 128 * 2, (uint64_t)d.seqlen * d.ngroups * 128 * 2};
+  const uint32_t xbox[3] = {64, CsLayout(d.chunk).kh, 1};
+  const uint32_t bbox[3] = {64, (uint32_t)d.chunk, 1};
+  cudaError_t e;
+  if ((e = encode_tensor_map_3d(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, xd, xs, xbox, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+      cudaSuccess)
+    return e;
+  if ((e = encode_tensor_map_3d(&map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, bd, bs, bbox, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+      cudaSuccess)
+    return e;
+  CsParams p;
+  p.G = ws.G;
+  p.dtT = ws.dtT;
+  p.Sc = ws.Sc;
+  p.hdr = ws.hdr;
+  p.lpad = d.lpad;
+  p.nchunks = d.nchunks;
+  p.nheads = d.nheads;
+  p.ngroups = d.ngroups;
+  p.chunk = d.chunk;
+  const int ppg = d.nheads / d.ngroups / 2;
+  int dev = 0, sms = 148;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  // split each group's pairs into runs so that there are about two CTAs per SM or more
+  const int64_t groups_total = d.batch * d.nchunks * d.ngroups;
+  int items = (int)((2 * (int64_t)sms + groups_total - 1) / groups_total);
+  items = items < 1 ? 1 : (items > ppg ? ppg : items);
+  p.pairs_per_item = (ppg + items - 1) / items;
+  p.items_per_group = (ppg + p.pairs_per_item - 1) / p.pairs_per_item;
+  const CsLayout L(d.chunk);
+  const size_t smem = L.total + 1024;
+  if ((e = cudaFuncSetAttribute(ssd_chunk_state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+      cudaSuccess)
+    return e;
+  const int64_t grid = groups_total * p.items_per_group;
+  ssd_chunk_state_tc_kernel<<<(unsigned)grid, kCsThreads, smem, s>>>(map_x, map_b, p, ctl);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_ssd_chunk_scan_tc(const void*, const void*, const void*, const float*, void*, const SsdDims&,
                                      const SsdWorkspace&, cudaStream_t) {
   return cudaErrorNotSupported;

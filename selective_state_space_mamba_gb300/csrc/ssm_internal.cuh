@@ -206,6 +206,10 @@ cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, co
                                  uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
                                  CUtensorMapSwizzle swizzle);
 
+// Host: encode a 3-D tiled tensor map (dims[0] contiguous; strides of dims 1 and 2 in bytes).
+cudaError_t encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, const uint64_t dims[3],
+                                 const uint64_t strides_bytes[2], const uint32_t box[3], CUtensorMapSwizzle swizzle);
+
 // Claim the next look-back tile (thread 0 only).
 __device__ __forceinline__ uint32_t claim_tile(WsHeader* hdr) { return atomicAdd(&hdr->counter, 1u); }
 
