@@ -16,8 +16,10 @@ cudaError_t launch_ssd_chunk_scan_simt(const void* x, const void* B, const void*
 bool ssd_tc_supported(const SsdDims& d);
 cudaError_t launch_ssd_chunk_state_tc(const void* x, const void* B, const SsdDims& d, const SsdWorkspace& ws,
                                       const LookbackCtl& ctl, cudaStream_t s);
+bool ssd_scan_tc_supported(const SsdDims& d);
 cudaError_t launch_ssd_chunk_scan_tc(const void* x, const void* B, const void* C, const float* D, void* y,
-                                     const SsdDims& d, const SsdWorkspace& ws, cudaStream_t s);
+                                     const SsdDims& d, const SsdWorkspace& ws, const LookbackCtl& ctl,
+                                     cudaStream_t s);
 
 namespace {
 
@@ -265,7 +267,7 @@ ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void
   const LookbackCtl ctl = next_lookback_ctl();
 
   const bool state_tc = ssd_tc_supported(d);
-  const bool scan_tc = false;
+  const bool scan_tc = ssd_scan_tc_supported(d);
   if (timed_launch(1, s, [&] { return launch_ssd_chunk_cumsum(dt, A, d, ws, s); }) != cudaSuccess)
     return SSM_ERR_CUDA;
   if (timed_launch(2, s, [&] {
@@ -275,7 +277,7 @@ ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void
   if (timed_launch(3, s, [&] { return launch_ssd_state_passing(h0, h_final, d, ws, ctl, s); }) != cudaSuccess)
     return SSM_ERR_CUDA;
   if (timed_launch(4, s, [&] {
-        return scan_tc ? launch_ssd_chunk_scan_tc(x, B, C, D, y, d, ws, s)
+        return scan_tc ? launch_ssd_chunk_scan_tc(x, B, C, D, y, d, ws, ctl, s)
                   : launch_ssd_chunk_scan_simt(x, B, C, D, y, d, ws, s);
       }) != cudaSuccess)
     return SSM_ERR_CUDA;

@@ -312,9 +312,4 @@ cudaError_t launch_ssd_chunk_state_tc(const void* x, const void* B, const SsdDim
   return cudaGetLastError();
 }
 
-cudaError_t launch_ssd_chunk_scan_tc(const void*, const void*, const void*, const float*, void*, const SsdDims&,
-                                     const SsdWorkspace&, cudaStream_t) {
-  return cudaErrorNotSupported;
-}
-
 }  // namespace ssm
