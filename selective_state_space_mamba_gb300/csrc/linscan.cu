@@ -273,12 +273,12 @@ __global__ void __launch_bounds__(kLsBlock, SSM_LS_MIN_BLOCKS)
   int64_t prev_tile = -1, prev_r0 = 0;
   for (int it = 0;; ++it) {
     const int st = it % kLsStages;
-    int64_t tile = ws.tiles;  // stop unless a tile arrives
-    if (mbar_wait(&sh.full[st], (uint32_t)(it / kLsStages) & 1u, ctl.spin_limit_ns)) {
-      tile = sh.tile[st];
-    } else if (threadIdx.x == 0) {
-      record_error(ws.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
-    }
+    // A wait that gave up in any consumer stops all of them, so that none is left behind in
+    // a later barrier.
+    const bool got = mbar_wait(&sh.full[st], (uint32_t)(it / kLsStages) & 1u, ctl.spin_limit_ns);
+    const bool gave_up = named_bar_any(kLsConsumerBar, kLsThreads, !got);
+    if (gave_up && threadIdx.x == 0) record_error(ws.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
+    const int64_t tile = gave_up ? ws.tiles : sh.tile[st];  // ws.tiles: stop
     const bool valid = tile < ws.tiles;  // uniform across the consumers
     Pair cur_excl{1.f, 0.f}, cur_wp{1.f, 0.f};
     int64_t cur_r0 = 0;

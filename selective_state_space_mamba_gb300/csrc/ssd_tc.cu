@@ -191,11 +191,12 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         const int64_t row = (bh0 + h + hh) * p.lpad + c * T;
         w[j] = p.dtT[row + tok] * exp2f(p.G[row + T - 1] - p.G[row + tok]);
       }
-      if (!mbar_wait(&bars[kXFull + st], (uint32_t)(i >> 1) & 1u, ctl.spin_limit_ns)) {
+      // w complete; a wait that gave up in any scaler thread ends the loop in all of them
+      const bool bad = !mbar_wait(&bars[kXFull + st], (uint32_t)(i >> 1) & 1u, ctl.spin_limit_ns);
+      if (named_bar_any(kCsScaleBar, 128, bad)) {
         if (t == 0) fail();
         break;
       }
-      named_bar_sync(kCsScaleBar, 128);  // w complete
       // every 16-byte chunk holds 8 p-values of one token row of one head
       uint4* hi = reinterpret_cast<uint4*>(base + st * L.stage_bytes);
       uint4* lo = reinterpret_cast<uint4*>(base + st * L.stage_bytes + L.half_bytes);
@@ -228,7 +229,8 @@ __global__ void __launch_bounds__(kCsThreads, 1)
     const int S = 128;
     for (int q = 0; q < nq; ++q) {
       const int acc = q & 1;
-      if (!mbar_wait(&bars[kAccFull + acc], (uint32_t)(q >> 1) & 1u, ctl.spin_limit_ns)) {
+      const bool bad = !mbar_wait(&bars[kAccFull + acc], (uint32_t)(q >> 1) & 1u, ctl.spin_limit_ns);
+      if (named_bar_any(kCsEpiBar, 128, bad)) {  // leave together, or not at all
         if (threadIdx.x == 192) fail();
         break;
       }

@@ -116,5 +116,13 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
                : "memory");
 }
 
+// 2^x with the hardware approximation (ex2.approx.ftz.f32: a few ulp, -inf -> 0).  Used for
+// decay weights that end up in bf16 operands.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 }  // namespace tc
 }  // namespace ssm
