@@ -8,8 +8,10 @@
 // at the same time, with 0 in the padding of the last chunk (decay 1, no input: exact).
 //
 // One CTA per (chunk, block of 32 heads, batch): the dt tile [chunk, 32 heads] is staged
-// through shared memory so both the read (heads contiguous) and the write (tokens
-// contiguous) are coalesced; each warp then scans whole head rows.
+// through shared memory so both the read (heads contiguous) and the writes (tokens
+// contiguous) are coalesced: each warp scans whole head rows in registers, and the results
+// go back through the same shared tile, so that every warp store writes 128 contiguous bytes
+// of one head row.
 #include "ssm_internal.cuh"
 
 namespace ssm {
@@ -17,6 +19,7 @@ namespace {
 
 constexpr int kCsHeads = 32;
 constexpr int kCsThreads = 256;
+constexpr int kCsMaxChunk = 256;
 
 template <typename DtT>
 __global__ void __launch_bounds__(kCsThreads) ssd_chunk_cumsum_kernel(const DtT* __restrict__ dt,
@@ -37,25 +40,38 @@ __global__ void __launch_bounds__(kCsThreads) ssd_chunk_cumsum_kernel(const DtT*
     hdr->done = 0u;
   }
 
-  for (int idx = threadIdx.x; idx < T * kCsHeads; idx += kCsThreads) {
+  // all of a thread's loads are issued before the first is used (one memory latency, not 32)
+  constexpr int kLoads = kCsMaxChunk * kCsHeads / kCsThreads;
+  float v[kLoads];
+#pragma unroll
+  for (int k = 0; k < kLoads; ++k) {
+    const int idx = threadIdx.x + k * kCsThreads;
     const int t = idx / kCsHeads, hh = idx % kCsHeads;
-    float v = 0.f;
-    if (hh < nhb && t0 + t < d.seqlen) v = to_f32(dt[((bi * d.seqlen) + t0 + t) * nh + h0 + hh]);
-    s_dt[t * (kCsHeads + 1) + hh] = v;
+    v[k] = 0.f;
+    if (t < T && hh < nhb && t0 + t < d.seqlen) v[k] = to_f32(dt[((bi * d.seqlen) + t0 + t) * nh + h0 + hh]);
+  }
+#pragma unroll
+  for (int k = 0; k < kLoads; ++k) {
+    const int idx = threadIdx.x + k * kCsThreads;
+    if (idx < T * kCsHeads) s_dt[(idx / kCsHeads) * (kCsHeads + 1) + idx % kCsHeads] = v[k];
   }
   __syncthreads();
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int per_lane = T / 32;  // chunk is a multiple of 64
-  for (int hh = warp; hh < nhb; hh += kCsThreads / 32) {
-    const float Ah = A[h0 + hh];
+  const int per_lane = T / 32;  // chunk is a multiple of 64 and at most 256
+  constexpr int kWarps = kCsThreads / 32;
+  constexpr int kHeadsPerWarp = kCsHeads / kWarps;
+  float gv[kHeadsPerWarp][8];
+#pragma unroll
+  for (int q = 0; q < kHeadsPerWarp; ++q) {
+    const int hh = warp + q * kWarps;
+    const float Ah = hh < nhb ? A[h0 + hh] : 0.f;
     float run = 0.f;
-    float vals[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       if (k < per_lane) {
         run += Ah * s_dt[(lane * per_lane + k) * (kCsHeads + 1) + hh];
-        vals[k] = run;
+        gv[q][k] = run;
       }
     }
     // exclusive prefix of the lane totals
@@ -66,16 +82,28 @@ __global__ void __launch_bounds__(kCsThreads) ssd_chunk_cumsum_kernel(const DtT*
       if (lane >= off) incl += o;
     }
     const float excl = incl - run;
-    const int64_t row = (bi * nh + h0 + hh) * d.lpad + t0;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (k < per_lane) {
-        const int t = lane * per_lane + k;
-        G[row + t] = (excl + vals[k]) * kLog2e;
-        dtT[row + t] = s_dt[t * (kCsHeads + 1) + hh];
-      }
-    }
+    for (int k = 0; k < 8; ++k) gv[q][k] = (excl + gv[q][k]) * kLog2e;
   }
+
+  // dt^T rows, then G rows, each warp writing 32 consecutive tokens of one head per store
+  auto store_rows = [&](float* dst) {
+    for (int idx = threadIdx.x; idx < nhb * T; idx += kCsThreads) {
+      const int hh = idx / T, t = idx % T;
+      dst[(bi * nh + h0 + hh) * d.lpad + t0 + t] = s_dt[t * (kCsHeads + 1) + hh];
+    }
+  };
+  store_rows(dtT);
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < kHeadsPerWarp; ++q) {
+    const int hh = warp + q * kWarps;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (k < per_lane) s_dt[(lane * per_lane + k) * (kCsHeads + 1) + hh] = gv[q][k];
+  }
+  __syncthreads();
+  store_rows(G);
 }
 
 }  // namespace

@@ -16,14 +16,23 @@
 // per-head weight goes on X — the "swap A/B" idea of the post's optimisation section read the
 // other way round).
 //
-// CTA = (batch, chunk, group, run of head pairs), warp-specialised:
-//   warp 0      TMA producer: B once, then X of each head pair, in 128-token halves, into a
-//               2-stage ring
-//   warp 1      TMEM owner and MMA issuer (one thread): K/16 MMAs per pair into one of two
-//               128-column f32 accumulators, tcgen05.commit to free the stage and hand the
-//               accumulator to the epilogue
-//   warps 2-5   scale X in shared memory by w (per head and token) into hi + lo parts, then
-//               release them to the MMA
+// The weighted X and its remainder come from three bf16x2 FMAs per pair of values, each with
+// one rounding: w is split into w_hi + w_lo (bf16 each); hi = x w_hi rounded; hi - x w_hi is
+// then exact (a 16-bit product minus its own 8-bit rounding); lo = x w - hi is that remainder
+// plus x w_lo, rounded once.  hi + lo equals x w to about 2^-17 relative.
+//
+// Work unit = (batch, chunk, group, head pair).  The units are split into one contiguous
+// range per CTA (one CTA per SM, so every SM gets the same number of units, give or take
+// one); a CTA reloads B only where its range crosses into the next (batch, chunk, group).
+// CTA warps:
+//   warp 0      TMA producer: B when the group changes; X of the pair's two heads, 64 tokens
+//               at a time, with those tokens' G and dt and the chunk's last G, into a 4-stage
+//               ring
+//   warp 1      TMEM owner and MMA issuer (one thread): 2 x 4 MMAs (hi, lo) per stage into one
+//               of two 128-column f32 accumulators; tcgen05.commit frees the stage, and after
+//               the last stage of a unit hands the accumulator to the epilogue
+//   warps 2-5   one token row of one head per thread: w = dt 2^(G_last - G_t), then the row's
+//               64 values of X in shared memory -> hi (in place) and lo
 //   warps 6-9   epilogue: TMEM -> registers -> S_c (f32), then free the accumulator
 // Every wait is bounded; on expiry the CTA records SSM_ERR_TIMEOUT, drains, frees its TMEM
 // and returns.
@@ -35,38 +44,71 @@ namespace {
 constexpr int kCsWarps = 10;
 constexpr int kCsThreads = kCsWarps * 32;
 constexpr int kCsMaxT = 256;
-constexpr int kCsKH = 128;        // tokens per stage (a chunk of 256 takes two stages)
+constexpr int kCsKH = 64;         // tokens per stage
+constexpr int kCsStages = 4;
 constexpr int kCsRowBytes = 128;  // 64 bf16 per swizzled row
 constexpr uint32_t kCsScaleBar = 1, kCsEpiBar = 2;
 constexpr uint32_t kCsTmemCols = 256;  // two 128-column accumulators
+// per stage and head: G of the stage's tokens, dt of the stage's tokens, the chunk's last 4 G
+constexpr uint32_t kCsGdHead = (2 * kCsKH + 4) * 4;
 
 struct CsParams {
   const float* G;
   const float* dtT;
   float* Sc;
   WsHeader* hdr;
-  int64_t lpad, nchunks;
+  int64_t lpad, nchunks, units;
   int nheads, ngroups, chunk;
-  int pairs_per_item, items_per_group;
 };
 
-// Shared-memory layout (offsets from a 1024-byte aligned base), chunk size T, stage tokens KH:
-//   stage[2] = { hi[2 heads][KH rows][128 B], lo[2 heads][KH rows][128 B] }   swizzled
+// Shared-memory layout (offsets from a 1024-byte aligned base), chunk size T:
+//   stage[4] = { hi[2 heads][64 rows][128 B], lo[2 heads][64 rows][128 B] }   swizzled
 //   bm[s block][T rows][128 B]                                                 swizzled
-//   w[stage][2 heads][KH] f32, barriers, TMEM base, abort flag
+//   gd[4 stages][2 heads] = { G[64], dt[64], G[T-4 .. T-1] }
+//   barriers, TMEM base, abort flag
 struct CsLayout {
-  uint32_t kh, stage_bytes, half_bytes, bm0, w0, bars, total;
+  uint32_t half_bytes, stage_bytes, bm0, gd0, bars, total;
   __host__ __device__ explicit CsLayout(int T) {
-    kh = T < kCsKH ? T : kCsKH;
-    half_bytes = 2u * kh * kCsRowBytes;  // one of hi / lo for the two heads
+    half_bytes = 2u * kCsKH * kCsRowBytes;
     stage_bytes = 2u * half_bytes;
-    bm0 = 2u * stage_bytes;
-    w0 = bm0 + 2u * T * kCsRowBytes;
-    bars = w0 + 2u * 2u * kh * 4u;
-    total = bars + 16 * 8 + 16;
+    bm0 = kCsStages * stage_bytes;
+    gd0 = bm0 + 2u * T * kCsRowBytes;
+    bars = gd0 + kCsStages * 2u * kCsGdHead;
+    total = bars + 24 * 8 + 16;
   }
 };
-enum CsBar { kBFull = 0, kXFull = 1, kXScaled = 3, kXEmpty = 5, kAccFull = 7, kAccEmpty = 9, kDone = 11, kNumBars = 12 };
+enum CsBar {
+  kBFull = 0, kXFull = 1, kXScaled = kXFull + kCsStages, kXEmpty = kXScaled + kCsStages,
+  kAccFull = kXEmpty + kCsStages, kAccEmpty = kAccFull + 2, kDone = kAccEmpty + 2, kNumBars = kDone + 1
+};
+
+// d = a * b + c on bf16 pairs, one rounding
+__device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t bf16_pair(float v) {
+  const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  return h | (h << 16);
+}
+
+struct CsUnit {
+  int64_t bi, c, grp;
+  int g, h;  // group, first head of the pair
+};
+__device__ __forceinline__ CsUnit cs_unit(const CsParams& p, int64_t u) {
+  const int hpg = p.nheads / p.ngroups, ppg = hpg / 2;
+  CsUnit r;
+  r.grp = u / ppg;
+  const int pair = (int)(u % ppg);
+  r.g = (int)(r.grp % p.ngroups);
+  const int64_t t = r.grp / p.ngroups;
+  r.c = t % p.nchunks;
+  r.bi = t / p.nchunks;
+  r.h = r.g * hpg + 2 * pair;
+  return r;
+}
 
 __global__ void __launch_bounds__(kCsThreads, 1)
     ssd_chunk_state_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_b,
@@ -76,27 +118,14 @@ __global__ void __launch_bounds__(kCsThreads, 1)
   unsigned char* base = cs_raw + ((1024u - (raw & 1023u)) & 1023u);
   const int T = p.chunk;
   const CsLayout L(T);
-  const int KH = (int)L.kh;
-  const int nk = T / KH;  // stages per head pair
+  const int nk = T / kCsKH;  // stages per unit
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bars);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.bars + kNumBars * 8);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.bars + kNumBars * 8 + 4);
-  float* wbuf = reinterpret_cast<float*>(base + L.w0);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.bars + 24 * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.bars + 24 * 8 + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // work item -> (batch, chunk, group, first pair)
-  int64_t item = blockIdx.x;
-  const int k_item = (int)(item % p.items_per_group);
-  item /= p.items_per_group;
-  const int g = (int)(item % p.ngroups);
-  item /= p.ngroups;
-  const int64_t c = item % p.nchunks;
-  const int64_t bi = item / p.nchunks;
-  const int hpg = p.nheads / p.ngroups;
-  const int ppg = hpg / 2;
-  const int q0 = k_item * p.pairs_per_item;
-  const int nq = min(p.pairs_per_item, ppg - q0);
-  const int nsteps = nq * nk;  // (pair, token half) steps through the stage ring
+  const int64_t u_begin = (int64_t)blockIdx.x * p.units / gridDim.x;
+  const int64_t u_end = (int64_t)(blockIdx.x + 1) * p.units / gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);  // every barrier has one arriving thread
@@ -118,108 +147,139 @@ __global__ void __launch_bounds__(kCsThreads, 1)
 
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------------------
-    if (lane == 0 && nsteps > 0) {
-      mbar_arrive_expect_tx(&bars[kBFull], 2u * T * kCsRowBytes);
-      for (int sb = 0; sb < 2; ++sb)
-        tc::tma_load_3d(base + L.bm0 + sb * T * kCsRowBytes, &map_b, g * 128 + sb * 64, (int)(c * T), (int)bi,
-                        &bars[kBFull]);
-      int issued = 0;
-      for (int i = 0; i < nsteps && !*abort_flag; ++i) {
-        const int st = i & 1;
-        if (i >= 2 && !mbar_wait(&bars[kXEmpty + st], (uint32_t)((i >> 1) - 1) & 1u, ctl.spin_limit_ns)) {
-          fail();
-          break;
+    if (lane == 0 && u_end > u_begin) {
+      int64_t cur_grp = -1;
+      int64_t i = 0;  // stage step
+      bool ok = true;
+      for (int64_t u = u_begin; u < u_end && ok && !*abort_flag; ++u) {
+        const CsUnit w = cs_unit(p, u);
+        for (int kh = 0; kh < nk; ++kh, ++i) {
+          const int st = (int)(i % kCsStages);
+          if (i >= kCsStages &&
+              !mbar_wait(&bars[kXEmpty + st], (uint32_t)((i / kCsStages) - 1) & 1u, ctl.spin_limit_ns)) {
+            ok = false;
+            break;
+          }
+          if (w.grp != cur_grp) {
+            // B is read by every MMA issued so far: wait for the last of them before replacing it
+            if (i > 0 && !mbar_wait(&bars[kXEmpty + (int)((i - 1) % kCsStages)],
+                                    (uint32_t)((i - 1) / kCsStages) & 1u, ctl.spin_limit_ns)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&bars[kBFull], 2u * T * kCsRowBytes);
+            for (int sb = 0; sb < 2; ++sb)
+              tc::tma_load_3d(base + L.bm0 + sb * T * kCsRowBytes, &map_b, w.g * 128 + sb * 64, (int)(w.c * T),
+                              (int)w.bi, &bars[kBFull]);
+            cur_grp = w.grp;
+          }
+          unsigned char* gd = base + L.gd0 + st * 2 * kCsGdHead;
+          mbar_arrive_expect_tx(&bars[kXFull + st], L.half_bytes + 2u * kCsGdHead);
+          for (int hh = 0; hh < 2; ++hh) {
+            tc::tma_load_3d(base + st * L.stage_bytes + hh * kCsKH * kCsRowBytes, &map_x, (w.h + hh) * 64,
+                            (int)(w.c * T + kh * kCsKH), (int)w.bi, &bars[kXFull + st]);
+            const int64_t row = (w.bi * p.nheads + w.h + hh) * p.lpad + w.c * T;
+            bulk_g2s(gd + hh * kCsGdHead, p.G + row + kh * kCsKH, 4u * kCsKH, &bars[kXFull + st]);
+            bulk_g2s(gd + hh * kCsGdHead + 4u * kCsKH, p.dtT + row + kh * kCsKH, 4u * kCsKH, &bars[kXFull + st]);
+            bulk_g2s(gd + hh * kCsGdHead + 8u * kCsKH, p.G + row + T - 4, 16u, &bars[kXFull + st]);
+          }
         }
-        const int q = i / nk, kh = i % nk;
-        const int h = g * hpg + 2 * (q0 + q);
-        mbar_arrive_expect_tx(&bars[kXFull + st], L.half_bytes);
-        for (int hh = 0; hh < 2; ++hh)
-          tc::tma_load_3d(base + st * L.stage_bytes + hh * KH * kCsRowBytes, &map_x, (h + hh) * 64,
-                          (int)(c * T + kh * KH), (int)bi, &bars[kXFull + st]);
-        issued = i + 1;
       }
+      if (!ok) fail();
       // leave no copy in flight: the last loads of each stage have landed (bounded)
-      for (int i = max(0, issued - 2); i < issued; ++i)
-        mbar_wait(&bars[kXFull + (i & 1)], (uint32_t)(i >> 1) & 1u, ctl.spin_limit_ns);
-      mbar_wait(&bars[kBFull], 0, ctl.spin_limit_ns);
+      for (int64_t j = (i > kCsStages ? i - kCsStages : 0); j < i; ++j)
+        mbar_wait(&bars[kXFull + (int)(j % kCsStages)], (uint32_t)(j / kCsStages) & 1u, ctl.spin_limit_ns);
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ---------------------------------------------
-    if (lane == 0 && nsteps > 0) {
+    if (lane == 0 && u_end > u_begin) {
       const uint32_t idesc = tc::idesc_bf16_f32(128, 128, /*a_mn=*/true, /*b_mn=*/true);
-      const uint32_t a_lbo = KH * kCsRowBytes;  // head 0 block -> head 1 block (MN blocks)
-      const uint32_t b_lbo = T * kCsRowBytes;   // s 0..63 block -> s 64..127 block
-      const uint32_t sbo = 8 * kCsRowBytes;     // next 8-token group
-      bool ok = mbar_wait(&bars[kBFull], 0, ctl.spin_limit_ns);
-      if (!ok) fail();
-      for (int i = 0; i < nsteps && ok && !*abort_flag; ++i) {
-        const int st = i & 1;
-        const int q = i / nk, kh = i % nk, acc = q & 1;
-        if (!mbar_wait(&bars[kXScaled + st], (uint32_t)(i >> 1) & 1u, ctl.spin_limit_ns) ||
-            (kh == 0 && q >= 2 && !mbar_wait(&bars[kAccEmpty + acc], (uint32_t)((q >> 1) - 1) & 1u, ctl.spin_limit_ns))) {
-          fail();
-          break;
+      const uint32_t a_lbo = kCsKH * kCsRowBytes;  // head 0 block -> head 1 block (MN blocks)
+      const uint32_t b_lbo = T * kCsRowBytes;      // s 0..63 block -> s 64..127 block
+      const uint32_t sbo = 8 * kCsRowBytes;        // next 8-token group
+      int64_t cur_grp = -1, i = 0;
+      int nb = 0, q = 0;
+      bool ok = true;
+      for (int64_t u = u_begin; u < u_end && ok && !*abort_flag; ++u, ++q) {
+        const CsUnit w = cs_unit(p, u);
+        const int acc = q & 1;
+        if (w.grp != cur_grp) {
+          ++nb;
+          cur_grp = w.grp;
+          ok = mbar_wait(&bars[kBFull], (uint32_t)(nb - 1) & 1u, ctl.spin_limit_ns);
         }
-        tc::fence_after_sync();
-        const uint32_t hi0 = smem_addr(base + st * L.stage_bytes);
-        const uint32_t lo0 = hi0 + L.half_bytes;
-        const uint32_t b0 = smem_addr(base + L.bm0) + kh * KH * kCsRowBytes;
-        for (int ks = 0; ks < KH / 16; ++ks) {
-          const uint32_t koff = ks * 16 * kCsRowBytes;  // 16 tokens = two 8-row groups
-          const uint64_t bdesc = tc::sdesc_sw128(b0 + koff, b_lbo, sbo);
-          tc::mma_bf16(tmem + acc * 128, tc::sdesc_sw128(hi0 + koff, a_lbo, sbo), bdesc, idesc, kh > 0 || ks > 0);
-          tc::mma_bf16(tmem + acc * 128, tc::sdesc_sw128(lo0 + koff, a_lbo, sbo), bdesc, idesc, true);
+        if (ok && q >= 2) ok = mbar_wait(&bars[kAccEmpty + acc], (uint32_t)((q >> 1) - 1) & 1u, ctl.spin_limit_ns);
+        for (int kh = 0; kh < nk && ok; ++kh, ++i) {
+          const int st = (int)(i % kCsStages);
+          if (!mbar_wait(&bars[kXScaled + st], (uint32_t)(i / kCsStages) & 1u, ctl.spin_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t hi0 = smem_addr(base + st * L.stage_bytes);
+          const uint32_t lo0 = hi0 + L.half_bytes;
+          const uint32_t b0 = smem_addr(base + L.bm0) + kh * kCsKH * kCsRowBytes;
+#pragma unroll
+          for (int ks = 0; ks < kCsKH / 16; ++ks) {
+            const uint32_t koff = ks * 16 * kCsRowBytes;  // 16 tokens = two 8-row groups
+            const uint64_t bdesc = tc::sdesc_sw128(b0 + koff, b_lbo, sbo);
+            tc::mma_bf16(tmem + acc * 128, tc::sdesc_sw128(hi0 + koff, a_lbo, sbo), bdesc, idesc, kh > 0 || ks > 0);
+            tc::mma_bf16(tmem + acc * 128, tc::sdesc_sw128(lo0 + koff, a_lbo, sbo), bdesc, idesc, true);
+          }
+          tc::mma_commit(&bars[kXEmpty + st]);  // the stage may be refilled
         }
-        tc::mma_commit(&bars[kXEmpty + st]);                   // the stage may be refilled
-        if (kh == nk - 1) tc::mma_commit(&bars[kAccFull + acc]);  // the accumulator is ready
+        if (ok) tc::mma_commit(&bars[kAccFull + acc]);  // the accumulator is ready
       }
+      if (!ok) fail();
       tc::mma_commit(&bars[kDone]);
       mbar_wait(&bars[kDone], 0, ctl.spin_limit_ns);  // every MMA has completed
     }
   } else if (warp < 6) {
     // ---------------- scale X by w, split into bf16 hi + lo parts --------------------------
-    const int t = threadIdx.x - 64;  // 0..127
-    const int64_t bh0 = bi * p.nheads;
-    for (int i = 0; i < nsteps; ++i) {
-      const int st = i & 1;
-      const int q = i / nk, kh = i % nk;
-      const int h = g * hpg + 2 * (q0 + q);
-      // weights of the pair's two heads for these tokens: w_t = dt_t 2^(G_last - G_t)
-      float* w = wbuf + st * 2 * KH;
-      for (int j = t; j < 2 * KH; j += 128) {
-        const int hh = j / KH, tok = kh * KH + j % KH;
-        const int64_t row = (bh0 + h + hh) * p.lpad + c * T;
-        w[j] = p.dtT[row + tok] * exp2f(p.G[row + T - 1] - p.G[row + tok]);
-      }
-      // w complete; a wait that gave up in any scaler thread ends the loop in all of them
-      const bool bad = !mbar_wait(&bars[kXFull + st], (uint32_t)(i >> 1) & 1u, ctl.spin_limit_ns);
-      if (named_bar_any(kCsScaleBar, 128, bad)) {
-        if (t == 0) fail();
-        break;
-      }
-      // every 16-byte chunk holds 8 p-values of one token row of one head
-      uint4* hi = reinterpret_cast<uint4*>(base + st * L.stage_bytes);
-      uint4* lo = reinterpret_cast<uint4*>(base + st * L.stage_bytes + L.half_bytes);
-      const int nchunk = 2 * KH * 8;
-      for (int j = t; j < nchunk; j += 128) {
-        const float wv = w[j >> 3];  // row = head * KH + token
-        uint4 v = hi[j], r;
-        __nv_bfloat162* e = reinterpret_cast<__nv_bfloat162*>(&v);
-        __nv_bfloat162* f = reinterpret_cast<__nv_bfloat162*>(&r);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 xv = __bfloat1622float2(e[k]);
-          const float2 s = make_float2(xv.x * wv, xv.y * wv);
-          e[k] = __floats2bfloat162_rn(s.x, s.y);
-          const float2 sh = __bfloat1622float2(e[k]);
-          f[k] = __floats2bfloat162_rn(s.x - sh.x, s.y - sh.y);
+    const int t = threadIdx.x - 64;  // token row of the stage: head t / 64, token t % 64
+    const int hh = t / kCsKH, tok = t % kCsKH;
+    int64_t i = 0;
+    bool ok = true;
+    for (int64_t u = u_begin; u < u_end && ok; ++u) {
+      for (int kh = 0; kh < nk; ++kh, ++i) {
+        const int st = (int)(i % kCsStages);
+        const bool bad = !mbar_wait(&bars[kXFull + st], (uint32_t)(i / kCsStages) & 1u, ctl.spin_limit_ns);
+        if (named_bar_any(kCsScaleBar, 128, bad)) {  // leave together, or not at all
+          if (t == 0) fail();
+          ok = false;
+          break;
         }
-        hi[j] = v;
-        lo[j] = r;
+        const float* gd = reinterpret_cast<const float*>(base + L.gd0 + (st * 2 + hh) * kCsGdHead);
+        const float wv = gd[kCsKH + tok] * tc::ex2_approx(gd[2 * kCsKH + 3] - gd[tok]);
+        const __nv_bfloat16 w_hi = __float2bfloat16_rn(wv);
+        const float w_lo = wv - __bfloat162float(w_hi);
+        const uint32_t whi2 = bf16_pair(__bfloat162float(w_hi));
+        const uint32_t nwhi2 = whi2 ^ 0x80008000u;
+        const uint32_t nwlo2 = bf16_pair(-w_lo);
+        unsigned char* hrow = base + st * L.stage_bytes + t * kCsRowBytes;
+        unsigned char* lrow = hrow + L.half_bytes;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const int off = (cc ^ (t & 7)) << 4;  // every chunk of the row; spread over the banks
+          uint4 v = *reinterpret_cast<const uint4*>(hrow + off);
+          uint32_t* e = reinterpret_cast<uint32_t*>(&v);
+          uint4 r;
+          uint32_t* f = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t x2 = e[k];
+            const uint32_t h2 = fma_bf16x2(x2, whi2, 0x80008000u);  // x w_hi, rounded
+            const uint32_t d2 = fma_bf16x2(x2, nwhi2, h2);           // hi - x w_hi, exact
+            f[k] = fma_bf16x2(x2, nwlo2, d2) ^ 0x80008000u;          // x w - hi, rounded
+            e[k] = h2;
+          }
+          *reinterpret_cast<uint4*>(hrow + off) = v;
+          *reinterpret_cast<uint4*>(lrow + off) = r;
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(kCsScaleBar, 128);
+        if (t == 0) mbar_arrive(&bars[kXScaled + st]);
       }
-      fence_proxy_async_smem();
-      named_bar_sync(kCsScaleBar, 128);
-      if (t == 0) mbar_arrive(&bars[kXScaled + st]);
     }
   } else {
     // ------------------------------ epilogue: TMEM -> S_c ----------------------------------
@@ -227,7 +287,9 @@ __global__ void __launch_bounds__(kCsThreads, 1)
     const int m = quad * 32 + lane;  // accumulator row
     const int hh = m >> 6, pp = m & 63;
     const int S = 128;
-    for (int q = 0; q < nq; ++q) {
+    int q = 0;
+    for (int64_t u = u_begin; u < u_end; ++u, ++q) {
+      const CsUnit w = cs_unit(p, u);
       const int acc = q & 1;
       const bool bad = !mbar_wait(&bars[kAccFull + acc], (uint32_t)(q >> 1) & 1u, ctl.spin_limit_ns);
       if (named_bar_any(kCsEpiBar, 128, bad)) {  // leave together, or not at all
@@ -235,8 +297,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         break;
       }
       tc::fence_after_sync();
-      const int h = g * hpg + 2 * (q0 + q) + hh;
-      float* out = p.Sc + ((((bi * p.nchunks + c) * p.nheads + h) * 64 + pp) * (int64_t)S);
+      float* out = p.Sc + ((((w.bi * p.nchunks + w.c) * p.nheads + w.h + hh) * 64 + pp) * (int64_t)S);
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t r[32];
@@ -275,7 +336,7 @@ cudaError_t launch_ssd_chunk_state_tc(const void* x, const void* B, const SsdDim
   const uint64_t xs[2] = {(uint64_t)d.nheads * 64 * 2, (uint64_t)d.seqlen * d.nheads * 64 * 2};
   const uint64_t bd[3] = {(uint64_t)d.ngroups * 128, (uint64_t)d.seqlen, (uint64_t)d.batch};
   const uint64_t bs[2] = {(uint64_t)d.ngroups * 128 * 2, (uint64_t)d.seqlen * d.ngroups * 128 * 2};
-  const uint32_t xbox[3] = {64, CsLayout(d.chunk).kh, 1};
+  const uint32_t xbox[3] = {64, (uint32_t)kCsKH, 1};
   const uint32_t bbox[3] = {64, (uint32_t)d.chunk, 1};
   cudaError_t e;
   if ((e = encode_tensor_map_3d(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, xd, xs, xbox, CU_TENSOR_MAP_SWIZZLE_128B)) !=
@@ -294,22 +355,17 @@ cudaError_t launch_ssd_chunk_state_tc(const void* x, const void* B, const SsdDim
   p.nheads = d.nheads;
   p.ngroups = d.ngroups;
   p.chunk = d.chunk;
-  const int ppg = d.nheads / d.ngroups / 2;
+  p.units = d.batch * d.nchunks * d.ngroups * (d.nheads / d.ngroups / 2);
   int dev = 0, sms = 148;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  // split each group's pairs into runs so that there are about two CTAs per SM or more
-  const int64_t groups_total = d.batch * d.nchunks * d.ngroups;
-  int items = (int)((2 * (int64_t)sms + groups_total - 1) / groups_total);
-  items = items < 1 ? 1 : (items > ppg ? ppg : items);
-  p.pairs_per_item = (ppg + items - 1) / items;
-  p.items_per_group = (ppg + p.pairs_per_item - 1) / p.pairs_per_item;
   const CsLayout L(d.chunk);
   const size_t smem = L.total + 1024;
   if ((e = cudaFuncSetAttribute(ssd_chunk_state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
       cudaSuccess)
     return e;
-  const int64_t grid = groups_total * p.items_per_group;
+  // one CTA per SM (shared memory allows no second), each with an equal share of the units
+  const int64_t grid = p.units < sms ? p.units : sms;
   ssd_chunk_state_tc_kernel<<<(unsigned)grid, kCsThreads, smem, s>>>(map_x, map_b, p, ctl);
   return cudaGetLastError();
 }
