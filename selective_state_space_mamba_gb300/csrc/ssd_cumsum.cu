@@ -20,6 +20,22 @@ namespace {
 constexpr int kCsHeads = 32;
 constexpr int kCsThreads = 256;
 constexpr int kCsMaxChunk = 256;
+constexpr int kCsWarps = kCsThreads / 32;
+constexpr int kCsHeadsPerWarp = kCsHeads / kCsWarps;
+constexpr int kCsLoads = kCsMaxChunk * kCsHeads / kCsThreads;
+
+// Raw bits of one dt value through the read-only path.  The loads are volatile asm so that all
+// of a thread's loads are issued, in order, before the first conversion waits on one of them.
+__device__ __forceinline__ uint32_t ld_bits(const __nv_bfloat16* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return (uint32_t)v << 16;  // bf16 bits in the top half are the f32 bits
+}
+__device__ __forceinline__ uint32_t ld_bits(const float* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
 
 template <typename DtT>
 __global__ void __launch_bounds__(kCsThreads) ssd_chunk_cumsum_kernel(const DtT* __restrict__ dt,
@@ -33,6 +49,7 @@ __global__ void __launch_bounds__(kCsThreads) ssd_chunk_cumsum_kernel(const DtT*
   const int h0 = hblk * kCsHeads;
   const int nhb = min(kCsHeads, nh - h0);
   const int64_t t0 = (int64_t)c * T;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   if (c == 0 && hblk == 0 && bi == 0 && threadIdx.x == 0) {
     // the state-passing kernel runs after this one on the same stream: start its claims at 0
@@ -40,37 +57,40 @@ __global__ void __launch_bounds__(kCsThreads) ssd_chunk_cumsum_kernel(const DtT*
     hdr->done = 0u;
   }
 
-  // all of a thread's loads are issued before the first is used (one memory latency, not 32)
-  constexpr int kLoads = kCsMaxChunk * kCsHeads / kCsThreads;
-  float v[kLoads];
+  // element k of this thread: token warp + 8 k, head lane (a warp reads one token's heads)
+  const int tmax = d.seqlen - t0 < T ? (int)(d.seqlen - t0) : T;  // real tokens in this chunk
+  const bool head_ok = lane < nhb;
+  const DtT* src = dt + (bi * d.seqlen + t0 + warp) * nh + h0 + (head_ok ? lane : 0);
+  uint32_t raw[kCsLoads];
 #pragma unroll
-  for (int k = 0; k < kLoads; ++k) {
-    const int idx = threadIdx.x + k * kCsThreads;
-    const int t = idx / kCsHeads, hh = idx % kCsHeads;
-    v[k] = 0.f;
-    if (t < T && hh < nhb && t0 + t < d.seqlen) v[k] = to_f32(dt[((bi * d.seqlen) + t0 + t) * nh + h0 + hh]);
+  for (int k = 0; k < kCsLoads; ++k) {
+    const int t = warp + kCsWarps * k;
+    raw[k] = 0u;
+    if (head_ok && t < tmax) raw[k] = ld_bits(src + (int64_t)kCsWarps * k * nh);
+  }
+  float Ah[kCsHeadsPerWarp];
+#pragma unroll
+  for (int q = 0; q < kCsHeadsPerWarp; ++q) {
+    const int hh = warp + q * kCsWarps;
+    Ah[q] = hh < nhb ? A[h0 + hh] : 0.f;
   }
 #pragma unroll
-  for (int k = 0; k < kLoads; ++k) {
-    const int idx = threadIdx.x + k * kCsThreads;
-    if (idx < T * kCsHeads) s_dt[(idx / kCsHeads) * (kCsHeads + 1) + idx % kCsHeads] = v[k];
+  for (int k = 0; k < kCsLoads; ++k) {
+    const int t = warp + kCsWarps * k;
+    if (t < T) s_dt[t * (kCsHeads + 1) + lane] = __uint_as_float(raw[k]);
   }
   __syncthreads();
 
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int per_lane = T / 32;  // chunk is a multiple of 64 and at most 256
-  constexpr int kWarps = kCsThreads / 32;
-  constexpr int kHeadsPerWarp = kCsHeads / kWarps;
-  float gv[kHeadsPerWarp][8];
+  float gv[kCsHeadsPerWarp][8];
 #pragma unroll
-  for (int q = 0; q < kHeadsPerWarp; ++q) {
-    const int hh = warp + q * kWarps;
-    const float Ah = hh < nhb ? A[h0 + hh] : 0.f;
+  for (int q = 0; q < kCsHeadsPerWarp; ++q) {
+    const int hh = warp + q * kCsWarps;
     float run = 0.f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       if (k < per_lane) {
-        run += Ah * s_dt[(lane * per_lane + k) * (kCsHeads + 1) + hh];
+        run += Ah[q] * s_dt[(lane * per_lane + k) * (kCsHeads + 1) + hh];
         gv[q][k] = run;
       }
     }
@@ -86,18 +106,27 @@ __global__ void __launch_bounds__(kCsThreads) ssd_chunk_cumsum_kernel(const DtT*
     for (int k = 0; k < 8; ++k) gv[q][k] = (excl + gv[q][k]) * kLog2e;
   }
 
-  // dt^T rows, then G rows, each warp writing 32 consecutive tokens of one head per store
+  // dt^T rows, then G rows: each warp store writes 32 consecutive tokens of one head
   auto store_rows = [&](float* dst) {
-    for (int idx = threadIdx.x; idx < nhb * T; idx += kCsThreads) {
-      const int hh = idx / T, t = idx % T;
-      dst[(bi * nh + h0 + hh) * d.lpad + t0 + t] = s_dt[t * (kCsHeads + 1) + hh];
+#pragma unroll
+    for (int q = 0; q < kCsHeadsPerWarp; ++q) {
+      const int hh = warp + q * kCsWarps;
+      if (hh < nhb) {
+        float* row = dst + (bi * nh + h0 + hh) * d.lpad + t0;
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = 32 * k < T ? s_dt[(lane + 32 * k) * (kCsHeads + 1) + hh] : 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (32 * k < T) row[lane + 32 * k] = v[k];
+      }
     }
   };
   store_rows(dtT);
   __syncthreads();
 #pragma unroll
-  for (int q = 0; q < kHeadsPerWarp; ++q) {
-    const int hh = warp + q * kWarps;
+  for (int q = 0; q < kCsHeadsPerWarp; ++q) {
+    const int hh = warp + q * kCsWarps;
 #pragma unroll
     for (int k = 0; k < 8; ++k)
       if (k < per_lane) s_dt[(lane * per_lane + k) * (kCsHeads + 1) + hh] = gv[q][k];

@@ -33,7 +33,8 @@
 //               the last stage of a unit hands the accumulator to the epilogue
 //   warps 2-5   one token row of one head per thread: w = dt 2^(G_last - G_t), then the row's
 //               64 values of X in shared memory -> hi (in place) and lo
-//   warps 6-9   epilogue: TMEM -> registers -> S_c (f32), then free the accumulator
+//   warps 6-9   epilogue: TMEM -> registers -> a swizzled 32 x 32 f32 block per warp in shared
+//               memory -> TMA store into S_c; the accumulator is freed after its last TMEM load
 // Every wait is bounded; on expiry the CTA records SSM_ERR_TIMEOUT, drains, frees its TMEM
 // and returns.
 #include "tc_common.cuh"
@@ -64,15 +65,17 @@ struct CsParams {
 // Shared-memory layout (offsets from a 1024-byte aligned base), chunk size T:
 //   stage[4] = { hi[2 heads][64 rows][128 B], lo[2 heads][64 rows][128 B] }   swizzled
 //   bm[s block][T rows][128 B]                                                 swizzled
+//   epi[4 warps][32 rows][128 B]   S_c staging for the TMA store (swizzled)
 //   gd[4 stages][2 heads] = { G[64], dt[64], G[T-4 .. T-1] }
 //   barriers, TMEM base, abort flag
 struct CsLayout {
-  uint32_t half_bytes, stage_bytes, bm0, gd0, bars, total;
+  uint32_t half_bytes, stage_bytes, bm0, epi0, gd0, bars, total;
   __host__ __device__ explicit CsLayout(int T) {
     half_bytes = 2u * kCsKH * kCsRowBytes;
     stage_bytes = 2u * half_bytes;
     bm0 = kCsStages * stage_bytes;
-    gd0 = bm0 + 2u * T * kCsRowBytes;
+    epi0 = bm0 + 2u * T * kCsRowBytes;
+    gd0 = epi0 + 4u * 32 * kCsRowBytes;
     bars = gd0 + kCsStages * 2u * kCsGdHead;
     total = bars + 24 * 8 + 16;
   }
@@ -112,7 +115,7 @@ __device__ __forceinline__ CsUnit cs_unit(const CsParams& p, int64_t u) {
 
 __global__ void __launch_bounds__(kCsThreads, 1)
     ssd_chunk_state_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_b,
-                              CsParams p, LookbackCtl ctl) {
+                              const __grid_constant__ CUtensorMap map_sc, CsParams p, LookbackCtl ctl) {
   extern __shared__ unsigned char cs_raw[];
   const uint32_t raw = smem_addr(cs_raw);
   unsigned char* base = cs_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -283,11 +286,10 @@ __global__ void __launch_bounds__(kCsThreads, 1)
     }
   } else {
     // ------------------------------ epilogue: TMEM -> S_c ----------------------------------
-    const int quad = warp & 3;       // TMEM lanes 32*quad .. +31
-    const int m = quad * 32 + lane;  // accumulator row
-    const int hh = m >> 6, pp = m & 63;
-    const int S = 128;
+    const int quad = warp & 3;  // TMEM lanes 32*quad .. +31 = accumulator rows
+    unsigned char* stg = base + L.epi0 + quad * 32 * kCsRowBytes;
     int q = 0;
+    bool stored = false;
     for (int64_t u = u_begin; u < u_end; ++u, ++q) {
       const CsUnit w = cs_unit(p, u);
       const int acc = q & 1;
@@ -297,21 +299,37 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         break;
       }
       tc::fence_after_sync();
-      float* out = p.Sc + ((((w.bi * p.nchunks + w.c) * p.nheads + w.h + hh) * 64 + pp) * (int64_t)S);
+      // the unit's 128 accumulator rows are 128 consecutive rows of S_c (two heads x 64 p)
+      const int row0 = (int)(((w.bi * p.nchunks + w.c) * p.nheads + w.h) * 64) + quad * 32;
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t r[32];
         tc::tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + acc * 128 + cb * 32, r);
         tc::tmem_ld_wait();
+        if (cb == 3) {  // the accumulator has been read
+          tc::fence_before_sync();
+          named_bar_sync(kCsEpiBar, 128);
+          if (threadIdx.x == 192) mbar_arrive(&bars[kAccEmpty + acc]);
+        }
+        if (stored) {  // the previous block's store has read the staging rows
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          reinterpret_cast<float4*>(out + cb * 32)[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                                                    __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+          *reinterpret_cast<float4*>(stg + lane * kCsRowBytes + ((j ^ (lane & 7)) << 4)) =
+              make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]), __uint_as_float(r[4 * j + 2]),
+                          __uint_as_float(r[4 * j + 3]));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&map_sc, stg, cb * 32, row0);
+          bulk_commit();
+        }
+        stored = true;
       }
-      tc::fence_before_sync();
-      named_bar_sync(kCsEpiBar, 128);
-      if (threadIdx.x == 192) mbar_arrive(&bars[kAccEmpty + acc]);
     }
+    if (lane == 0) bulk_wait<0>();
   }
 
   tc::fence_before_sync();
@@ -345,6 +363,11 @@ cudaError_t launch_ssd_chunk_state_tc(const void* x, const void* B, const SsdDim
   if ((e = encode_tensor_map_3d(&map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, bd, bs, bbox, CU_TENSOR_MAP_SWIZZLE_128B)) !=
       cudaSuccess)
     return e;
+  CUtensorMap map_sc;  // S_c as rows (batch, chunk, head, p) x 128 s, f32
+  const uint64_t sc_rows = (uint64_t)d.batch * d.nchunks * d.nheads * 64;
+  if ((e = encode_tensor_map_2d(&map_sc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ws.Sc, 128, sc_rows, 512, 32, 32,
+                                CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return e;
   CsParams p;
   p.G = ws.G;
   p.dtT = ws.dtT;
@@ -366,7 +389,7 @@ cudaError_t launch_ssd_chunk_state_tc(const void* x, const void* B, const SsdDim
     return e;
   // one CTA per SM (shared memory allows no second), each with an equal share of the units
   const int64_t grid = p.units < sms ? p.units : sms;
-  ssd_chunk_state_tc_kernel<<<(unsigned)grid, kCsThreads, smem, s>>>(map_x, map_b, p, ctl);
+  ssd_chunk_state_tc_kernel<<<(unsigned)grid, kCsThreads, smem, s>>>(map_x, map_b, map_sc, p, ctl);
   return cudaGetLastError();
 }
 
