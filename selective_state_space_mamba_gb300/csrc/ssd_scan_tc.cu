@@ -3,26 +3,33 @@
 //     Y = 2^G (C h_in^T) + ((C B^T) . 2^(G_i - G_j) dt_j . [i >= j]) X + D X,
 // on the 5th-generation tensor cores for bf16 inputs (f32 accumulation).
 //
-// CTA = (batch, chunk, 128-row tile of the chunk, group, run of heads), warp-specialised:
-//   warp 0     TMA producer: the tile's C rows and the chunk's B rows once; then, per head,
-//              X, the chunk-initial state h_in and the head's G and dt over the chunk into a
-//              2-stage ring
-//   warp 1     TMEM owner and MMA issuer (one thread): CB = C B^T once (M = 128 rows,
-//              N = columns up to the tile's end, K = S; shared by all heads of the run: the
-//              post recomputes it per head); per head Y2 = C h_in^T as soon as the stage lands,
-//              and Y1 = P X once P is ready (P read from TMEM as the A operand)
-//   warps 2-9  math: CB once to bf16 in shared memory; per head, P = CB . w with
-//              w(i, j) = dt_j 2^(G_i - G_j) for j <= i, written to TMEM as bf16, and the row's
-//              x values kept in registers; then the previous head's epilogue
-//              y = Y1 + 2^(G_i) Y2 + D x (f32) -> bf16 -> swizzled stage -> TMA store
-// P and the accumulators are double-buffered in TMEM, so the MMA of head k runs while the
-// math warps finish head k-1.
+// CTA = (batch, chunk, 128-row tile of the chunk starting at row i0, group, run of heads).
+// The tile's columns j split into the rectangle j < i0 and the triangle i0 <= j < i0 + 128.
+// In the rectangle every weight factors through the tile's first row:
+//     2^(G_i - G_j) dt_j = u_i f_j,   u_i = 2^(G_i - G_i0) <= 1,   f_j = dt_j 2^(G_i0 - G_j) <= dt_j,
+// so its part of Y is u_i (CB_rect (f . X_rect)): one MMA whose A operand (CB) is the same for
+// all heads of the run and whose B operand is X with its rows scaled by f; u_i is applied in
+// the f32 epilogue.  Only the 128 x 128 triangle needs a per-element weight matrix P.
 //
-// The decay weight is a product of two factors that are both <= 1 wherever row i lies in a
-// later 32-token block than column j: w = 2^(G_i - G_r) * dt_j 2^(G_r - G_j), r the first token
-// of i's block (G is non-increasing).  Only in the diagonal 32 x 32 block of a warp's rows is
-// 2^(G_i - G_j) evaluated per element, with the exponent set to -inf above the diagonal before
-// the exponential (the post masks after exp2; masking the exponent first never produces inf).
+// Warp roles (320 threads):
+//   warp 0     TMA producer: the tile's C rows and B rows 0 .. i0+127 once; then, per head,
+//              X rows 0 .. i0+127, the chunk-initial state h_in and the head's G and dt over
+//              the chunk into a 2-stage ring
+//   warp 1     TMEM owner and MMA issuer (one thread): CB = C B^T once; per head
+//              Y2 = C h_in^T as soon as the stage lands, then Ya = CB_rect (f . X_rect) and
+//              Yt = P X_tri (P read from TMEM as the A operand) once the math warps are done
+//   warps 2-9  math: CB once to bf16 in shared memory (the MMA operand layout); per head the
+//              rectangle's X rows scaled by f, the triangle P (bf16, to TMEM) and the row's x
+//              values kept in registers; then the previous head's epilogue
+//              y = Yt + 2^(G_i) Y2 + u_i Ya + D x (f32) -> bf16 -> swizzled stage -> TMA store
+// P and the accumulators are double-buffered in TMEM, so the MMAs of head k run while the math
+// warps finish head k-1.
+//
+// Inside the triangle the same factoring is used per 32-row block I: w = 2^(G_i - G_r) *
+// dt_j 2^(G_r - G_j), r = i0 + 32 I, both factors <= 1 for columns in earlier blocks.  In the
+// diagonal 32 x 32 block the weight is 2^(G_i + c_j), c_j = log2(dt_j) - G_j, with the exponent
+// set to -inf above the diagonal before the exponential (masking the exponent first never
+// produces inf).  Weights are rounded to bf16 and multiplied into CB with one bf16x2 FMA.
 //
 // Every wait is bounded.  A math-warp wait that gives up is voted on (bar.red.or) so that all
 // math warps leave together; the CTA then drains, frees its TMEM and returns.
@@ -35,13 +42,24 @@ constexpr int kScThreads = 320;  // warp 0 producer, warp 1 MMA, warps 2..9 math
 constexpr int kScMath = 256;
 constexpr uint32_t kScMathBar = 1;
 constexpr uint32_t kScTmemCols = 512;
-// TMEM columns: CB (f32, first phase only) 0..Nj-1; then P[b] at 128 b (bf16 pairs, 128 columns)
-// and Y1[b] / Y2[b] at 256 + 128 b / 320 + 128 b (64 f32 columns each).
-constexpr uint32_t kColCB = 0;
-__device__ __forceinline__ uint32_t col_p(int b) { return 128u * b; }
-__device__ __forceinline__ uint32_t col_y1(int b) { return 256u + 128u * b; }
-__device__ __forceinline__ uint32_t col_y2(int b) { return 320u + 128u * b; }
 constexpr int kRowB = 128;  // bytes per swizzled operand row (64 bf16)
+constexpr int kCbBlock = 128 * kRowB;  // one 64-column block of CB (bf16) for the tile's 128 rows
+
+// TMEM columns.  CB (f32) takes 0 .. i0+127 during the first phase only.  Afterwards P[b]
+// (bf16 pairs, 64 columns) sits at 64 b, and accumulator set b at 320 (b = 0) or 128 (b = 1):
+// Yt at +0, Y2 at +64, Ya at +128 (64 f32 columns each).  Set 1 overlaps CB; its first MMA
+// is issued only after the math warps have signalled P of head 0, i.e. after CB was read.
+constexpr uint32_t kColCB = 0;
+__device__ __forceinline__ uint32_t col_p(int b) { return 64u * b; }
+__device__ __forceinline__ uint32_t col_y(int b) { return b ? 128u : 320u; }
+
+// Per-head factor table (floats):
+//   [0, 192)    triangle: local row block I = 1..3 holds dt_j 2^(G_r - G_j) for the 32 I
+//               columns i0 <= j < r, r = i0 + 32 I, at offset 16 I (I - 1)
+//   [192, 320)  rectangle: f_j = dt_j 2^(G_i0 - G_j), j < i0 (tiles with i0 > 0)
+//   [320, 448)  diagonal blocks: c_j = log2(dt_j) - G_j, i0 <= j < i0 + 128
+constexpr int kVTri = 0, kVRect = 192, kVDiag = 320, kVFloats = 448;
+__device__ __forceinline__ int v_off(int I) { return 16 * I * (I - 1); }
 
 struct ScParams {
   const float* G;
@@ -54,14 +72,14 @@ struct ScParams {
 };
 
 // Shared memory (offsets from a 1024-byte aligned base), chunk size T:
-//   C tile   2 s-blocks x 128 rows x 128 B                                      32 KB
-//   B rows   2 s-blocks x T rows x 128 B; after CB: CB as bf16 [128 rows][Nj] (16-byte chunks
-//            swizzled within each row)
+//   C tile   2 s-blocks x 128 rows x 128 B                                        32 KB
+//   B rows   2 s-blocks x T rows x 128 B; after CB: CB as bf16 in the K-major operand layout,
+//            [column block of 64][128 rows][128 B], 16-byte chunks swizzled by row
 //   stage[2] X: T rows x 128 B | h_in: 2 s-blocks x 64 rows x 128 B | G, dt: T floats each
 //   y stage  128 rows x 128 B (swizzled, for the TMA store)
-//   v[2]     the off-diagonal factor tables of two heads, packed by 32-row block
+//   v[2]     the factor tables of two heads
 struct ScLayout {
-  uint32_t c0, b0, st0, st_bytes, hin_off, g_off, dt_off, y0, v0, v_floats, bars, total;
+  uint32_t c0, b0, st0, st_bytes, hin_off, g_off, dt_off, y0, v0, bars, total;
   __host__ __device__ explicit ScLayout(int T) {
     c0 = 0;
     b0 = c0 + 2u * 128 * kRowB;
@@ -72,8 +90,7 @@ struct ScLayout {
     st_bytes = dt_off + 4u * T;
     y0 = st0 + 2u * st_bytes;
     v0 = y0 + 128u * kRowB;
-    v_floats = 16u * 8 * 7;  // row blocks 1..7 hold 32 * block entries: 32 * 28
-    bars = v0 + 2u * 4u * v_floats;
+    bars = v0 + 2u * 4u * kVFloats;
     total = bars + 16 * 8 + 16;
   }
 };
@@ -88,8 +105,21 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
-// offset of row block I's factors in a packed table (block I >= 1 holds 32 I entries)
-__device__ __forceinline__ int v_off(int I) { return 16 * I * (I - 1); }
+// a * b on bf16 pairs, one rounding (fma with -0 keeps the sign of a zero product)
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(0x80008000u));
+  return d;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// address of the 16-byte chunk holding columns 8 q .. 8 q + 7 of tile row r in the CB layout
+__device__ __forceinline__ uint32_t cb_chunk(int r, int q) {
+  return (uint32_t)((q >> 3) * kCbBlock + r * kRowB + (((q & 7) ^ (r & 7)) << 4));
+}
 
 __global__ void __launch_bounds__(kScThreads, 1)
     ssd_chunk_scan_tc_kernel(const __grid_constant__ CUtensorMap map_c, const __grid_constant__ CUtensorMap map_b,
@@ -119,7 +149,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
   const int hpg = p.nheads / p.ngroups;
   const int h_first = g * hpg + k_item * p.heads_per_item;
   const int nh_run = min(p.heads_per_item, hpg - k_item * p.heads_per_item);
-  const int i0 = R * 128;   // first chunk row of the tile
+  const int i0 = R * 128;   // first chunk row of the tile (0 or 128)
   const int Nj = i0 + 128;  // columns 0 .. Nj-1 can be at or below the diagonal
   const int tok0 = (int)(c * T);
 
@@ -193,8 +223,9 @@ __global__ void __launch_bounds__(kScThreads, 1)
         }
         tc::mma_commit(&bars[kCbDone]);
       }
-      const uint32_t id_y2 = tc::idesc_bf16_f32(128, 64, false, false);
-      const uint32_t id_y1 = tc::idesc_bf16_f32(128, 64, false, true);
+      const uint32_t id_kk = tc::idesc_bf16_f32(128, 64, false, false);  // Y2: C, h_in both K-major
+      const uint32_t id_kn = tc::idesc_bf16_f32(128, 64, false, true);   // Ya, Yt: X MN-major
+      const uint32_t xlbo = (uint32_t)T * kRowB;
       for (int k = 0; k < nh_run && ok && !*abort_flag; ++k) {
         const int st = k & 1, bf = k & 1;
         if (!mbar_wait(&bars[kStFull + st], (uint32_t)(k >> 1) & 1u, ctl.spin_limit_ns) ||
@@ -205,22 +236,29 @@ __global__ void __launch_bounds__(kScThreads, 1)
         tc::fence_after_sync();
         const uint32_t x_addr = smem_addr(base + L.st0 + st * L.st_bytes);
         const uint32_t h_addr = x_addr + L.hin_off;
-        // Y2 = C h_in^T: M = 128, N = 64 (p), K = S (both K-major); runs while P is being formed
+        const uint32_t ycol = tmem + col_y(bf);
+        // Y2 = C h_in^T: M = 128, N = 64 (p), K = S; runs while the math warps work
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t ko = (ks & 3) * 32;
           const uint64_t a = tc::sdesc_sw128(c_addr + (ks >> 2) * 128 * kRowB + ko, 16, sbo);
           const uint64_t b = tc::sdesc_sw128(h_addr + (ks >> 2) * 64 * kRowB + ko, 16, sbo);
-          tc::mma_bf16(tmem + col_y2(bf), a, b, id_y2, ks > 0);
+          tc::mma_bf16(ycol + 64, a, b, id_kk, ks > 0);
         }
         if (!mbar_wait(&bars[kPFull + bf], (uint32_t)(k >> 1) & 1u, ctl.spin_limit_ns)) {
           fail();
           break;
         }
         tc::fence_after_sync();
-        // Y1 = P X: A = P from TMEM (8 columns per 16 K), B = X rows (MN-major, p contiguous)
-        for (int ks = 0; ks < Nj / 16; ++ks) {
-          const uint64_t b = tc::sdesc_sw128(x_addr + ks * 16 * kRowB, (uint32_t)T * kRowB, sbo);
-          tc::mma_bf16_ts(tmem + col_y1(bf), tmem + col_p(bf) + ks * 8, b, id_y1, ks > 0);
+        // Ya = CB_rect (f . X_rect): A = CB from shared memory (K = j < i0), B = scaled X rows
+        for (int ks = 0; ks < i0 / 16; ++ks) {
+          const uint64_t a = tc::sdesc_sw128(b_addr + (ks >> 2) * kCbBlock + (ks & 3) * 32, 16, sbo);
+          const uint64_t b = tc::sdesc_sw128(x_addr + ks * 16 * kRowB, xlbo, sbo);
+          tc::mma_bf16(ycol + 128, a, b, id_kn, ks > 0);
+        }
+        // Yt = P X_tri: A = P from TMEM (8 columns per 16 K), B = X rows i0 .. i0+127
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t b = tc::sdesc_sw128(x_addr + (i0 + ks * 16) * kRowB, xlbo, sbo);
+          tc::mma_bf16_ts(ycol, tmem + col_p(bf) + ks * 8, b, id_kn, ks > 0);
         }
         tc::mma_commit(&bars[kStEmpty + st]);  // X, h_in, G, dt of this head are no longer needed
         tc::mma_commit(&bars[kMmaDone + bf]);
@@ -231,17 +269,15 @@ __global__ void __launch_bounds__(kScThreads, 1)
   } else {
     // ------------------------------ math warps ---------------------------------------------
     const int mt = threadIdx.x - 64;   // 0..255
-    const int quad = warp & 3;         // TMEM lanes 32*quad .. +31
+    const int quad = warp & 3;         // TMEM lanes 32*quad .. +31 = the row's 32-row block
     const int half = (warp - 2) >> 2;  // which interleaved 32-column blocks
     const int r = quad * 32 + lane;    // tile row
     const int i = i0 + r;              // chunk row
-    const int I = i >> 5;              // 32-token block of the row (warp-uniform)
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    const int row_bytes = Nj * 2;      // CB row in bf16
     unsigned char* cb_smem = base + L.b0;
     bool ok = nh_run > 0;
 
-    // ---- CB (f32, TMEM) -> bf16 rows in shared memory over the dead B rows ----
+    // ---- CB (f32, TMEM) -> bf16 in the K-major operand layout, over the B rows ----
     if (ok) {
       const bool bad = !mbar_wait(&bars[kCbDone], 0, ctl.spin_limit_ns);
       if (named_bar_any(kScMathBar, kScMath, bad)) {
@@ -257,57 +293,71 @@ __global__ void __launch_bounds__(kScThreads, 1)
         tc::tmem_ld_wait();
 #pragma unroll
         for (int q = 0; q < 4; ++q) {  // four 16-byte chunks of 8 columns
-          const int chunk = (cb >> 3) + q;
           uint4 w;
           w.x = pack_bf16(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1]));
           w.y = pack_bf16(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
           w.z = pack_bf16(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
           w.w = pack_bf16(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
-          *reinterpret_cast<uint4*>(cb_smem + r * row_bytes + ((chunk ^ (r & 7)) << 4)) = w;
+          *reinterpret_cast<uint4*>(cb_smem + cb_chunk(r, (cb >> 3) + q)) = w;
         }
       }
+      fence_proxy_async_smem();  // the rectangle MMA reads CB through the async proxy
       tc::fence_before_sync();
     }
 
-    // Off-diagonal factors of head k for the tile's row blocks: v[I][j] = dt_j 2^(G_{32I} - G_j),
-    // j < 32 I.  Returns false (all threads alike) when the head's stage never arrived.
+    // Factor table of head k (layout at kVTri / kVRect / kVDiag).  Returns false (all threads
+    // alike) when the head's stage never arrived.
     auto build_table = [&](int k) -> bool {
       const int st = k & 1;
       const bool bad = !mbar_wait(&bars[kStFull + st], (uint32_t)(k >> 1) & 1u, ctl.spin_limit_ns);
       if (named_bar_any(kScMathBar, kScMath, bad)) return false;
       const float* gq = reinterpret_cast<const float*>(base + L.st0 + st * L.st_bytes + L.g_off);
       const float* dq = reinterpret_cast<const float*>(base + L.st0 + st * L.st_bytes + L.dt_off);
-      float* vq = v_all + (k & 1) * L.v_floats;
-      const int Ilo = max(1, i0 >> 5), Ihi = (i0 + 128) >> 5;  // row blocks of this tile
-      for (int e = v_off(Ilo) + mt; e < v_off(Ihi); e += kScMath) {
-        int II = Ilo;
-        while (v_off(II + 1) <= e) ++II;
-        const int j = e - v_off(II);
-        vq[e] = dq[j] * tc::ex2_approx(gq[32 * II] - gq[j]);
+      float* vq = v_all + (k & 1) * kVFloats;
+      for (int e = mt; e < kVRect + i0; e += kScMath) {
+        int j, ref;
+        if (e < kVRect) {  // triangle: local row block I, reference row i0 + 32 I
+          const int I = e < 32 ? 1 : (e < 96 ? 2 : 3);
+          j = i0 + e - v_off(I);
+          ref = i0 + 32 * I;
+        } else {  // rectangle: reference row i0
+          j = e - kVRect;
+          ref = i0;
+        }
+        vq[e] = dq[j] * tc::ex2_approx(gq[ref] - gq[j]);
       }
+      if (mt < 128) vq[kVDiag + mt] = lg2_approx(dq[i0 + mt]) - gq[i0 + mt];  // dt = 0 -> -inf
       return true;
     };
 
-    // y = Y1 + 2^(G_i) Y2 + D x of head kk -> swizzled stage -> TMA store.  False (all alike)
-    // on a wait that gave up.
-    auto epilogue = [&](int kk, float e_i, float Dk, const uint32_t (&xk)[16]) -> bool {
+    // y = Yt + 2^(G_i) Y2 + u_i Ya + D x of head kk -> swizzled stage -> TMA store.  False (all
+    // alike) on a wait that gave up.
+    auto epilogue = [&](int kk, float e_i, float u_i, float Dk, const uint32_t (&xk)[16]) -> bool {
       const int b2 = kk & 1;
       const bool bad = !mbar_wait(&bars[kMmaDone + b2], (uint32_t)(kk >> 1) & 1u, ctl.spin_limit_ns);
       if (named_bar_any(kScMathBar, kScMath, bad)) return false;
       tc::fence_after_sync();
-      uint32_t y1[32], y2[32];
-      tc::tmem_ld32(tmem + lane_base + col_y1(b2) + half * 32, y1);
-      tc::tmem_ld32(tmem + lane_base + col_y2(b2) + half * 32, y2);
+      const uint32_t ycol = tmem + lane_base + col_y(b2) + half * 32;
+      uint32_t yt[32], y2[32], ya[32];
+      tc::tmem_ld32(ycol, yt);
+      tc::tmem_ld32(ycol + 64, y2);
+      if (i0 > 0) tc::tmem_ld32(ycol + 128, ya);
       tc::tmem_ld_wait();
+      float o[32];
+#pragma unroll
+      for (int q = 0; q < 32; ++q) o[q] = __uint_as_float(yt[q]) + e_i * __uint_as_float(y2[q]);
+      if (i0 > 0) {
+#pragma unroll
+        for (int q = 0; q < 32; ++q) o[q] += u_i * __uint_as_float(ya[q]);
+      }
       uint32_t outp[16];
 #pragma unroll
       for (int q = 0; q < 16; ++q)
-        outp[q] = pack_bf16(__uint_as_float(y1[2 * q]) + e_i * __uint_as_float(y2[2 * q]) + Dk * bf_lo(xk[q]),
-                            __uint_as_float(y1[2 * q + 1]) + e_i * __uint_as_float(y2[2 * q + 1]) + Dk * bf_hi(xk[q]));
+        outp[q] = pack_bf16(o[2 * q] + Dk * bf_lo(xk[q]), o[2 * q + 1] + Dk * bf_hi(xk[q]));
       tc::fence_before_sync();
       if (mt == 0) bulk_wait_read<0>();  // the previous y store has read the stage
       named_bar_sync(kScMathBar, kScMath);
-      if (mt == 0) mbar_arrive(&bars[kYFree + b2]);  // Y[b2] may be overwritten
+      if (mt == 0) mbar_arrive(&bars[kYFree + b2]);  // accumulator set b2 may be overwritten
       unsigned char* yrow = base + L.y0 + r * kRowB;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
@@ -328,8 +378,9 @@ __global__ void __launch_bounds__(kScThreads, 1)
       if (mt == 0) fail();
       ok = false;
     }
-    // 2^(G_i), D and the row's x values of the previous head, taken before its stage is released
-    float prev_e = 0.f, prev_D = 0.f;
+    // 2^(G_i), u_i, D and the row's x values of the previous head, taken before its stage is
+    // released
+    float prev_e = 0.f, prev_u = 0.f, prev_D = 0.f;
     uint32_t prev_x[16];
 #pragma unroll
     for (int q = 0; q < 16; ++q) prev_x[q] = 0u;
@@ -337,16 +388,17 @@ __global__ void __launch_bounds__(kScThreads, 1)
       const int st = k & 1, bf = k & 1;
       const int h = h_first + k;
       named_bar_sync(kScMathBar, kScMath);  // CB (first head) and this head's table are complete
-      const float* g_s = reinterpret_cast<const float*>(base + L.st0 + st * L.st_bytes + L.g_off);
-      const float* dt_s = reinterpret_cast<const float*>(base + L.st0 + st * L.st_bytes + L.dt_off);
-      const float* v_s = v_all + (k & 1) * L.v_floats + (I >= 1 ? v_off(I) : 0);
+      unsigned char* stage = base + L.st0 + st * L.st_bytes;
+      const float* g_s = reinterpret_cast<const float*>(stage + L.g_off);
+      const float* v_s = v_all + (k & 1) * kVFloats;
       const float gi = g_s[i];
-      const float ui = I > 0 ? tc::ex2_approx(gi - g_s[32 * I]) : 0.f;
-      const float cur_D = p.D[h];
+      const float ui = quad > 0 ? tc::ex2_approx(gi - g_s[i0 + 32 * quad]) : 0.f;  // triangle row factor
+      const float cur_u = i0 > 0 ? tc::ex2_approx(gi - g_s[i0]) : 0.f;            // rectangle row factor
       const float cur_e = tc::ex2_approx(gi);
+      const float cur_D = p.D[h];
       uint32_t cur_x[16];  // x(i, 32 half .. 32 half + 31) as bf16 pairs
       {
-        const unsigned char* xrow = base + L.st0 + st * L.st_bytes + i * kRowB;
+        const unsigned char* xrow = stage + i * kRowB;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           const uint4 w = *reinterpret_cast<const uint4*>(xrow + (((half * 4 + cc) ^ (i & 7)) << 4));
@@ -354,69 +406,88 @@ __global__ void __launch_bounds__(kScThreads, 1)
         }
       }
 
-      // ---- P = CB . w for my row: bf16 pairs into P[bf] ----
-      for (int J = half; J < Nj / 32; J += 2) {
-        const int cb = J * 32;
+      // ---- rectangle: X rows j < i0 scaled by f_j in place (two threads per row) ----
+      if (i0 > 0) {
+        const int j = mt >> 1;
+        const float f = v_s[kVRect + j];
+        const uint32_t f2 = pack_bf16(f, f);
+        unsigned char* xrow = stage + j * kRowB;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint4* q = reinterpret_cast<uint4*>(xrow + ((((mt & 1) * 4 + cc) ^ (j & 7)) << 4));
+          uint4 w = *q;
+          w.x = mul_bf16x2(w.x, f2);
+          w.y = mul_bf16x2(w.y, f2);
+          w.z = mul_bf16x2(w.z, f2);
+          w.w = mul_bf16x2(w.w, f2);
+          *q = w;
+        }
+        fence_proxy_async_smem();
+      }
+
+      // ---- triangle P for my row: bf16 pairs into P[bf] ----
+#pragma unroll
+      for (int Jp = half; Jp < 4; Jp += 2) {
+        const int cb = i0 + 32 * Jp;  // first column of the block
         uint32_t pk[16];
-        if (J > I) {  // entirely above the diagonal
+        if (Jp > quad) {  // entirely above the diagonal
 #pragma unroll
           for (int q = 0; q < 16; ++q) pk[q] = 0u;
         } else {
           uint32_t cw[16];  // CB row segment as bf16 pairs
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const uint4 w = *reinterpret_cast<const uint4*>(cb_smem + r * row_bytes + ((((cb >> 3) + q) ^ (r & 7)) << 4));
+            const uint4 w = *reinterpret_cast<const uint4*>(cb_smem + cb_chunk(r, (cb >> 3) + q));
             cw[4 * q] = w.x; cw[4 * q + 1] = w.y; cw[4 * q + 2] = w.z; cw[4 * q + 3] = w.w;
           }
-          if (J < I) {  // w = 2^(G_i - G_r) * dt_j 2^(G_r - G_j), both factors <= 1
-            const float4* vv = reinterpret_cast<const float4*>(v_s + cb);
+          if (Jp < quad) {  // w = 2^(G_i - G_r) * dt_j 2^(G_r - G_j), both factors <= 1
+            const float4* vv = reinterpret_cast<const float4*>(v_s + kVTri + v_off(quad) + 32 * Jp);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
               const float4 f = vv[q];
-              pk[2 * q] = pack_bf16(bf_lo(cw[2 * q]) * (ui * f.x), bf_hi(cw[2 * q]) * (ui * f.y));
-              pk[2 * q + 1] = pack_bf16(bf_lo(cw[2 * q + 1]) * (ui * f.z), bf_hi(cw[2 * q + 1]) * (ui * f.w));
+              pk[2 * q] = mul_bf16x2(cw[2 * q], pack_bf16(ui * f.x, ui * f.y));
+              pk[2 * q + 1] = mul_bf16x2(cw[2 * q + 1], pack_bf16(ui * f.z, ui * f.w));
             }
-          } else {  // diagonal 32 x 32 block: per-element 2^(G_i - G_j), exponent -inf above it
-            const float4* gg = reinterpret_cast<const float4*>(g_s + cb);
-            const float4* dd = reinterpret_cast<const float4*>(dt_s + cb);
+          } else {  // diagonal 32 x 32 block: 2^(G_i + c_j), exponent -inf above the diagonal
+            const float4* cc4 = reinterpret_cast<const float4*>(v_s + kVDiag + 32 * Jp);
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-              const float4 gq = gg[q], dq = dd[q];
-              const int j = cb + 4 * q;
-              const float p0 = bf_lo(cw[2 * q]) * dq.x * tc::ex2_approx(j <= i ? gi - gq.x : -INFINITY);
-              const float p1 = bf_hi(cw[2 * q]) * dq.y * tc::ex2_approx(j + 1 <= i ? gi - gq.y : -INFINITY);
-              const float p2 = bf_lo(cw[2 * q + 1]) * dq.z * tc::ex2_approx(j + 2 <= i ? gi - gq.z : -INFINITY);
-              const float p3 = bf_hi(cw[2 * q + 1]) * dq.w * tc::ex2_approx(j + 3 <= i ? gi - gq.w : -INFINITY);
-              pk[2 * q] = pack_bf16(p0, p1);
-              pk[2 * q + 1] = pack_bf16(p2, p3);
+              const float4 cq = cc4[q];  // columns cb + 4q .. +3; my row is column cb + lane
+              const float w0 = tc::ex2_approx(4 * q <= lane ? gi + cq.x : -INFINITY);
+              const float w1 = tc::ex2_approx(4 * q + 1 <= lane ? gi + cq.y : -INFINITY);
+              const float w2 = tc::ex2_approx(4 * q + 2 <= lane ? gi + cq.z : -INFINITY);
+              const float w3 = tc::ex2_approx(4 * q + 3 <= lane ? gi + cq.w : -INFINITY);
+              pk[2 * q] = mul_bf16x2(cw[2 * q], pack_bf16(w0, w1));
+              pk[2 * q + 1] = mul_bf16x2(cw[2 * q + 1], pack_bf16(w2, w3));
             }
           }
         }
-        tc::tmem_st16(tmem + lane_base + col_p(bf) + (cb >> 1), pk);
+        tc::tmem_st16(tmem + lane_base + col_p(bf) + 16 * Jp, pk);
       }
       tc::tmem_st_wait();
       tc::fence_before_sync();
       named_bar_sync(kScMathBar, kScMath);
       if (mt == 0) mbar_arrive(&bars[kPFull + bf]);
 
-      // ---- the previous head's epilogue while the MMA multiplies this one ----
-      if (k >= 1 && !epilogue(k - 1, prev_e, prev_D, prev_x)) {
+      // ---- the previous head's epilogue while the MMAs multiply this one ----
+      if (k >= 1 && !epilogue(k - 1, prev_e, prev_u, prev_D, prev_x)) {
         if (mt == 0) fail();
         ok = false;
         break;
       }
       prev_e = cur_e;
+      prev_u = cur_u;
       prev_D = cur_D;
 #pragma unroll
       for (int q = 0; q < 16; ++q) prev_x[q] = cur_x[q];
-      // ---- the next head's table while the MMA works ----
+      // ---- the next head's table while the MMAs work ----
       if (k + 1 < nh_run && !build_table(k + 1)) {
         if (mt == 0) fail();
         ok = false;
         break;
       }
     }
-    if (ok && !epilogue(nh_run - 1, prev_e, prev_D, prev_x) && mt == 0) fail();
+    if (ok && !epilogue(nh_run - 1, prev_e, prev_u, prev_D, prev_x) && mt == 0) fail();
     if (mt == 0) bulk_wait<0>();
   }
 
@@ -475,12 +546,22 @@ cudaError_t launch_ssd_chunk_scan_tc(const void* x, const void* B, const void* C
   int dev = 0, sms = 148;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  // split each (batch, chunk, group, row tile)'s heads into runs: about three CTAs per SM or more
+  // Split each (batch, chunk, group, row tile)'s heads into runs, one CTA per run and one CTA
+  // per SM at a time: choose the run length that minimises waves x (heads per run + the
+  // per-CTA set-up, about three heads' worth).
   const int64_t tiles = d.batch * d.nchunks * d.ngroups * p.row_tiles;
-  int runs = (int)((3 * (int64_t)sms + tiles - 1) / tiles);
-  runs = runs < 1 ? 1 : (runs > hpg ? hpg : runs);
-  p.heads_per_item = (hpg + runs - 1) / runs;
-  p.items_per_tile = (hpg + p.heads_per_item - 1) / p.heads_per_item;
+  int64_t best_cost = -1;
+  for (int hpi = 1; hpi <= hpg; ++hpi) {
+    const int items = (hpg + hpi - 1) / hpi;
+    if (hpi > 1 && (hpg + hpi - 2) / (hpi - 1) == items) continue;  // same split, shorter runs
+    const int64_t waves = (tiles * items + sms - 1) / sms;
+    const int64_t cost = waves * (hpi + 3);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      p.heads_per_item = hpi;
+      p.items_per_tile = items;
+    }
+  }
   const ScLayout L(d.chunk);
   const size_t smem = L.total + 1024;
   if ((e = cudaFuncSetAttribute(ssd_chunk_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
