@@ -14,6 +14,12 @@
 // same chain (a warp inspects 32 flags at once, atomic claim order guarantees progress),
 // publishes its inclusive state (flag P), then writes h_in for each of its chunks.  The
 // decay of an aggregate is not published: every tile recomputes it from G.
+//
+// When there are enough state entries to fill the GPU without splitting the chunk axis (the
+// usual case: batch x heads x H x S in the millions), the recurrence runs as written instead:
+// ssd_state_passing_seq_kernel gives each thread four entries of one (batch, head) and walks
+// all chunks in order, with the chunk increments of the next kSeqAhead chunks already in
+// flight (copied into shared memory).  No flags, fences or workspace beyond S_c and h_in.
 #include "ssm_internal.cuh"
 
 namespace ssm {
@@ -181,10 +187,93 @@ __global__ void __launch_bounds__(kSpThreads) ssd_state_passing_kernel(const flo
   if (threadIdx.x == 0) retire_tile(ws.hdr, (uint32_t)ws.sp_tiles);
 }
 
+constexpr int kSeqThreads = 256;
+constexpr int kSeqAhead = 8;             // chunk increments in flight per thread
+constexpr int64_t kSeqMinGroups = 32768;  // fewer four-entry groups than this: the look-back kernel
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Each thread streams its own four entries of S_c for chunk c + kSeqAhead into its own
+// 16-byte slot of a shared-memory ring while it combines chunk c, so the loads in flight cost
+// no registers; a thread only ever reads slots it filled itself (cp.async.wait_group).
+template <typename HinT>
+__global__ void __launch_bounds__(kSeqThreads) ssd_state_passing_seq_kernel(const float* __restrict__ h0,
+                                                                            float* __restrict__ h_final, SsdDims d,
+                                                                            SsdWorkspace ws) {
+  __shared__ float4 ring[kSeqAhead][kSeqThreads];
+  const int HS = d.headdim * d.dstate;
+  const int64_t q4 = HS / 4;
+  const int64_t gidx = (int64_t)blockIdx.x * kSeqThreads + threadIdx.x;
+  if (gidx >= d.batch * d.nheads * q4) return;
+  const int64_t bh = gidx / q4;  // bi * nheads + h
+  const int e = (int)(gidx % q4) * 4;
+  const int64_t bi = bh / d.nheads;
+  const int h = (int)(bh % d.nheads);
+  const int64_t nc = d.nchunks;
+  const float* Grow = ws.G + bh * d.lpad + (d.chunk - 1);  // G_last of chunk c at Grow[c * chunk]
+  const int64_t step = (int64_t)d.nheads * HS;              // chunk c -> c + 1 in S_c and h_in
+  const float* src = ws.Sc + (bi * nc * d.nheads + h) * (int64_t)HS + e;
+  HinT* hin = static_cast<HinT*>(ws.hin) + (bi * nc * d.nheads + h) * (int64_t)HS + e;
+  float4* slot = &ring[0][threadIdx.x];
+
+  float lg[kSeqAhead];
+#pragma unroll
+  for (int u = 0; u < kSeqAhead; ++u) {
+    if (u < nc) {
+      cp_async16(slot + u * kSeqThreads, src + u * step);
+      lg[u] = Grow[u * d.chunk];
+    }
+    cp_async_commit();  // one group per chunk, empty past the end
+  }
+  const float* next = src + kSeqAhead * step;
+  float4 X = h0 ? *reinterpret_cast<const float4*>(h0 + bh * HS + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t c0 = 0; c0 < nc; c0 += kSeqAhead) {
+#pragma unroll
+    for (int u = 0; u < kSeqAhead; ++u) {
+      const int64_t c = c0 + u;
+      if (c < nc) {
+        cp_async_wait<kSeqAhead - 1>();  // chunk c's group (the oldest) has landed
+        const float4 v = slot[u * kSeqThreads];
+        store4<HinT>(hin, X);  // state entering chunk c
+        hin += step;
+        X = f4_fma(exp2f(lg[u]), X, v);
+        if (c + kSeqAhead < nc) {
+          cp_async16(slot + u * kSeqThreads, next);
+          lg[u] = Grow[(c + kSeqAhead) * d.chunk];
+        }
+        next += step;
+        cp_async_commit();
+      }
+    }
+  }
+  cp_async_wait<0>();
+  if (h_final) *reinterpret_cast<float4*>(h_final + bh * HS + e) = X;
+}
+
 }  // namespace
+
+bool ssd_state_passing_sequential(const SsdDims& d) {
+  return d.batch * d.nheads * (int64_t)(d.headdim * d.dstate / 4) >= kSeqMinGroups;
+}
 
 cudaError_t launch_ssd_state_passing(const float* h0, float* h_final, const SsdDims& d, const SsdWorkspace& ws,
                                      const LookbackCtl& ctl, cudaStream_t s) {
+  if (ssd_state_passing_sequential(d)) {
+    const int64_t groups = d.batch * d.nheads * (int64_t)(d.headdim * d.dstate / 4);
+    const unsigned grid = (unsigned)((groups + kSeqThreads - 1) / kSeqThreads);
+    if (d.dtype == SSM_BF16)
+      ssd_state_passing_seq_kernel<__nv_bfloat16><<<grid, kSeqThreads, 0, s>>>(h0, h_final, d, ws);
+    else
+      ssd_state_passing_seq_kernel<float><<<grid, kSeqThreads, 0, s>>>(h0, h_final, d, ws);
+    return cudaGetLastError();
+  }
   if (d.dtype == SSM_BF16) {
     ssd_state_passing_kernel<__nv_bfloat16><<<(unsigned)ws.sp_tiles, kSpThreads, 0, s>>>(h0, h_final, d, ws, ctl);
   } else {
