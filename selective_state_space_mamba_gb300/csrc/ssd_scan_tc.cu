@@ -11,20 +11,21 @@
 // all heads of the run and whose B operand is X with its rows scaled by f; u_i is applied in
 // the f32 epilogue.  Only the 128 x 128 triangle needs a per-element weight matrix P.
 //
-// Warp roles (320 threads):
-//   warp 0     TMA producer: the tile's C rows and B rows 0 .. i0+127 once; then, per head,
-//              X rows 0 .. i0+127, the chunk-initial state h_in and the head's G and dt over
-//              the chunk into a 2-stage ring
-//   warp 1     TMEM owner and MMA issuer (one thread): CB = C B^T once; per head
-//              Y2 = C h_in^T as soon as the stage lands, then Ya = CB_rect (f . X_rect) and
-//              Yt = P X_tri (P read from TMEM as the A operand) once the math warps are done
-//   warps 2-9  math: CB once to bf16 in shared memory (the MMA operand layout); per head the
-//              rectangle's X rows scaled by f, the triangle P (bf16, to TMEM) and the row's x
-//              values kept in registers; then the previous head's epilogue
-//              y = Yt + 2^(G_i) Y2 + u_i Ya + D x (f32) -> bf16 -> swizzled stage -> TMA store
-// P and the accumulators are double-buffered in TMEM, so the MMAs of head k run while the math
-// warps finish head k-1.
-//
+// Warp roles (448 threads):
+//   warp 0       TMA producer: the tile's C rows and B rows 0 .. i0+127 once; then, per head,
+//                X rows 0 .. i0+127, the chunk-initial state h_in and the head's G and dt over
+//                the chunk into a 2-stage ring (and the same tiles of later heads into L2)
+//   warp 1       TMEM owner and MMA issuer (one thread): CB = C B^T once; per head
+//                Y2 = C h_in^T as soon as the stage lands, then Ya = CB_rect (f . X_rect) and
+//                Yt = P X_tri (P read from TMEM as the A operand) once the P warps are done
+//   warps 2-9    P warps: CB once to bf16 in shared memory (the MMA operand layout); per head
+//                the factor table, the rectangle's X rows scaled by f and the triangle P
+//                (bf16, to TMEM)
+//   warps 10-13  epilogue warps, one row per thread: x and G from the stage as it lands, then
+//                y = Yt + 2^(G_i) Y2 + u_i Ya + D x (f32) -> bf16 -> swizzled stage -> TMA store
+// P and the accumulators are double-buffered in TMEM, so the P warps build head k + 1 while
+// the MMAs and the epilogue warps finish head k.
+
 // Inside the triangle the same factoring is used per 32-row block I: w = 2^(G_i - G_r) *
 // dt_j 2^(G_r - G_j), r = i0 + 32 I, both factors <= 1 for columns in earlier blocks.  In the
 // diagonal 32 x 32 block the weight is 2^(G_i + c_j), c_j = log2(dt_j) - G_j, with the exponent
@@ -38,9 +39,10 @@
 namespace ssm {
 namespace {
 
-constexpr int kScThreads = 320;  // warp 0 producer, warp 1 MMA, warps 2..9 math
-constexpr int kScMath = 256;
-constexpr uint32_t kScMathBar = 1;
+constexpr int kScThreads = 448;  // warp 0 producer, warp 1 MMA, warps 2..9 P, warps 10..13 epilogue
+constexpr int kScMath = 256;     // P warps
+constexpr int kScEpi = 128;      // epilogue warps
+constexpr uint32_t kScMathBar = 1, kScEpiBar = 2;
 constexpr uint32_t kScTmemCols = 512;
 constexpr int kRowB = 128;  // bytes per swizzled operand row (64 bf16)
 constexpr int kCbBlock = 128 * kRowB;  // one 64-column block of CB (bf16) for the tile's 128 rows
@@ -95,8 +97,8 @@ struct ScLayout {
   }
 };
 enum ScBar {
-  kInFull = 0, kCbDone = 1, kStFull = 2, kStEmpty = 4, kPFull = 6, kMmaDone = 8, kYFree = 10, kDone = 12,
-  kScNumBars = 13
+  kInFull = 0, kCbDone = 1, kStFull = 2, kStEmpty = 4, kPFull = 6, kMmaDone = 8, kYFree = 10, kXRead = 12,
+  kDone = 14, kScNumBars = 15
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -105,6 +107,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+// (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1), one f32x2 FMA
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                     float c1) {
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+      " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
 // a * b on bf16 pairs, one rounding (fma with -0 keeps the sign of a zero product)
 __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -181,10 +191,28 @@ __global__ void __launch_bounds__(kScThreads, 1)
           tc::tma_load_3d(base + L.b0 + sb * T * kRowB + rb * 128 * kRowB, &map_b, g * 128 + sb * 64, tok0 + rb * 128,
                           (int)bi, &bars[kInFull]);
       }
+      // A stage is refilled only when the MMAs of the head two before it are done, about one
+      // head's time before it is needed: too short for DRAM.  So the head's tiles are first
+      // prefetched into L2, three heads ahead; the stage load then reads L2.
+      auto prefetch_head = [&](int kk) {
+        if (kk >= nh_run) return;
+        const int h = h_first + kk;
+        for (int rb = 0; rb < Nj / 128; ++rb) tc::tma_prefetch_3d(&map_x, h * 64, tok0 + rb * 128, (int)bi);
+        const int hin_row = (int)(((bi * p.nchunks + c) * p.nheads + h) * 64);
+        for (int sb = 0; sb < 2; ++sb) tc::tma_prefetch_2d(&map_hin, sb * 64, hin_row);
+        const int64_t grow = (bi * p.nheads + h) * p.lpad + tok0;
+        tc::bulk_prefetch_l2(p.G + grow, 4u * T);
+        tc::bulk_prefetch_l2(p.dtT + grow, 4u * T);
+      };
+      prefetch_head(2);
       int issued = 0;
       for (int k = 0; k < nh_run && !*abort_flag; ++k) {
         const int st = k & 1;
-        if (k >= 2 && !mbar_wait(&bars[kStEmpty + st], (uint32_t)((k >> 1) - 1) & 1u, ctl.spin_limit_ns)) {
+        prefetch_head(k + 3);
+        // the stage is free once the MMAs of head k - 2 are done and the epilogue warps have
+        // taken its x and G
+        if (k >= 2 && (!mbar_wait(&bars[kStEmpty + st], (uint32_t)((k >> 1) - 1) & 1u, ctl.spin_limit_ns) ||
+                       !mbar_wait(&bars[kXRead + st], (uint32_t)((k >> 1) - 1) & 1u, ctl.spin_limit_ns))) {
           fail();
           break;
         }
@@ -266,8 +294,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
       tc::mma_commit(&bars[kDone]);
       mbar_wait(&bars[kDone], 0, ctl.spin_limit_ns);
     }
-  } else {
-    // ------------------------------ math warps ---------------------------------------------
+  } else if (warp < 10) {
+    // ------------------------------ P warps ------------------------------------------------
     const int mt = threadIdx.x - 64;   // 0..255
     const int quad = warp & 3;         // TMEM lanes 32*quad .. +31 = the row's 32-row block
     const int half = (warp - 2) >> 2;  // which interleaved 32-column blocks
@@ -330,81 +358,24 @@ __global__ void __launch_bounds__(kScThreads, 1)
       return true;
     };
 
-    // y = Yt + 2^(G_i) Y2 + u_i Ya + D x of head kk -> swizzled stage -> TMA store.  False (all
-    // alike) on a wait that gave up.
-    auto epilogue = [&](int kk, float e_i, float u_i, float Dk, const uint32_t (&xk)[16]) -> bool {
-      const int b2 = kk & 1;
-      const bool bad = !mbar_wait(&bars[kMmaDone + b2], (uint32_t)(kk >> 1) & 1u, ctl.spin_limit_ns);
-      if (named_bar_any(kScMathBar, kScMath, bad)) return false;
-      tc::fence_after_sync();
-      const uint32_t ycol = tmem + lane_base + col_y(b2) + half * 32;
-      uint32_t yt[32], y2[32], ya[32];
-      tc::tmem_ld32(ycol, yt);
-      tc::tmem_ld32(ycol + 64, y2);
-      if (i0 > 0) tc::tmem_ld32(ycol + 128, ya);
-      tc::tmem_ld_wait();
-      float o[32];
-#pragma unroll
-      for (int q = 0; q < 32; ++q) o[q] = __uint_as_float(yt[q]) + e_i * __uint_as_float(y2[q]);
-      if (i0 > 0) {
-#pragma unroll
-        for (int q = 0; q < 32; ++q) o[q] += u_i * __uint_as_float(ya[q]);
-      }
-      uint32_t outp[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q)
-        outp[q] = pack_bf16(o[2 * q] + Dk * bf_lo(xk[q]), o[2 * q + 1] + Dk * bf_hi(xk[q]));
-      tc::fence_before_sync();
-      if (mt == 0) bulk_wait_read<0>();  // the previous y store has read the stage
-      named_bar_sync(kScMathBar, kScMath);
-      if (mt == 0) mbar_arrive(&bars[kYFree + b2]);  // accumulator set b2 may be overwritten
-      unsigned char* yrow = base + L.y0 + r * kRowB;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const int chunk = half * 4 + cc;
-        *reinterpret_cast<uint4*>(yrow + ((chunk ^ (r & 7)) << 4)) =
-            make_uint4(outp[cc * 4], outp[cc * 4 + 1], outp[cc * 4 + 2], outp[cc * 4 + 3]);
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(kScMathBar, kScMath);
-      if (mt == 0) {
-        tc::tma_store_3d(&map_y, base + L.y0, (h_first + kk) * 64, tok0 + i0, (int)bi);
-        bulk_commit();
-      }
-      return true;
-    };
-
     if (ok && !build_table(0)) {
       if (mt == 0) fail();
       ok = false;
     }
-    // 2^(G_i), u_i, D and the row's x values of the previous head, taken before its stage is
-    // released
-    float prev_e = 0.f, prev_u = 0.f, prev_D = 0.f;
-    uint32_t prev_x[16];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) prev_x[q] = 0u;
     for (int k = 0; k < nh_run && ok; ++k) {
       const int st = k & 1, bf = k & 1;
-      const int h = h_first + k;
-      named_bar_sync(kScMathBar, kScMath);  // CB (first head) and this head's table are complete
+      // this head's table is complete, and P[bf] has been read by the MMAs of head k - 2
+      const bool bad = k >= 2 && !mbar_wait(&bars[kMmaDone + bf], (uint32_t)((k - 2) >> 1) & 1u, ctl.spin_limit_ns);
+      if (named_bar_any(kScMathBar, kScMath, bad)) {
+        if (mt == 0) fail();
+        break;
+      }
+      tc::fence_after_sync();
       unsigned char* stage = base + L.st0 + st * L.st_bytes;
       const float* g_s = reinterpret_cast<const float*>(stage + L.g_off);
       const float* v_s = v_all + (k & 1) * kVFloats;
       const float gi = g_s[i];
       const float ui = quad > 0 ? tc::ex2_approx(gi - g_s[i0 + 32 * quad]) : 0.f;  // triangle row factor
-      const float cur_u = i0 > 0 ? tc::ex2_approx(gi - g_s[i0]) : 0.f;            // rectangle row factor
-      const float cur_e = tc::ex2_approx(gi);
-      const float cur_D = p.D[h];
-      uint32_t cur_x[16];  // x(i, 32 half .. 32 half + 31) as bf16 pairs
-      {
-        const unsigned char* xrow = stage + i * kRowB;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          const uint4 w = *reinterpret_cast<const uint4*>(xrow + (((half * 4 + cc) ^ (i & 7)) << 4));
-          cur_x[4 * cc] = w.x; cur_x[4 * cc + 1] = w.y; cur_x[4 * cc + 2] = w.z; cur_x[4 * cc + 3] = w.w;
-        }
-      }
 
       // ---- rectangle: X rows j < i0 scaled by f_j in place (two threads per row) ----
       if (i0 > 0) {
@@ -469,26 +440,91 @@ __global__ void __launch_bounds__(kScThreads, 1)
       named_bar_sync(kScMathBar, kScMath);
       if (mt == 0) mbar_arrive(&bars[kPFull + bf]);
 
-      // ---- the previous head's epilogue while the MMAs multiply this one ----
-      if (k >= 1 && !epilogue(k - 1, prev_e, prev_u, prev_D, prev_x)) {
-        if (mt == 0) fail();
-        ok = false;
-        break;
-      }
-      prev_e = cur_e;
-      prev_u = cur_u;
-      prev_D = cur_D;
-#pragma unroll
-      for (int q = 0; q < 16; ++q) prev_x[q] = cur_x[q];
-      // ---- the next head's table while the MMAs work ----
+      // ---- the next head's table while the MMAs and the epilogue warps work ----
       if (k + 1 < nh_run && !build_table(k + 1)) {
         if (mt == 0) fail();
-        ok = false;
         break;
       }
     }
-    if (ok && !epilogue(nh_run - 1, prev_e, prev_u, prev_D, prev_x) && mt == 0) fail();
-    if (mt == 0) bulk_wait<0>();
+  } else {
+    // ------------------------------ epilogue warps -----------------------------------------
+    // y = Yt + 2^(G_i) Y2 + u_i Ya + D x for the tile's 128 rows (one per thread) x 64 p.
+    // x and G are read from the stage as soon as it lands (the stage is refilled only after
+    // this group has released it through kXRead); the accumulators once the MMAs are done.
+    const int et = threadIdx.x - 320;  // 0..127
+    const int quad = warp & 3;         // TMEM lanes 32*quad .. +31
+    const int r = quad * 32 + lane;    // tile row
+    const int i = i0 + r;              // chunk row
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    for (int k = 0; k < nh_run; ++k) {
+      const int st = k & 1, b = k & 1;
+      const int h = h_first + k;
+      bool bad = !mbar_wait(&bars[kStFull + st], (uint32_t)(k >> 1) & 1u, ctl.spin_limit_ns);
+      if (named_bar_any(kScEpiBar, kScEpi, bad)) {
+        if (et == 0) fail();
+        break;
+      }
+      const unsigned char* stage = base + L.st0 + st * L.st_bytes;
+      const float* g_s = reinterpret_cast<const float*>(stage + L.g_off);
+      const float gi = g_s[i];
+      const float e_i = tc::ex2_approx(gi);
+      const float u_i = i0 > 0 ? tc::ex2_approx(gi - g_s[i0]) : 0.f;
+      const float Dh = p.D[h];
+      uint32_t xr[32];  // x(i, 0 .. 63) as bf16 pairs
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        const uint4 w = *reinterpret_cast<const uint4*>(stage + i * kRowB + ((cc ^ (i & 7)) << 4));
+        xr[4 * cc] = w.x; xr[4 * cc + 1] = w.y; xr[4 * cc + 2] = w.z; xr[4 * cc + 3] = w.w;
+      }
+      named_bar_sync(kScEpiBar, kScEpi);
+      if (et == 0) {
+        mbar_arrive(&bars[kXRead + st]);  // x and G of this stage are in registers
+        if (k > 0) bulk_wait_read<0>();   // the previous y store has read the y stage
+      }
+      bad = !mbar_wait(&bars[kMmaDone + b], (uint32_t)(k >> 1) & 1u, ctl.spin_limit_ns);
+      if (named_bar_any(kScEpiBar, kScEpi, bad)) {
+        if (et == 0) fail();
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t ycol = tmem + lane_base + col_y(b);
+      unsigned char* yrow = base + L.y0 + r * kRowB;
+#pragma unroll
+      for (int ps = 0; ps < 4; ++ps) {  // 16 p at a time
+        uint32_t yt[16], y2[16], ya[16];
+        tc::tmem_ld16(ycol + 16 * ps, yt);
+        tc::tmem_ld16(ycol + 64 + 16 * ps, y2);
+        if (i0 > 0) tc::tmem_ld16(ycol + 128 + 16 * ps, ya);
+        tc::tmem_ld_wait();
+        uint32_t out[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          float o0, o1;
+          fma2(o0, o1, e_i, e_i, __uint_as_float(y2[2 * q]), __uint_as_float(y2[2 * q + 1]),
+               __uint_as_float(yt[2 * q]), __uint_as_float(yt[2 * q + 1]));
+          if (i0 > 0)
+            fma2(o0, o1, u_i, u_i, __uint_as_float(ya[2 * q]), __uint_as_float(ya[2 * q + 1]), o0, o1);
+          const uint32_t xp = xr[8 * ps + q];
+          fma2(o0, o1, Dh, Dh, bf_lo(xp), bf_hi(xp), o0, o1);
+          out[q] = pack_bf16(o0, o1);
+        }
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int chunk = 2 * ps + cc;
+          *reinterpret_cast<uint4*>(yrow + ((chunk ^ (r & 7)) << 4)) =
+              make_uint4(out[4 * cc], out[4 * cc + 1], out[4 * cc + 2], out[4 * cc + 3]);
+        }
+      }
+      tc::fence_before_sync();
+      fence_proxy_async_smem();
+      named_bar_sync(kScEpiBar, kScEpi);
+      if (et == 0) {
+        mbar_arrive(&bars[kYFree + b]);  // accumulator set b may be overwritten
+        tc::tma_store_3d(&map_y, base + L.y0, h * 64, tok0 + i0, (int)bi);
+        bulk_commit();
+      }
+    }
+    if (et == 0) bulk_wait<0>();
   }
 
   tc::fence_before_sync();
