@@ -24,16 +24,17 @@ constexpr int kCsWarps = kCsThreads / 32;
 constexpr int kCsHeadsPerWarp = kCsHeads / kCsWarps;
 constexpr int kCsLoads = kCsMaxChunk * kCsHeads / kCsThreads;
 
-// Raw bits of one dt value through the read-only path.  The loads are volatile asm so that all
-// of a thread's loads are issued, in order, before the first conversion waits on one of them.
+// Raw bits of one dt value.  The loads are volatile asm so that all of a thread's loads are
+// issued, in order, before the first conversion waits on one of them.  (Not the read-only
+// path: under programmatic dependent launch the previous kernel may have just written dt.)
 __device__ __forceinline__ uint32_t ld_bits(const __nv_bfloat16* p) {
   unsigned short v;
-  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  asm volatile("ld.global.u16 %0, [%1];" : "=h"(v) : "l"(p));
   return (uint32_t)v << 16;  // bf16 bits in the top half are the f32 bits
 }
 __device__ __forceinline__ uint32_t ld_bits(const float* p) {
   uint32_t v;
-  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  asm volatile("ld.global.b32 %0, [%1];" : "=r"(v) : "l"(p));
   return v;
 }
 
@@ -43,6 +44,8 @@ __global__ void __launch_bounds__(kCsThreads) ssd_chunk_cumsum_kernel(const DtT*
                                                                        float* __restrict__ G, float* __restrict__ dtT,
                                                                        WsHeader* hdr) {
   extern __shared__ float s_dt[];  // [chunk][kCsHeads + 1]
+  griddep_launch_dependents();
+  griddep_wait();  // dt may come from, and G / dtT may still be read by, the previous kernel
   const int c = blockIdx.x, hblk = blockIdx.y;
   const int64_t bi = blockIdx.z;
   const int T = d.chunk, nh = d.nheads;
@@ -141,14 +144,11 @@ cudaError_t launch_ssd_chunk_cumsum(const void* dt, const float* A, const SsdDim
                                     cudaStream_t s) {
   dim3 grid((unsigned)d.nchunks, (unsigned)((d.nheads + kCsHeads - 1) / kCsHeads), (unsigned)d.batch);
   const size_t smem = sizeof(float) * d.chunk * (kCsHeads + 1);
-  if (d.dtype == SSM_BF16) {
-    ssd_chunk_cumsum_kernel<__nv_bfloat16><<<grid, kCsThreads, smem, s>>>(
-        static_cast<const __nv_bfloat16*>(dt), A, d, ws.G, ws.dtT, ws.hdr);
-  } else {
-    ssd_chunk_cumsum_kernel<float><<<grid, kCsThreads, smem, s>>>(static_cast<const float*>(dt), A, d, ws.G,
-                                                                   ws.dtT, ws.hdr);
-  }
-  return cudaGetLastError();
+  if (d.dtype == SSM_BF16)
+    return launch_pdl(ssd_chunk_cumsum_kernel<__nv_bfloat16>, grid, dim3(kCsThreads), smem, s,
+                      static_cast<const __nv_bfloat16*>(dt), A, d, ws.G, ws.dtT, ws.hdr);
+  return launch_pdl(ssd_chunk_cumsum_kernel<float>, grid, dim3(kCsThreads), smem, s, static_cast<const float*>(dt),
+                    A, d, ws.G, ws.dtT, ws.hdr);
 }
 
 }  // namespace ssm

@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.bars + 16 * 8 + 4);
   float* v_all = reinterpret_cast<float*>(base + L.v0);
 
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // work item -> (batch, chunk, group, row tile, run of heads)
   int64_t item = blockIdx.x;
@@ -176,6 +177,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();  // set-up above touched no global memory; h_in comes from the previous kernel
   auto fail = [&](void) {
     record_error(p.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
     *abort_flag = 1;
@@ -604,8 +606,8 @@ cudaError_t launch_ssd_chunk_scan_tc(const void* x, const void* B, const void* C
       cudaSuccess)
     return e;
   const int64_t grid = tiles * p.items_per_tile;
-  ssd_chunk_scan_tc_kernel<<<(unsigned)grid, kScThreads, smem, s>>>(map_c, map_b, map_x, map_hin, map_y, p, ctl);
-  return cudaGetLastError();
+  return launch_pdl(ssd_chunk_scan_tc_kernel, dim3((unsigned)grid), dim3(kScThreads), smem, s, map_c, map_b, map_x,
+                    map_hin, map_y, p, ctl);
 }
 
 }  // namespace ssm

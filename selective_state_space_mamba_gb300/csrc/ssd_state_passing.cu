@@ -47,6 +47,8 @@ __global__ void __launch_bounds__(kSpThreads) ssd_state_passing_kernel(const flo
                                                                         SsdWorkspace ws, LookbackCtl ctl) {
   __shared__ uint32_t s_tile;
   __shared__ int s_last, s_found;
+  griddep_launch_dependents();
+  griddep_wait();  // S_c, G and the claim counter come from the previous kernels
 
   if (threadIdx.x == 0) s_tile = claim_tile(ws.hdr);
   __syncthreads();
@@ -208,6 +210,8 @@ __global__ void __launch_bounds__(kSeqThreads) ssd_state_passing_seq_kernel(cons
                                                                             float* __restrict__ h_final, SsdDims d,
                                                                             SsdWorkspace ws) {
   __shared__ float4 ring[kSeqAhead][kSeqThreads];
+  griddep_launch_dependents();
+  griddep_wait();  // S_c and G come from the previous kernels
   const int HS = d.headdim * d.dstate;
   const int64_t q4 = HS / 4;
   const int64_t gidx = (int64_t)blockIdx.x * kSeqThreads + threadIdx.x;
@@ -269,17 +273,15 @@ cudaError_t launch_ssd_state_passing(const float* h0, float* h_final, const SsdD
     const int64_t groups = d.batch * d.nheads * (int64_t)(d.headdim * d.dstate / 4);
     const unsigned grid = (unsigned)((groups + kSeqThreads - 1) / kSeqThreads);
     if (d.dtype == SSM_BF16)
-      ssd_state_passing_seq_kernel<__nv_bfloat16><<<grid, kSeqThreads, 0, s>>>(h0, h_final, d, ws);
-    else
-      ssd_state_passing_seq_kernel<float><<<grid, kSeqThreads, 0, s>>>(h0, h_final, d, ws);
-    return cudaGetLastError();
+      return launch_pdl(ssd_state_passing_seq_kernel<__nv_bfloat16>, dim3(grid), dim3(kSeqThreads), 0, s, h0, h_final,
+                        d, ws);
+    return launch_pdl(ssd_state_passing_seq_kernel<float>, dim3(grid), dim3(kSeqThreads), 0, s, h0, h_final, d, ws);
   }
-  if (d.dtype == SSM_BF16) {
-    ssd_state_passing_kernel<__nv_bfloat16><<<(unsigned)ws.sp_tiles, kSpThreads, 0, s>>>(h0, h_final, d, ws, ctl);
-  } else {
-    ssd_state_passing_kernel<float><<<(unsigned)ws.sp_tiles, kSpThreads, 0, s>>>(h0, h_final, d, ws, ctl);
-  }
-  return cudaGetLastError();
+  if (d.dtype == SSM_BF16)
+    return launch_pdl(ssd_state_passing_kernel<__nv_bfloat16>, dim3((unsigned)ws.sp_tiles), dim3(kSpThreads), 0, s,
+                      h0, h_final, d, ws, ctl);
+  return launch_pdl(ssd_state_passing_kernel<float>, dim3((unsigned)ws.sp_tiles), dim3(kSpThreads), 0, s, h0,
+                    h_final, d, ws, ctl);
 }
 
 }  // namespace ssm

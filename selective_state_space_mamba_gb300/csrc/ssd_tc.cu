@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.bars + 24 * 8 + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_launch_dependents();
   const int64_t u_begin = (int64_t)blockIdx.x * p.units / gridDim.x;
   const int64_t u_end = (int64_t)(blockIdx.x + 1) * p.units / gridDim.x;
 
@@ -143,6 +144,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();  // set-up above touched no global memory; G and dt come from the previous kernel
   auto fail = [&](void) {
     record_error(p.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
     *abort_flag = 1;
@@ -389,8 +391,8 @@ cudaError_t launch_ssd_chunk_state_tc(const void* x, const void* B, const SsdDim
     return e;
   // one CTA per SM (shared memory allows no second), each with an equal share of the units
   const int64_t grid = p.units < sms ? p.units : sms;
-  ssd_chunk_state_tc_kernel<<<(unsigned)grid, kCsThreads, smem, s>>>(map_x, map_b, map_sc, p, ctl);
-  return cudaGetLastError();
+  return launch_pdl(ssd_chunk_state_tc_kernel, dim3((unsigned)grid), dim3(kCsThreads), smem, s, map_x, map_b, map_sc, p,
+                    ctl);
 }
 
 }  // namespace ssm

@@ -144,6 +144,33 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
 // Named barrier that also ORs `pred` over the participating threads: every thread gets the
 // same answer, so a bounded wait that gave up in one thread makes all of them leave together
 // (a thread that left alone would strand the others in the next barrier).
+// ---- programmatic dependent launch ----
+// A kernel started with launch_pdl may begin while the previous kernel of the stream is still
+// running.  It lets its own successor start early (griddep_launch_dependents, at entry) and
+// must pass griddep_wait (every thread that touches global memory) before it reads or writes
+// anything in global memory: the previous kernel may be producing its inputs or still reading
+// its outputs.  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 __device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t count, bool pred) {
   uint32_t r;
   asm volatile(
