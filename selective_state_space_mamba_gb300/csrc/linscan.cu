@@ -100,6 +100,16 @@ struct LsArgs {
   int64_t lines;  // n / 32: full 128-byte lines covered by the tensor maps (0: no TMA)
 };
 
+// Position within its row of element e0 of a tile whose first element sits at r0 (< len):
+// (r0 + e0) mod len, without a division when rows are at least a tile long.
+__device__ __forceinline__ int64_t row_pos(int64_t r0, int e0, int64_t len) {
+  if (len >= kLsTile) {
+    const int64_t v = r0 + e0;
+    return v >= len ? v - len : v;
+  }
+  return (r0 + e0) % len;
+}
+
 // Shared-memory word index of 16-byte chunk `chunk` (0..7) of line `line` in the 128-byte
 // swizzled box.  The eight lanes of a quarter-warp read eight different bank groups.
 __device__ __forceinline__ int swz(int line, int chunk) { return line * kLsRow + ((chunk ^ (line & 7)) << 2); }
@@ -293,7 +303,9 @@ __global__ void __launch_bounds__(kLsBlock, SSM_LS_MIN_BLOCKS)
       const float* sa = sh.stage[st].a;
       const float* sb = sh.stage[st].b;
       Pair tot{1.f, 0.f};
-      int64_t m = (cur_r0 + e0) % p.len;  // position of my first element within its row
+      int64_t m = row_pos(cur_r0, e0, p.len);  // position of my first element within its row
+      // no row starts among my elements: the plain combine, without the per-element row logic
+      const bool no_reset = m != 0 && m + kLsElems <= p.len;
 #pragma unroll
       for (int c = 0; c < kLsElems / 4; ++c) {
         float va[4], vb[4];
@@ -310,11 +322,19 @@ __global__ void __launch_bounds__(kLsBlock, SSM_LS_MIN_BLOCKS)
             vb[j] = e < nv ? p.b[tile_base + e] : 0.f;
           }
         }
+        if (no_reset) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const Pair q{m == 0 ? 0.f : va[j], vb[j]};
-          tot = (c == 0 && j == 0) ? q : combine(tot, q);
-          if (++m == p.len) m = 0;
+          for (int j = 0; j < 4; ++j) {
+            const Pair q{va[j], vb[j]};
+            tot = (c == 0 && j == 0) ? q : combine(tot, q);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const Pair q{m == 0 ? 0.f : va[j], vb[j]};
+            tot = (c == 0 && j == 0) ? q : combine(tot, q);
+            if (++m == p.len) m = 0;
+          }
         }
       }
       Pair inc = tot;
@@ -368,7 +388,8 @@ __global__ void __launch_bounds__(kLsBlock, SSM_LS_MIN_BLOCKS)
       float* sa = sh.stage[ps].a;
       const float* sb = sh.stage[ps].b;
       float hcur = apply(prev_excl, apply(prev_wp, x));  // state before my line
-      int64_t m = (prev_r0 + e0) % p.len;
+      int64_t m = row_pos(prev_r0, e0, p.len);
+      const bool no_reset = m != 0 && m + kLsElems <= p.len;
 #pragma unroll
       for (int c = 0; c < kLsElems / 4; ++c) {
         float va[4], vb[4];
@@ -386,11 +407,19 @@ __global__ void __launch_bounds__(kLsBlock, SSM_LS_MIN_BLOCKS)
           }
         }
         float o[4];
+        if (no_reset) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          hcur = (m == 0) ? vb[j] : fmaf(va[j], hcur, vb[j]);
-          o[j] = hcur;
-          if (++m == p.len) m = 0;
+          for (int j = 0; j < 4; ++j) {
+            hcur = fmaf(va[j], hcur, vb[j]);
+            o[j] = hcur;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            hcur = (m == 0) ? vb[j] : fmaf(va[j], hcur, vb[j]);
+            o[j] = hcur;
+            if (++m == p.len) m = 0;
+          }
         }
         if (in_map) {
           *reinterpret_cast<float4*>(&sa[swz(my_line, my_chunk0 + c)]) = make_float4(o[0], o[1], o[2], o[3]);
