@@ -115,9 +115,13 @@ __device__ __forceinline__ int64_t row_pos(int64_t r0, int e0, int64_t len) {
 __device__ __forceinline__ int swz(int line, int chunk) { return line * kLsRow + ((chunk ^ (line & 7)) << 2); }
 
 // Producer (one thread): claim tiles in counter order and fill the stage ring; it ends after
-// the first claim past the last tile, which it hands on as a sentinel.
+// the first claim past the last tile, which it hands on as a sentinel.  Each claim is made
+// one tile ahead, so the atomic's round trip overlaps the wait for a free stage.  Progress is
+// unchanged: the smallest unfinished tile, if it is only claimed, waits for a stage that
+// holds smaller tiles, all of which are finished.
 __device__ void ls_producer(LsShared& sh, const LsArgs& p, const CUtensorMap* map_a, const CUtensorMap* map_b,
                             const LinscanWorkspace& ws, const LookbackCtl& ctl) {
+  int64_t tile = claim_tile(ws.hdr);
   for (int i = 0;; ++i) {
     const int st = i % kLsStages;
     const int use = i / kLsStages;
@@ -125,7 +129,6 @@ __device__ void ls_producer(LsShared& sh, const LsArgs& p, const CUtensorMap* ma
       record_error(ws.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
       return;  // the consumers give up on their own bounded wait
     }
-    const int64_t tile = claim_tile(ws.hdr);
     sh.tile[st] = tile;
     if (tile >= ws.tiles) {
       mbar_arrive(&sh.full[st]);  // sentinel, no data
@@ -141,6 +144,7 @@ __device__ void ls_producer(LsShared& sh, const LsArgs& p, const CUtensorMap* ma
     } else {
       mbar_arrive(&sh.full[st]);  // only the ragged tail: consumers read it directly
     }
+    tile = claim_tile(ws.hdr);
   }
 }
 
