@@ -37,7 +37,8 @@ METRIC = "SSD fwd tokens/s + % of roofline; linear-scan GB/s vs GB300 HBM peak"
 SSD = synth.SSD_B4_L8192
 SCAN = synth.SCAN_384x65536
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNELS = ("linscan_lookback", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan")
+KERNELS = ("linscan_lookback", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
+           "ssd_state_fused")
 
 
 # ----------------------------------------------------------------------------------------
@@ -59,6 +60,8 @@ def kernel_bytes(s):
         "ssd_chunk_state": z["x"] + z["BC"] + z["gd"] + z["chunk_states_f32"],
         "ssd_state_passing": z["chunk_states_f32"] + z["state"] + z["hin"] + z["state"],
         "ssd_chunk_scan": z["x"] + 2 * z["BC"] + z["gd"] + z["hin"] + z["AD"] // 2 + z["y"],
+        # chunk states and state passing in one pass: x, B, G/dt and h0 in; h_in and h_final out
+        "ssd_state_fused": z["x"] + z["BC"] + z["gd"] + z["hin"] + 2 * z["state"],
     }
 
 
@@ -73,7 +76,7 @@ def ssd_flops(s):
     nc = -(-L // T)
     state = 2 * b * nc * nh * T * H * S                 # X~^T B per (b, c, h)
     scan = b * nc * nh * (2 * T * T * H + 2 * T * S * H) + b * nc * G * 2 * T * T * S  # CB once per group
-    return {"ssd_chunk_state": state, "ssd_chunk_scan": scan, "total": state + scan}
+    return {"ssd_chunk_state": state, "ssd_state_fused": state, "ssd_chunk_scan": scan, "total": state + scan}
 
 
 def scan_bytes(rows, length):

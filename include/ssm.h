@@ -181,9 +181,11 @@ SSM_API void ssm_debug_set_lookback_fault(int64_t stall_tile, uint64_t spin_limi
  * recorded events and writes, for each kernel id below, the summed device time in
  * milliseconds and the number of launches (arrays of length SSM_PROFILE_KERNELS).
  * Kernel ids: 0 linscan_lookback, 1 ssd_chunk_cumsum, 2 ssd_chunk_state,
- * 3 ssd_state_passing, 4 ssd_chunk_scan.  Host-side only; process-global; not thread-safe.
+ * 3 ssd_state_passing, 4 ssd_chunk_scan, 5 ssd_state_fused (chunk states and state passing in
+ * one pass; used instead of 2 and 3 where it applies).  Host-side only; process-global; not
+ * thread-safe.
  */
-#define SSM_PROFILE_KERNELS 5
+#define SSM_PROFILE_KERNELS 6
 SSM_API ssm_status ssm_profile_begin(int max_launches);
 SSM_API ssm_status ssm_profile_end(double *ms_out, int64_t *launches_out);
 

@@ -19,7 +19,8 @@ SSM_F32, SSM_BF16 = 0, 1
 EXPORTS = ("ssm_status_string", "ssm_version", "ssm_ssd_fwd_workspace_bytes", "ssm_ssd_fwd",
            "ssm_linscan_workspace_bytes", "ssm_linscan_fwd", "ssm_check_device_status",
            "ssm_debug_set_lookback_fault", "ssm_profile_begin", "ssm_profile_end", "ssm_linscan_fwd_noalloc")
-PROFILE_KERNELS = ("linscan_lookback", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan")
+PROFILE_KERNELS = ("linscan_lookback", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
+                   "ssd_state_fused")
 
 _lib = None
 _lock = threading.Lock()

@@ -17,6 +17,10 @@ bool ssd_tc_supported(const SsdDims& d);
 cudaError_t launch_ssd_chunk_state_tc(const void* x, const void* B, const SsdDims& d, const SsdWorkspace& ws,
                                       const LookbackCtl& ctl, cudaStream_t s);
 bool ssd_scan_tc_supported(const SsdDims& d);
+bool ssd_state_fused_supported(const SsdDims& d);
+cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float* h0, float* h_final,
+                                      const SsdDims& d, const SsdWorkspace& ws, const LookbackCtl& ctl,
+                                      cudaStream_t s);
 cudaError_t launch_ssd_chunk_scan_tc(const void* x, const void* B, const void* C, const float* D, void* y,
                                      const SsdDims& d, const SsdWorkspace& ws, const LookbackCtl& ctl,
                                      cudaStream_t s);
@@ -268,14 +272,23 @@ ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void
 
   const bool state_tc = ssd_tc_supported(d);
   const bool scan_tc = ssd_scan_tc_supported(d);
+  const bool fused = state_tc && ssd_state_fused_supported(d);
   if (timed_launch(1, s, [&] { return launch_ssd_chunk_cumsum(dt, A, d, ws, s); }) != cudaSuccess)
     return SSM_ERR_CUDA;
-  if (timed_launch(2, s, [&] {
-        return state_tc ? launch_ssd_chunk_state_tc(x, B, d, ws, ctl, s) : launch_ssd_chunk_state_simt(x, B, d, ws, s);
-      }) != cudaSuccess)
-    return SSM_ERR_CUDA;
-  if (timed_launch(3, s, [&] { return launch_ssd_state_passing(h0, h_final, d, ws, ctl, s); }) != cudaSuccess)
-    return SSM_ERR_CUDA;
+  if (fused) {
+    // chunk states and the recurrence over chunks in one pass: S_c never goes to memory
+    if (timed_launch(5, s, [&] { return launch_ssd_state_fused_tc(x, B, h0, h_final, d, ws, ctl, s); }) !=
+        cudaSuccess)
+      return SSM_ERR_CUDA;
+  } else {
+    if (timed_launch(2, s, [&] {
+          return state_tc ? launch_ssd_chunk_state_tc(x, B, d, ws, ctl, s)
+                          : launch_ssd_chunk_state_simt(x, B, d, ws, s);
+        }) != cudaSuccess)
+      return SSM_ERR_CUDA;
+    if (timed_launch(3, s, [&] { return launch_ssd_state_passing(h0, h_final, d, ws, ctl, s); }) != cudaSuccess)
+      return SSM_ERR_CUDA;
+  }
   if (timed_launch(4, s, [&] {
         return scan_tc ? launch_ssd_chunk_scan_tc(x, B, C, D, y, d, ws, ctl, s)
                   : launch_ssd_chunk_scan_simt(x, B, C, D, y, d, ws, s);

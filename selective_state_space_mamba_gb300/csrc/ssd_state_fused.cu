@@ -1,0 +1,393 @@
+// ssd_state_fused_tc: the chunk states and the inter-chunk recurrence of the Mamba-2 SSD
+// forward in one pass, for bf16 inputs ("Accelerating Mamba-2 with High-Performance Forward
+// Pass Kernels in NVIDIA CUDA Tile", "Kernel 2: fwd_pass_state": the chunk loop runs inside one
+// program and every chunk-initial state is written once):
+//     h_in[0] = h0,   h_in[c+1] = 2^(G_last[c]) h_in[c] + X_c^T (w_c . B_c),   h_final = h_in[nc]
+// with w_t = dt_t 2^(G_last - G_t) inside chunk c.
+//
+// One CTA walks the chunks of one (batch, head pair) in order.  The pair's rows (2 heads x 64 p
+// = 128 TMEM lanes, x 128 s columns, f32) have three TMEM homes: the running state h and two
+// accumulators S[0], S[1].  The MMAs add chunk c's weighted X^T B into S[c & 1] without
+// waiting for the state; the state warps then write h out as h_in[c] (bf16), fold S[c & 1] in
+// (h = 2^(G_last) h + S) and release the accumulator for chunk c + 2.  The weighted X is split
+// into bf16 hi + lo halves exactly as in ssd_chunk_state_tc, so the state keeps f32 accuracy.
+// The per-chunk increments S_c never go to memory: against the chunk-state + state-passing
+// pair this saves writing and re-reading them (f32) entirely.
+//
+// Warps (448 threads):
+//   warp 0     TMA producer: per 64-token step, X of the pair's two heads, the step's rows of
+//              the group's B, and the step's G and dt with the chunk's last G, into a ring
+//   warp 1     TMEM owner and MMA issuer (one thread): per chunk, once S[c & 1] is free,
+//              2 x 4 MMAs (hi, lo) per step accumulating into it
+//   warps 2-9  scalers: half a token row per thread, x w -> hi (in place) + lo
+//   warps 10-13 state warps, one state row per thread: h0 in, h_in out per chunk, the decay and
+//              S folded in, h_final at the end
+// Every wait is bounded; on expiry the CTA records SSM_ERR_TIMEOUT, drains, frees its TMEM and
+// returns.
+#include "tc_common.cuh"
+
+namespace ssm {
+namespace {
+
+constexpr int kSfThreads = 448;  // warps 0 producer, 1 MMA, 2-9 scalers, 10-13 state
+constexpr int kSfKH = 64;         // tokens per step
+constexpr int kSfStages = 4;      // one chunk of 256 tokens in flight
+constexpr int kSfRowBytes = 128;  // 64 bf16 per swizzled row
+constexpr uint32_t kSfScaleBar = 1, kSfStateBar = 2;
+constexpr uint32_t kSfTmemCols = 512;  // h at 0, S[0] at 128, S[1] at 256
+constexpr uint32_t kSfGdHead = (2 * kSfKH + 4) * 4;  // G[64], dt[64], G[T-4 .. T-1] of one head
+
+struct SfParams {
+  const float* G;
+  const float* dtT;
+  const float* h0;   // [b, nh, 64, 128] f32 or null (zeros)
+  __nv_bfloat16* hin;  // [b, nc, nh, 64, 128]
+  float* h_final;    // [b, nh, 64, 128] or null
+  WsHeader* hdr;
+  int64_t lpad, nchunks;
+  int nheads, ngroups, chunk;
+};
+
+// Shared memory (offsets from a 1024-byte aligned base):
+//   stage[2] = { hi[2 heads][64 rows][128 B], lo[2 heads][64 rows][128 B],
+//                B[2 s blocks][64 rows][128 B] }                       all swizzled
+//   gd[2 stages][2 heads]
+//   barriers, TMEM base, abort flag
+struct SfLayout {
+  uint32_t half_bytes, b_off, stage_bytes, gd0, bars, total;
+  __host__ __device__ SfLayout() {
+    half_bytes = 2u * kSfKH * kSfRowBytes;  // 16 KB
+    b_off = 2u * half_bytes;
+    stage_bytes = b_off + 2u * kSfKH * kSfRowBytes;  // 48 KB
+    gd0 = kSfStages * stage_bytes;
+    bars = gd0 + kSfStages * 2u * kSfGdHead;
+    total = bars + 24 * 8 + 16;
+  }
+};
+enum SfBar {
+  kXFull = 0, kXScaled = kXFull + kSfStages, kXEmpty = kXScaled + kSfStages, kSReady = kXEmpty + kSfStages,
+  kSFree = kSReady + 2, kDone = kSFree + 2, kSfNumBars = kDone + 1
+};
+
+// d = a * b + c on bf16 pairs, one rounding
+__device__ __forceinline__ uint32_t sf_fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t sf_bf16_pair(float v) {
+  const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  return h | (h << 16);
+}
+__device__ __forceinline__ uint32_t sf_pack(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(kSfThreads, 1)
+    ssd_state_fused_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_b,
+                              SfParams p, LookbackCtl ctl) {
+  extern __shared__ unsigned char sf_raw[];
+  griddep_launch_dependents();
+  const uint32_t raw = smem_addr(sf_raw);
+  unsigned char* base = sf_raw + ((1024u - (raw & 1023u)) & 1023u);
+  const int T = p.chunk;
+  const SfLayout L;
+  const int nk = T / kSfKH;  // steps per chunk
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.bars + 24 * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.bars + 24 * 8 + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // chain -> (batch, group, pair)
+  const int hpg = p.nheads / p.ngroups, ppg = hpg / 2;
+  const int pair = (int)(blockIdx.x % ppg);
+  const int g = (int)((blockIdx.x / ppg) % p.ngroups);
+  const int64_t bi = blockIdx.x / ((int64_t)ppg * p.ngroups);
+  const int h = g * hpg + 2 * pair;  // first head of the pair
+  const int64_t nc = p.nchunks;
+  const int64_t nsteps = nc * nk;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSfNumBars; ++i) mbar_init(&bars[i], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, kSfTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  griddep_wait();  // G and dt come from the previous kernel
+  auto fail = [&](void) {
+    record_error(p.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
+    *abort_flag = 1;
+  };
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ------------------------------------------
+    if (lane == 0) {
+      int64_t i = 0;
+      bool ok = true;
+      for (; i < nsteps && ok && !*abort_flag; ++i) {
+        const int st = (int)(i % kSfStages);
+        if (i >= kSfStages &&
+            !mbar_wait(&bars[kXEmpty + st], (uint32_t)((i / kSfStages) - 1) & 1u, ctl.spin_limit_ns)) {
+          ok = false;
+          break;
+        }
+        const int64_t c = i / nk;
+        const int kh = (int)(i % nk);
+        const int tok = (int)(c * T + kh * kSfKH);
+        unsigned char* stage = base + st * L.stage_bytes;
+        unsigned char* gd = base + L.gd0 + st * 2 * kSfGdHead;
+        mbar_arrive_expect_tx(&bars[kXFull + st], L.half_bytes + 2u * kSfKH * kSfRowBytes + 2u * kSfGdHead);
+        for (int hh = 0; hh < 2; ++hh)
+          tc::tma_load_3d(stage + hh * kSfKH * kSfRowBytes, &map_x, (h + hh) * 64, tok, (int)bi, &bars[kXFull + st]);
+        for (int sb = 0; sb < 2; ++sb)
+          tc::tma_load_3d(stage + L.b_off + sb * kSfKH * kSfRowBytes, &map_b, g * 128 + sb * 64, tok, (int)bi,
+                          &bars[kXFull + st]);
+        for (int hh = 0; hh < 2; ++hh) {
+          const int64_t row = (bi * p.nheads + h + hh) * p.lpad + c * T;
+          bulk_g2s(gd + hh * kSfGdHead, p.G + row + kh * kSfKH, 4u * kSfKH, &bars[kXFull + st]);
+          bulk_g2s(gd + hh * kSfGdHead + 4u * kSfKH, p.dtT + row + kh * kSfKH, 4u * kSfKH, &bars[kXFull + st]);
+          bulk_g2s(gd + hh * kSfGdHead + 8u * kSfKH, p.G + row + T - 4, 16u, &bars[kXFull + st]);
+        }
+      }
+      if (!ok) fail();
+      // leave no copy in flight (bounded)
+      for (int64_t j = (i > kSfStages ? i - kSfStages : 0); j < i; ++j)
+        mbar_wait(&bars[kXFull + (int)(j % kSfStages)], (uint32_t)(j / kSfStages) & 1u, ctl.spin_limit_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer ---------------------------------------------
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16_f32(128, 128, /*a_mn=*/true, /*b_mn=*/true);
+      const uint32_t ab_lbo = kSfKH * kSfRowBytes;  // head 0 -> head 1 block, s 0..63 -> s 64..127 block
+      const uint32_t sbo = 8 * kSfRowBytes;         // next 8-token group
+      bool ok = true;
+      int64_t i = 0;
+      for (int64_t c = 0; c < nc && ok && !*abort_flag; ++c) {
+        const int sb = (int)(c & 1);
+        const uint32_t acc = tmem + 128u + 128u * sb;
+        // the state warps have folded S[sb] (chunk c - 2) into the state
+        if (c >= 2 && !mbar_wait(&bars[kSFree + sb], (uint32_t)(((c - 2) >> 1) & 1), ctl.spin_limit_ns)) {
+          ok = false;
+          break;
+        }
+        for (int kh = 0; kh < nk; ++kh, ++i) {
+          const int st = (int)(i % kSfStages);
+          if (!mbar_wait(&bars[kXScaled + st], (uint32_t)(i / kSfStages) & 1u, ctl.spin_limit_ns)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const uint32_t hi0 = smem_addr(base + st * L.stage_bytes);
+          const uint32_t lo0 = hi0 + L.half_bytes;
+          const uint32_t b0 = hi0 + L.b_off;
+#pragma unroll
+          for (int ks = 0; ks < kSfKH / 16; ++ks) {
+            const uint32_t koff = ks * 16 * kSfRowBytes;  // 16 tokens = two 8-row groups
+            const uint64_t bdesc = tc::sdesc_sw128(b0 + koff, ab_lbo, sbo);
+            tc::mma_bf16(acc, tc::sdesc_sw128(hi0 + koff, ab_lbo, sbo), bdesc, idesc, kh > 0 || ks > 0);
+            tc::mma_bf16(acc, tc::sdesc_sw128(lo0 + koff, ab_lbo, sbo), bdesc, idesc, true);
+          }
+          tc::mma_commit(&bars[kXEmpty + st]);  // the stage may be refilled
+        }
+        if (ok) tc::mma_commit(&bars[kSReady + sb]);  // S[sb] holds chunk c
+      }
+      if (!ok) fail();
+      tc::mma_commit(&bars[kDone]);
+      mbar_wait(&bars[kDone], 0, ctl.spin_limit_ns);  // every MMA has completed
+    }
+  } else if (warp < 10) {
+    // ---------------- scale X by w, split into bf16 hi + lo parts --------------------------
+    const int st_t = threadIdx.x - 64;  // 0..255
+    const int t = st_t >> 1;            // token row of the step: head t / 64, token t % 64
+    const int part = st_t & 1;          // which half of the row's eight 16-byte chunks
+    const int hh = t / kSfKH, tok = t % kSfKH;
+    for (int64_t i = 0; i < nsteps; ++i) {
+      const int st = (int)(i % kSfStages);
+      const bool bad = !mbar_wait(&bars[kXFull + st], (uint32_t)(i / kSfStages) & 1u, ctl.spin_limit_ns);
+      if (named_bar_any(kSfScaleBar, 256, bad)) {  // leave together, or not at all
+        if (st_t == 0) fail();
+        break;
+      }
+      const float* gd = reinterpret_cast<const float*>(base + L.gd0 + (st * 2 + hh) * kSfGdHead);
+      const float wv = gd[kSfKH + tok] * tc::ex2_approx(gd[2 * kSfKH + 3] - gd[tok]);
+      const __nv_bfloat16 w_hi = __float2bfloat16_rn(wv);
+      const float w_lo = wv - __bfloat162float(w_hi);
+      const uint32_t whi2 = sf_bf16_pair(__bfloat162float(w_hi));
+      const uint32_t nwhi2 = whi2 ^ 0x80008000u;
+      const uint32_t nwlo2 = sf_bf16_pair(-w_lo);
+      unsigned char* hrow = base + st * L.stage_bytes + t * kSfRowBytes;
+      unsigned char* lrow = hrow + L.half_bytes;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const int cc = part * 4 + c4;
+        const int off = (cc ^ (t & 7)) << 4;  // the row's chunks, spread over the banks
+        uint4 v = *reinterpret_cast<const uint4*>(hrow + off);
+        uint32_t* e = reinterpret_cast<uint32_t*>(&v);
+        uint4 r;
+        uint32_t* f = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t x2 = e[k];
+          const uint32_t h2 = sf_fma_bf16x2(x2, whi2, 0x80008000u);  // x w_hi, rounded
+          const uint32_t d2 = sf_fma_bf16x2(x2, nwhi2, h2);           // hi - x w_hi, exact
+          f[k] = sf_fma_bf16x2(x2, nwlo2, d2) ^ 0x80008000u;          // x w - hi, rounded
+          e[k] = h2;
+        }
+        *reinterpret_cast<uint4*>(hrow + off) = v;
+        *reinterpret_cast<uint4*>(lrow + off) = r;
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(kSfScaleBar, 256);
+      if (st_t == 0) mbar_arrive(&bars[kXScaled + st]);
+    }
+  } else {
+    // ------------------------------ state warps --------------------------------------------
+    const int quad = warp & 3;       // TMEM lanes 32*quad .. +31
+    const int m = quad * 32 + lane;  // state row: head h + m / 64, p = m % 64
+    const int hh = m >> 6, pp = m & 63;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    const int64_t bh = bi * p.nheads + h + hh;
+    const float* h0r = p.h0 ? p.h0 + (bh * 64 + pp) * 128 : nullptr;
+    const float* Glast = p.G + bh * p.lpad + (T - 1);  // G_last of chunk c at Glast[c * T]
+    for (int64_t c = 0; c < nc; ++c) {
+      const int sb = (int)(c & 1);
+      const bool bad = !mbar_wait(&bars[kSReady + sb], (uint32_t)((c >> 1) & 1), ctl.spin_limit_ns);
+      if (named_bar_any(kSfStateBar, 128, bad)) {  // S[sb] holds chunk c
+        if (m == 0) fail();
+        break;
+      }
+      tc::fence_after_sync();
+      const float dec = exp2f(Glast[c * T]);  // decay over chunk c
+      __nv_bfloat16* hr = p.hin + (((bi * nc + c) * p.nheads + h + hh) * 64 + pp) * 128;
+      const bool last = c == nc - 1;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {  // 32 columns (s) at a time
+        float v[32];
+        uint32_t sv[32];
+        tc::tmem_ld32(tmem + lane_base + 128u + 128u * sb + 32 * q, sv);
+        if (c == 0) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 f = h0r ? reinterpret_cast<const float4*>(h0r + 32 * q)[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+          }
+        } else {
+          uint32_t r[32];
+          tc::tmem_ld32(tmem + lane_base + 32 * q, r);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        }
+        tc::tmem_ld_wait();
+        // h_in[c] (bf16): the state entering chunk c
+        uint4* o = reinterpret_cast<uint4*>(hr + 32 * q);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          o[j] = make_uint4(sf_pack(v[8 * j], v[8 * j + 1]), sf_pack(v[8 * j + 2], v[8 * j + 3]),
+                            sf_pack(v[8 * j + 4], v[8 * j + 5]), sf_pack(v[8 * j + 6], v[8 * j + 7]));
+        // the state after chunk c
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = fmaf(dec, v[j], __uint_as_float(sv[j]));
+        if (last) {
+          if (p.h_final) {
+            float4* f = reinterpret_cast<float4*>(p.h_final + (bh * 64 + pp) * 128 + 32 * q);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          }
+        } else {
+          uint32_t s0[16], s1[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            s0[j] = __float_as_uint(v[j]);
+            s1[j] = __float_as_uint(v[16 + j]);
+          }
+          tc::tmem_st16(tmem + lane_base + 32 * q, s0);
+          tc::tmem_st16(tmem + lane_base + 32 * q + 16, s1);
+        }
+      }
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      named_bar_sync(kSfStateBar, 128);
+      if (m == 0) mbar_arrive(&bars[kSFree + sb]);  // S[sb] may take chunk c + 2
+    }
+    if (nc == 0 && p.h_final) {  // no chunks: the final state is the initial one
+      float4* f = reinterpret_cast<float4*>(p.h_final + (bh * 64 + pp) * 128);
+#pragma unroll 4
+      for (int j = 0; j < 32; ++j) f[j] = h0r ? reinterpret_cast<const float4*>(h0r)[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kSfTmemCols);
+  }
+}
+
+}  // namespace
+
+// One CTA per (batch, head pair) walks all chunks.  Per 64-token step it does the same work as
+// ssd_chunk_state_tc, so against the chunk-state + state-passing pair it saves the f32 chunk
+// states' round trip and the second launch, but it serialises each chain's chunks and cannot
+// spread a chain over several SMs.  It wins when all chains fit in one wave and are short
+// (b8 L2048 nh24: 42 us against ~49 us); with more chains than SMs the second wave costs a
+// whole chain (b4 L8192 nh80, 160 chains: 264 us against 211 us).
+bool ssd_state_fused_supported(const SsdDims& d) {
+  if (!(d.dtype == SSM_BF16 && d.headdim == 64 && d.dstate == 128 && (d.nheads / d.ngroups) % 2 == 0 &&
+        d.chunk % kSfKH == 0 && d.chunk <= 256))
+    return false;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return false;
+  const int64_t chains = d.batch * (int64_t)(d.nheads / 2);
+  return chains <= sms && d.nchunks <= 16;
+}
+
+cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float* h0, float* h_final,
+                                      const SsdDims& d, const SsdWorkspace& ws, const LookbackCtl& ctl,
+                                      cudaStream_t s) {
+  CUtensorMap map_x, map_b;
+  const uint64_t xd[3] = {(uint64_t)d.nheads * 64, (uint64_t)d.seqlen, (uint64_t)d.batch};
+  const uint64_t xs[2] = {(uint64_t)d.nheads * 64 * 2, (uint64_t)d.seqlen * d.nheads * 64 * 2};
+  const uint64_t bd[3] = {(uint64_t)d.ngroups * 128, (uint64_t)d.seqlen, (uint64_t)d.batch};
+  const uint64_t bs[2] = {(uint64_t)d.ngroups * 128 * 2, (uint64_t)d.seqlen * d.ngroups * 128 * 2};
+  const uint32_t box[3] = {64, (uint32_t)kSfKH, 1};
+  cudaError_t e;
+  if ((e = encode_tensor_map_3d(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, xd, xs, box, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+      cudaSuccess)
+    return e;
+  if ((e = encode_tensor_map_3d(&map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, bd, bs, box, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+      cudaSuccess)
+    return e;
+  SfParams p;
+  p.G = ws.G;
+  p.dtT = ws.dtT;
+  p.h0 = h0;
+  p.hin = static_cast<__nv_bfloat16*>(ws.hin);
+  p.h_final = h_final;
+  p.hdr = ws.hdr;
+  p.lpad = d.lpad;
+  p.nchunks = d.nchunks;
+  p.nheads = d.nheads;
+  p.ngroups = d.ngroups;
+  p.chunk = d.chunk;
+  const SfLayout L;
+  const size_t smem = L.total + 1024;
+  if ((e = cudaFuncSetAttribute(ssd_state_fused_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+      cudaSuccess)
+    return e;
+  const int64_t chains = d.batch * (int64_t)(d.nheads / 2);
+  return launch_pdl(ssd_state_fused_tc_kernel, dim3((unsigned)chains), dim3(kSfThreads), smem, s, map_x, map_b, p, ctl);
+}
+
+}  // namespace ssm

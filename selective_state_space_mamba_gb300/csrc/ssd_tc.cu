@@ -31,9 +31,9 @@
 //   warp 1      TMEM owner and MMA issuer (one thread): 2 x 4 MMAs (hi, lo) per stage into one
 //               of two 128-column f32 accumulators; tcgen05.commit frees the stage, and after
 //               the last stage of a unit hands the accumulator to the epilogue
-//   warps 2-5   one token row of one head per thread: w = dt 2^(G_last - G_t), then the row's
-//               64 values of X in shared memory -> hi (in place) and lo
-//   warps 6-9   epilogue: TMEM -> registers -> a swizzled 32 x 32 f32 block per warp in shared
+//   warps 2-9   half a token row of one head per thread: w = dt 2^(G_last - G_t), then 32 of
+//               the row's 64 values of X in shared memory -> hi (in place) and lo
+//   warps 10-13 epilogue: TMEM -> registers -> a swizzled 32 x 32 f32 block per warp in shared
 //               memory -> TMA store into S_c; the accumulator is freed after its last TMEM load
 // Every wait is bounded; on expiry the CTA records SSM_ERR_TIMEOUT, drains, frees its TMEM
 // and returns.
@@ -42,7 +42,7 @@
 namespace ssm {
 namespace {
 
-constexpr int kCsWarps = 10;
+constexpr int kCsWarps = 14;  // 0 producer, 1 MMA, 2-9 scalers, 10-13 epilogue
 constexpr int kCsThreads = kCsWarps * 32;
 constexpr int kCsMaxT = 256;
 constexpr int kCsKH = 64;         // tokens per stage
@@ -239,9 +239,11 @@ __global__ void __launch_bounds__(kCsThreads, 1)
       tc::mma_commit(&bars[kDone]);
       mbar_wait(&bars[kDone], 0, ctl.spin_limit_ns);  // every MMA has completed
     }
-  } else if (warp < 6) {
+  } else if (warp < 10) {
     // ---------------- scale X by w, split into bf16 hi + lo parts --------------------------
-    const int t = threadIdx.x - 64;  // token row of the stage: head t / 64, token t % 64
+    const int st_t = threadIdx.x - 64;  // 0..255
+    const int t = st_t >> 1;            // token row of the stage: head t / 64, token t % 64
+    const int part = st_t & 1;          // which half of the row's eight 16-byte chunks
     const int hh = t / kCsKH, tok = t % kCsKH;
     int64_t i = 0;
     bool ok = true;
@@ -249,8 +251,8 @@ __global__ void __launch_bounds__(kCsThreads, 1)
       for (int kh = 0; kh < nk; ++kh, ++i) {
         const int st = (int)(i % kCsStages);
         const bool bad = !mbar_wait(&bars[kXFull + st], (uint32_t)(i / kCsStages) & 1u, ctl.spin_limit_ns);
-        if (named_bar_any(kCsScaleBar, 128, bad)) {  // leave together, or not at all
-          if (t == 0) fail();
+        if (named_bar_any(kCsScaleBar, 256, bad)) {  // leave together, or not at all
+          if (st_t == 0) fail();
           ok = false;
           break;
         }
@@ -264,8 +266,9 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         unsigned char* hrow = base + st * L.stage_bytes + t * kCsRowBytes;
         unsigned char* lrow = hrow + L.half_bytes;
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          const int off = (cc ^ (t & 7)) << 4;  // every chunk of the row; spread over the banks
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const int cc = part * 4 + c4;
+          const int off = (cc ^ (t & 7)) << 4;  // the row's chunks, spread over the banks
           uint4 v = *reinterpret_cast<const uint4*>(hrow + off);
           uint32_t* e = reinterpret_cast<uint32_t*>(&v);
           uint4 r;
@@ -282,8 +285,8 @@ __global__ void __launch_bounds__(kCsThreads, 1)
           *reinterpret_cast<uint4*>(lrow + off) = r;
         }
         fence_proxy_async_smem();
-        named_bar_sync(kCsScaleBar, 128);
-        if (t == 0) mbar_arrive(&bars[kXScaled + st]);
+        named_bar_sync(kCsScaleBar, 256);
+        if (st_t == 0) mbar_arrive(&bars[kXScaled + st]);
       }
     }
   } else {
@@ -297,7 +300,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
       const int acc = q & 1;
       const bool bad = !mbar_wait(&bars[kAccFull + acc], (uint32_t)(q >> 1) & 1u, ctl.spin_limit_ns);
       if (named_bar_any(kCsEpiBar, 128, bad)) {  // leave together, or not at all
-        if (threadIdx.x == 192) fail();
+        if (threadIdx.x == 320) fail();
         break;
       }
       tc::fence_after_sync();
@@ -311,7 +314,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         if (cb == 3) {  // the accumulator has been read
           tc::fence_before_sync();
           named_bar_sync(kCsEpiBar, 128);
-          if (threadIdx.x == 192) mbar_arrive(&bars[kAccEmpty + acc]);
+          if (threadIdx.x == 320) mbar_arrive(&bars[kAccEmpty + acc]);
         }
         if (stored) {  // the previous block's store has read the staging rows
           if (lane == 0) bulk_wait_read<0>();
