@@ -238,7 +238,7 @@ def run_ours(args, world, rank, local):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks, ssm.KernelTimer(max_launches=8 * args.steps + 8) as kt:
+    with ClockSampler(local) as clocks:
         time.sleep(0.1)  # let the sampler start
         t_wall0 = time.time()
         t_wall = time.perf_counter()
@@ -253,6 +253,17 @@ def run_ours(args, world, rank, local):
         t_wall = time.perf_counter() - t_wall
         t_wall1 = time.time()
         time.sleep(0.05)
+    barrier(world)
+    # Per-kernel breakdown: the same steps again, with the library's events around every launch.
+    # Those events keep consecutive launches from overlapping (programmatic dependent launch), so
+    # this second timed pass gives the per-kernel times and the roofline, not the headline.
+    torch.cuda.synchronize()
+    with ssm.KernelTimer(max_launches=8 * args.steps + 8) as kt:
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)
+            ssd_call()
+            scan_call()
+        torch.cuda.synchronize()
     barrier(world)
     if ssm.check_device_status(kind="ssd") or ssm.check_device_status(kind="linscan"):
         raise RuntimeError("device status error during the timed region")
@@ -320,6 +331,7 @@ def run_ours(args, world, rank, local):
             "workload": (f"ssd_fwd b{SSD.batch} L{SSD.seqlen} nh{SSD.nheads} H{SSD.headdim} S{SSD.dstate} "
                          f"G{SSD.ngroups} chunk{SSD.chunk} bf16/fp32-acc + linscan {SCAN.rows}x{SCAN.length} f32"),
             "step": "ssd_fwd (4 kernels) then linscan_fwd (1 kernel); value from the ssd_fwd events",
+            "per_kernel": "a second timed pass of the same steps with per-launch events",
             "l2": "inputs larger than L2, and L2 flushed by a 256 MiB write before each timed step",
             "parallelism": f"replicas x{world} (independent problems, no collective)",
         },
