@@ -7,7 +7,7 @@
 // kernels read one head's G and dt as contiguous runs.  dt is written out transposed as f32
 // at the same time, with 0 in the padding of the last chunk (decay 1, no input: exact).
 //
-// One CTA per (chunk, block of 32 heads, batch): the dt tile [chunk, 32 heads] is staged
+// One CTA per (chunk, block of 8 heads, batch): the dt tile [chunk, 8 heads] is staged
 // through shared memory so both the read (heads contiguous) and the writes (tokens
 // contiguous) are coalesced: each warp scans whole head rows in registers, and the results
 // go back through the same shared tile, so that every warp store writes 128 contiguous bytes
@@ -17,7 +17,7 @@
 namespace ssm {
 namespace {
 
-constexpr int kCsHeads = 32;
+constexpr int kCsHeads = 8;
 constexpr int kCsThreads = 256;
 constexpr int kCsMaxChunk = 256;
 constexpr int kCsWarps = kCsThreads / 32;
@@ -60,16 +60,19 @@ __global__ void __launch_bounds__(kCsThreads) ssd_chunk_cumsum_kernel(const DtT*
     hdr->done = 0u;
   }
 
-  // element k of this thread: token warp + 8 k, head lane (a warp reads one token's heads)
+  // element k of this thread: head threadIdx % kCsHeads, token threadIdx / kCsHeads +
+  // (threads / kCsHeads) k: a warp reads whole tokens' head blocks
+  constexpr int kTokStride = kCsThreads / kCsHeads;
+  const int lh = threadIdx.x % kCsHeads, lt = threadIdx.x / kCsHeads;
   const int tmax = d.seqlen - t0 < T ? (int)(d.seqlen - t0) : T;  // real tokens in this chunk
-  const bool head_ok = lane < nhb;
-  const DtT* src = dt + (bi * d.seqlen + t0 + warp) * nh + h0 + (head_ok ? lane : 0);
+  const bool head_ok = lh < nhb;
+  const DtT* src = dt + (bi * d.seqlen + t0 + lt) * nh + h0 + (head_ok ? lh : 0);
   uint32_t raw[kCsLoads];
 #pragma unroll
   for (int k = 0; k < kCsLoads; ++k) {
-    const int t = warp + kCsWarps * k;
+    const int t = lt + kTokStride * k;
     raw[k] = 0u;
-    if (head_ok && t < tmax) raw[k] = ld_bits(src + (int64_t)kCsWarps * k * nh);
+    if (head_ok && t < tmax) raw[k] = ld_bits(src + (int64_t)kTokStride * k * nh);
   }
   float Ah[kCsHeadsPerWarp];
 #pragma unroll
@@ -79,8 +82,8 @@ __global__ void __launch_bounds__(kCsThreads) ssd_chunk_cumsum_kernel(const DtT*
   }
 #pragma unroll
   for (int k = 0; k < kCsLoads; ++k) {
-    const int t = warp + kCsWarps * k;
-    if (t < T) s_dt[t * (kCsHeads + 1) + lane] = __uint_as_float(raw[k]);
+    const int t = lt + kTokStride * k;
+    if (t < T) s_dt[t * (kCsHeads + 1) + lh] = __uint_as_float(raw[k]);
   }
   __syncthreads();
 
