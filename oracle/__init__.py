@@ -7,7 +7,8 @@ The oracle shares no code with the CUDA path: the only common module is the
 seeded input generator, which holds none of the method's arithmetic.
 
 Contents
-  ssd.py      sequential recurrence (numpy, float64), the definition
+  ssd.py      sequential recurrence (numpy, float64), the definition, and
+              its single-token step (the decode step with a carried state)
   linscan.py  sequential scalar scan and the affine pair combine (numpy, float64)
   ssm_oracle.c + native.py
               the same two definitions in plain C (float64, OpenMP over

@@ -70,3 +70,45 @@ def ssd_fwd(x, dt, A, B, C, D, h0=None):
         # y_t = h_t c_t + D x_t
         y[:, t] = np.einsum("bnps,bns->bnp", state, c_t) + D[None, :, None] * x_t
     return y, state
+
+
+def ssd_step(state, x, dt, A, B, C, D):
+    """One token of the recurrence with a carried state: the decode step.
+
+    Same definition and readings as ssd_fwd (the post's section "Mamba-2
+    architecture"), applied to a single new token.  The post contrasts this
+    recurrent form, one state update per token, with the chunked form used
+    for whole sequences; its note that the final state of one call can start
+    the next is what lets a prefill hand its state to the decode loop.
+
+    Args (any float dtype, upcast to float64):
+      state [batch, nheads, H, S] or None (zeros: the first token)
+      x     [batch, nheads, H]
+      dt    [batch, nheads]
+      A, D  [nheads]
+      B, C  [batch, ngroups, S]
+    Returns (y [batch, nheads, H], new state [batch, nheads, H, S]), float64:
+      new state = exp(A dt) state + x (dt B)^T      (H x S per head)
+      y         = new state . c + D x                (inclusive reading)
+    """
+    x = np.asarray(x, np.float64)
+    dt = np.asarray(dt, np.float64)
+    A = np.asarray(A, np.float64)
+    B = np.asarray(B, np.float64)
+    C = np.asarray(C, np.float64)
+    D = np.asarray(D, np.float64)
+    batch, nh, H = x.shape
+    G, S = B.shape[1], B.shape[2]
+    if nh % G:
+        raise ValueError("nheads must be a multiple of ngroups")
+    group_of_head = np.arange(nh) // (nh // G)
+    if state is None:
+        h = np.zeros((batch, nh, H, S))
+    else:
+        h = np.asarray(state, np.float64).reshape(batch, nh, H, S)
+    decay = np.exp(A[None, :] * dt)                        # [batch, nh]
+    b = dt[:, :, None] * B[:, group_of_head]               # [batch, nh, S]
+    c = C[:, group_of_head]                                # [batch, nh, S]
+    h_new = decay[:, :, None, None] * h + x[:, :, :, None] * b[:, :, None, :]
+    y = np.einsum("bnps,bns->bnp", h_new, c) + D[None, :, None] * x
+    return y, h_new

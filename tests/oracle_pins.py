@@ -187,6 +187,73 @@ SSD_PINS = ("pin_chunked", "pin_linear_attention", "pin_skip_only", "pin_state_c
 
 
 # ---------------------------------------------------------------------------
+# decode-step pins: a step callable has the signature of oracle.ssd.ssd_step,
+# (state, x_t, dt_t, A, B_t, C_t, D) -> (y_t, new state)
+# ---------------------------------------------------------------------------
+
+def pin_step_chain(step, ssd, rng):
+    """Stepping token by token from h0 reproduces the sequential forward over the same tokens,
+    and so does a prefill of the first tokens followed by steps from its final state (the
+    post's note that a final state can start the next call).  ``ssd`` is the pinned forward."""
+    x, dt, A, B, C, D, h0 = small_problem(rng, batch=2, L=12, nh=6, H=3, S=5, G=3)
+    y_ref, h_ref = ssd(x, dt, A, B, C, D, h0)
+    for start in (0, 7):
+        if start:
+            _, state = ssd(x[:, :start], dt[:, :start], A, B[:, :start], C[:, :start], D, h0)
+        else:
+            state = h0
+        ys = []
+        for t in range(start, x.shape[1]):
+            yt, state = step(state, x[:, t], dt[:, t], A, B[:, t], C[:, t], D)
+            ys.append(np.asarray(yt))
+        _close(np.stack(ys, axis=1), np.asarray(y_ref)[:, start:], f"steps after {start} prefill tokens: y")
+        _close(state, h_ref, f"steps after {start} prefill tokens: state")
+
+
+def pin_step_from_zero(step, rng):
+    """From a zero state one step gives the rank-one state dt x (outer) B and the readout
+    dt (B . C) x + D x, written out per head with the group of head h at h // (nh / G)."""
+    x, dt, A, B, C, D, _ = small_problem(rng, batch=2, L=1, nh=6, H=3, S=5, G=3)
+    x, dt, B, C = x[:, 0], dt[:, 0], B[:, 0], C[:, 0]
+    y, h = step(None, x, dt, A, B, C, D)
+    y, h = np.asarray(y), np.asarray(h)
+    for bi in range(2):
+        for hd in range(6):
+            g = hd // 2
+            _close(h[bi, hd], np.outer(x[bi, hd], dt[bi, hd] * B[bi, g]), f"zero state: h[{bi},{hd}]")
+            bc = sum(B[bi, g, s] * C[bi, g, s] for s in range(5))
+            _close(y[bi, hd], dt[bi, hd] * bc * x[bi, hd] + D[hd] * x[bi, hd], f"zero state: y[{bi},{hd}]")
+
+
+def pin_step_no_input(step, rng):
+    """dt = 0 leaves the state exactly as it was (decay 1, no input) and reads it out;
+    x = 0 only decays it: new state = exp(A dt) state, y = exp(A dt) (state . c)."""
+    x, dt, A, B, C, D, h0 = small_problem(rng, batch=2, L=1, nh=4, H=3, S=5, G=2)
+    x, dt, B, C = x[:, 0], dt[:, 0], B[:, 0], C[:, 0]
+    y, h = step(h0, x, np.zeros_like(dt), A, B, C, D)
+    assert np.array_equal(np.asarray(h), h0), "dt = 0: state changed"
+    want = np.empty_like(x)
+    for bi in range(2):
+        for hd in range(4):
+            g = hd // 2
+            for p in range(3):
+                want[bi, hd, p] = sum(h0[bi, hd, p, s] * C[bi, g, s] for s in range(5)) + D[hd] * x[bi, hd, p]
+    _close(y, want, "dt = 0: y")
+    y, h = step(h0, np.zeros_like(x), dt, A, B, C, D)
+    dec = np.exp(A[None, :] * dt)
+    _close(h, dec[:, :, None, None] * h0, "x = 0: state")
+    for bi in range(2):
+        for hd in range(4):
+            g = hd // 2
+            for p in range(3):
+                want[bi, hd, p] = dec[bi, hd] * sum(h0[bi, hd, p, s] * C[bi, g, s] for s in range(5))
+    _close(y, want, "x = 0: y")
+
+
+STEP_PINS = ("pin_step_chain", "pin_step_from_zero", "pin_step_no_input")
+
+
+# ---------------------------------------------------------------------------
 # scan pins
 # ---------------------------------------------------------------------------
 
