@@ -10,7 +10,9 @@ by a 256 MiB write before every timed step, outside the timed events.
 Prints ONE JSON line (rank 0).  value = SSD forward tokens/s (batch*seqlen per SSD call,
 summed over ranks, divided by the max over ranks of the SSD device time); the scan's GB/s,
 per-kernel times, the roofline of the dominant kernel, clocks, the end-to-end leg through the
-public API with host buffers, and the float64 oracle timed on the host cores ride along.
+public API with host buffers, and the float64 oracle timed on the host cores ride along.  The
+decode step (ssd_step: one token for each of 128 sequences of the same model shape, f32 state
+carried in place) is timed on its own and reported under "decode".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -36,9 +38,10 @@ from selective_state_space_mamba_gb300 import synth  # noqa: E402
 METRIC = "SSD fwd tokens/s + % of roofline; linear-scan GB/s vs GB300 HBM peak"
 SSD = synth.SSD_B4_L8192
 SCAN = synth.SCAN_384x65536
+STEP = synth.STEP_B128
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNELS = ("linscan_lookback", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
-           "ssd_state_fused")
+           "ssd_state_fused")  # the headline step's kernels; the decode step is timed on its own
 
 
 # ----------------------------------------------------------------------------------------
@@ -77,6 +80,14 @@ def ssd_flops(s):
     state = 2 * b * nc * nh * T * H * S                 # X~^T B per (b, c, h)
     scan = b * nc * nh * (2 * T * T * H + 2 * T * S * H) + b * nc * G * 2 * T * T * S  # CB once per group
     return {"ssd_chunk_state": state, "ssd_state_fused": state, "ssd_chunk_scan": scan, "total": state + scan}
+
+
+def step_bytes(s):
+    """Decode step: the f32 state read and written once, x in, y out, dt, B, C, A, D."""
+    e = 2 if s.dtype == "bf16" else 4
+    state = s.batch * s.nheads * s.headdim * s.dstate * 4
+    return 2 * state + 2 * s.batch * s.nheads * s.headdim * e + s.batch * s.nheads * e \
+        + 2 * s.batch * s.ngroups * s.dstate * e + 2 * s.nheads * 4
 
 
 def scan_bytes(rows, length):
@@ -267,6 +278,7 @@ def run_ours(args, world, rank, local):
     barrier(world)
     if ssm.check_device_status(kind="ssd") or ssm.check_device_status(kind="linscan"):
         raise RuntimeError("device status error during the timed region")
+    decode = run_decode(args, peaks)
 
     ssd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
     scan_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
@@ -341,12 +353,47 @@ def run_ours(args, world, rank, local):
         "linscan": {"value": round(scan_gbs, 1), "unit": "GB/s", "ms": round(scan_ms_max, 4),
                     "alg_bytes": sbytes, "frac": round(scan_gbs / world / peaks["hbm_gbs"], 4)},
         "kernels": kernels,
+        "decode": decode,
         "roofline": roof,
         "gpu_launches": sum(kt.launches.values()),
         "clocks": clocks.summary(t_wall0, t_wall1),
         "wall_s_timed": round(t_wall, 3),
     }
     return out, ssd_np, scan_np
+
+
+def run_decode(args, peaks):
+    """The decode step (ssm_ssd_step) on its own workload: one token for each of 128 sequences,
+    state updated in place, so every step starts from the state the previous one left.  The
+    state (335.5 MB) is larger than L2; CUDA events around every launch on its stream."""
+    import torch
+    import selective_state_space_mamba_gb300 as ssm
+    inp = synth.step_inputs(STEP)
+    d = device_inputs(torch, inp, STEP.dtype)
+    y = torch.empty_like(d["x"])
+    stream = torch.cuda.current_stream()
+
+    def call():
+        ssm.ssd_step(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["state"], y=y, inplace=True)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        call()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    ms = statistics.median(per)
+    nbytes = step_bytes(STEP)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"ssd_step b{STEP.batch} nh{STEP.nheads} H{STEP.headdim} S{STEP.dstate} G{STEP.ngroups} "
+                        f"bf16, f32 state in place",
+            "launches": args.steps, "ms_per_launch": round(ms, 5), "ms_mean": round(sum(per) / len(per), 5),
+            "tokens_per_s": round(STEP.batch / (ms * 1e-3), 1), "alg_bytes": nbytes, "GB/s": round(gbs, 1),
+            "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "timing": "median of per-launch CUDA events"}
 
 
 def run_e2e(args):
@@ -437,7 +484,14 @@ def oracle_sample(ssd_np, scan_np, budget_s, unit_batch):
     t0 = time.perf_counter()
     native.linscan(scan_np["a"], scan_np["b"], rows=np.arange(rows))
     t_scan = time.perf_counter() - t0
+    # decode step: the one-token forward from the carried state, on every unit of the workload
+    st = synth.step_inputs(STEP)
+    t0 = time.perf_counter()
+    native.ssd_fwd(st["x"][:, None], st["dt"][:, None], st["A"], st["B"][:, None], st["C"][:, None], st["D"],
+                   st["state"].astype(np.float64))
+    t_step = time.perf_counter() - t0
     return {
+        "step_tokens_per_s": STEP.batch / t_step, "step_s": t_step,
         "ssd_tokens_per_s": ssd_tokens_equiv / t_ssd, "ssd_units": done, "ssd_s": t_ssd,
         "scan_gbs": scan_bytes(rows, SCAN.length) / t_scan / 1e9, "scan_rows": rows, "scan_s": t_scan,
         "cores": threads,
@@ -510,6 +564,8 @@ def main():
                        f"in {cb['ssd_s']:.1f} s; tokens/s counts a token once all its heads are done"),
             "linscan": {"value": round(cb["scan_gbs"], 2), "unit": "GB/s",
                         "sample": f"{cb['scan_rows']} of {SCAN.rows} rows in {cb['scan_s']:.2f} s"},
+            "decode": {"value": round(cb["step_tokens_per_s"], 1), "unit": "tokens/s",
+                       "sample": f"one whole decode step ({STEP.batch} tokens) in {cb['step_s']:.2f} s"},
         }
     if world > 1:
         import torch.distributed as dist

@@ -1,7 +1,7 @@
 /*
  * ssm.h: C ABI of the GB300 (sm_103a) selective state-space forward library.
  *
- * Two operations, both forward only, both on one GPU:
+ * Three operations, all forward only, all on one GPU:
  *
  *   ssm_ssd_fwd      Mamba-2 chunked SSD forward, (x, dt, A, B, C, D, h0) -> (y, h_final).
  *                    Definition: "Accelerating Mamba-2 with High-Performance Forward
@@ -17,6 +17,10 @@
  *                    run as four kernels (chunk cumsum, chunk state, state passing,
  *                    chunk scan; the post's "Kernel 1".."Kernel 3" with the chunk loop of
  *                    Kernel 2 split into a parallel part and a look-back scan).
+ *
+ *   ssm_ssd_step     the same recurrence for ONE new token per sequence with a carried
+ *                    state (decode): (x, dt, A, B, C, D, state) -> (y, state'), one
+ *                    streaming kernel over the f32 state.
  *
  *   ssm_linscan_fwd  scalar selective scan h[t] = a[t] h[t-1] + b[t], h[-1] = 0, per row.
  *                    Definition: "Selective-scan CUDA kernels", section "The problem";
@@ -117,6 +121,39 @@ SSM_API ssm_status ssm_ssd_fwd(const void *x, const void *dt, const float *A, co
                        int ngroups, int chunk, ssm_dtype dtype,
                        void *workspace, size_t workspace_bytes, ssm_stream_t stream);
 
+/*
+ * Mamba-2 decode step: ONE new token per sequence, with the state carried between calls.
+ * Definition: the recurrence above applied to a single token ("Accelerating Mamba-2 with
+ * High-Performance Forward Pass Kernels in NVIDIA CUDA Tile", section "Mamba-2
+ * architecture": the recurrent form, one state update per token, that the post contrasts
+ * with the chunked form; and its note that the final state of one call can start the next,
+ * so the h_final of ssm_ssd_fwd over a prompt is the state_in of the first step):
+ *     state_out = exp(A dt) state_in + x (dt B)^T      (per head, H x S, S contiguous)
+ *     y         = state_out c + D x                     (inclusive reading)
+ *
+ * Inputs (element type `dtype` unless marked f32):
+ *   x         [batch, nheads, headdim]
+ *   dt        [batch, nheads]            time steps, used as given (already positive)
+ *   A, D      [nheads] f32
+ *   B, C      [batch, ngroups, dstate]   head h reads group h / (nheads / ngroups)
+ *   state_in  [batch, nheads, headdim, dstate] f32, or NULL for zeros (a first token)
+ * Outputs:
+ *   state_out [batch, nheads, headdim, dstate] f32.  It may be the same pointer as
+ *             state_in (the state is then updated in place); any other overlap of the two
+ *             is rejected with SSM_ERR_INVALID_ARG.
+ *   y         [batch, nheads, headdim], element type `dtype`
+ * Sizes: batch >= 0 (0: nothing is enqueued), nheads >= 1, ngroups >= 1 dividing nheads,
+ *   headdim a positive multiple of 16, dstate in {64, 128}.  No workspace.  One kernel is
+ *   enqueued on `stream`; it reads and writes the state once (8 * headdim * dstate bytes per
+ *   head), so it runs at the HBM rate.
+ * Errors: SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_ALIGNMENT (any tensor not 16-byte
+ *   aligned), SSM_ERR_CUDA.
+ */
+SSM_API ssm_status ssm_ssd_step(const void *x, const void *dt, const float *A, const void *B, const void *C,
+                                const float *D, const float *state_in, float *state_out, void *y,
+                                int64_t batch, int nheads, int headdim, int dstate, int ngroups,
+                                ssm_dtype dtype, ssm_stream_t stream);
+
 /* Workspace size in bytes for ssm_linscan_fwd on rows x len (0 when a size is negative). */
 SSM_API size_t ssm_linscan_workspace_bytes(int64_t rows, int64_t len);
 
@@ -175,17 +212,17 @@ SSM_API void ssm_debug_set_lookback_fault(int64_t stall_tile, uint64_t spin_limi
 
 /*
  * Kernel timing (measurement aid; not needed in normal use).  Between ssm_profile_begin()
- * and ssm_profile_end(), every ssm_ssd_fwd / ssm_linscan_fwd call records a CUDA event on its
- * own stream before and after each kernel it launches (at most `max_launches` launches are
- * recorded; later ones are counted but not timed).  ssm_profile_end() synchronizes the
+ * and ssm_profile_end(), every ssm_ssd_fwd / ssm_ssd_step / ssm_linscan_fwd call records a
+ * CUDA event on its own stream before and after each kernel it launches (at most
+ * `max_launches` launches are recorded; later ones are counted but not timed).  ssm_profile_end() synchronizes the
  * recorded events and writes, for each kernel id below, the summed device time in
  * milliseconds and the number of launches (arrays of length SSM_PROFILE_KERNELS).
  * Kernel ids: 0 linscan_lookback, 1 ssd_chunk_cumsum, 2 ssd_chunk_state,
  * 3 ssd_state_passing, 4 ssd_chunk_scan, 5 ssd_state_fused (chunk states and state passing in
- * one pass; used instead of 2 and 3 where it applies).  Host-side only; process-global; not
- * thread-safe.
+ * one pass; used instead of 2 and 3 where it applies), 6 ssd_step (ssm_ssd_step).  Host-side
+ * only; process-global; not thread-safe.
  */
-#define SSM_PROFILE_KERNELS 6
+#define SSM_PROFILE_KERNELS 7
 SSM_API ssm_status ssm_profile_begin(int max_launches);
 SSM_API ssm_status ssm_profile_end(double *ms_out, int64_t *launches_out);
 

@@ -5,6 +5,7 @@ CUDA tensors into the C calls; every step of the computation runs in the library
 kernels, enqueued on the current torch stream.  PyTorch supplies device memory and streams.
 
     y, h_final = ssd_fwd(x, dt, A, B, C, D, h0=None, chunk=256)
+    y_t, state = ssd_step(x_t, dt_t, A, B_t, C_t, D, state)     # one decode token
     h = linscan_fwd(a, b)
 
 Importing the package does not load the library; the first call does (and fails loudly if
@@ -15,7 +16,7 @@ from __future__ import annotations
 from . import _lib
 from ._lib import SSM_BF16, SSM_F32, SsmError
 
-__all__ = ["ssd_fwd", "linscan_fwd", "Workspace", "check_device_status", "ssd_fwd_workspace_bytes",
+__all__ = ["ssd_fwd", "ssd_step", "linscan_fwd", "Workspace", "check_device_status", "ssd_fwd_workspace_bytes",
            "linscan_workspace_bytes", "SsmError", "version"]
 
 
@@ -147,6 +148,43 @@ def ssd_fwd(x, dt, A, B, C, D, h0=None, chunk: int = 256, *, y=None, h_final=Non
                          _ptr(h_final), b, L, nh, H, S, G, chunk, code, ws.ptr(), ws.nbytes, _stream_ptr(x.device))
     _lib.check(st, "ssm_ssd_fwd")
     return y, h_final
+
+
+def ssd_step(x, dt, A, B, C, D, state=None, *, y=None, state_out=None, inplace: bool = False):
+    """Mamba-2 decode step: one new token per sequence (see include/ssm.h, ssm_ssd_step).
+
+    x [b, nh, H], dt [b, nh], B/C [b, G, S] (all float32 or all bfloat16); A, D [nh] float32;
+    state [b, nh, H, S] float32 or None (zeros).  Returns (y, new_state): y like x, new_state
+    float32 [b, nh, H, S].  With ``inplace=True`` the new state overwrites ``state``.
+    """
+    torch = _torch()
+    lib = _lib.load()
+    code = _dtype_code(x)
+    _require(x.dim() == 3 and dt.dim() == 2 and B.dim() == 3 and C.dim() == 3, "bad ranks")
+    b, nh, H = x.shape
+    G, S = B.shape[1], B.shape[2]
+    _require(tuple(dt.shape) == (b, nh), "dt must be [b, nh]")
+    _require(tuple(B.shape) == (b, G, S) and tuple(C.shape) == (b, G, S), "B, C must be [b, G, S]")
+    _require(tuple(A.shape) == (nh,) and tuple(D.shape) == (nh,), "A, D must be [nh]")
+    for name, t in (("dt", dt), ("B", B), ("C", C)):
+        _require(t.dtype == x.dtype, f"{name} must have x's dtype")
+    _require(A.dtype == torch.float32 and D.dtype == torch.float32, "A, D must be float32")
+    for t in [x, dt, A, B, C, D] + ([state] if state is not None else []):
+        _require(t.is_cuda and t.is_contiguous(), "all tensors must be contiguous CUDA tensors")
+    if state is not None:
+        _require(tuple(state.shape) == (b, nh, H, S) and state.dtype == torch.float32,
+                 "state must be f32 [b, nh, H, S]")
+    if inplace:
+        _require(state is not None and state_out is None, "inplace needs a state and no state_out")
+        state_out = state
+    if state_out is None:
+        state_out = torch.empty((b, nh, H, S), dtype=torch.float32, device=x.device)
+    if y is None:
+        y = torch.empty_like(x)
+    st = lib.ssm_ssd_step(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(state), _ptr(state_out),
+                          _ptr(y), b, nh, H, S, G, code, _stream_ptr(x.device))
+    _lib.check(st, "ssm_ssd_step")
+    return y, state_out
 
 
 def linscan_fwd(a, b, *, h=None, workspace: Workspace | None = None):

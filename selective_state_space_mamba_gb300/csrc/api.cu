@@ -297,6 +297,38 @@ ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void
   return SSM_OK;
 }
 
+ssm_status ssm_ssd_step(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                        const float* D, const float* state_in, float* state_out, void* y, int64_t batch, int nheads,
+                        int headdim, int dstate, int ngroups, ssm_dtype dtype, ssm_stream_t stream) {
+  if (batch < 0 || nheads < 1 || headdim < 1 || dstate < 1 || ngroups < 1 || nheads % ngroups != 0)
+    return SSM_ERR_INVALID_ARG;
+  if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_INVALID_ARG;
+  if (headdim % 16 != 0 || (dstate != 64 && dstate != 128)) return SSM_ERR_UNSUPPORTED;
+  if (batch == 0) return SSM_OK;
+  if (!x || !dt || !A || !B || !C || !D || !state_out || !y) return SSM_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, dt, A, B, C, D, state_out, y};
+  for (const void* p : ptrs)
+    if (!aligned(p, 16)) return SSM_ERR_ALIGNMENT;
+  if (state_in && !aligned(state_in, 16)) return SSM_ERR_ALIGNMENT;
+  const int64_t units = batch * nheads;
+  if (units / nheads != batch) return SSM_ERR_INVALID_ARG;
+  const int64_t state_elems = units * headdim * dstate;
+  if (state_elems / ((int64_t)headdim * dstate) != units) return SSM_ERR_INVALID_ARG;
+  if (state_in && state_in != state_out) {
+    // in place is allowed; any other overlap of the two states is not
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(state_in), b0 = reinterpret_cast<uintptr_t>(state_out);
+    const uintptr_t n = sizeof(float) * (uintptr_t)state_elems;
+    if (a0 < b0 + n && b0 < a0 + n) return SSM_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (timed_launch(6, s, [&] {
+        return launch_ssd_step(x, dt, A, B, C, D, state_in, state_out, y, batch, nheads, headdim, dstate, ngroups,
+                               dtype, s);
+      }) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  return SSM_OK;
+}
+
 size_t ssm_linscan_workspace_bytes(int64_t rows, int64_t len) {
   if (rows < 0 || len < 0) return 0;
   return linscan_workspace_layout(rows * len, nullptr).total_bytes;

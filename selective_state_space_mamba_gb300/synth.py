@@ -77,12 +77,35 @@ SSD_B4_L8192 = SSDShape("ssd_b4_L8192_nh80_H64_S128_T256_bf16", 4, 8192, 80, 64,
 SSD_B1_L131072 = SSDShape("ssd_b1_L131072_nh32_H64_S128_G8_T256_bf16", 1, 131072, 32, 64, 128, 8, 256,
                           "bf16", dt_shift=4.0, h0=True)
 
+
+@dataclasses.dataclass(frozen=True)
+class StepShape:
+    """Shape of one decode-step workload: one new token for each of ``batch`` sequences."""
+
+    name: str
+    batch: int
+    nheads: int
+    headdim: int
+    dstate: int
+    ngroups: int
+    dtype: str  # "f32" or "bf16"
+    dt_shift: float = 2.0
+
+    def replace(self, **kw) -> "StepShape":
+        return dataclasses.replace(self, **kw)
+
+
+# Decode: the model shape of the b4 L8192 forward (80 heads of 64 x 128, one group) with a
+# batch of 128 sequences, so that the carried f32 state (335.5 MB) is larger than L2.
+STEP_B128 = StepShape("ssd_step_b128_nh80_H64_S128_bf16", 128, 80, 64, 128, 1, "bf16")
+
 WORKLOAD_SEED = {
     SSD_SMALL_F32.name: BASE_SEED + 0,
     SCAN_384x65536.name: BASE_SEED + 1,
     SSD_B8_L2048.name: BASE_SEED + 2,
     SSD_B4_L8192.name: BASE_SEED + 3,
     SSD_B1_L131072.name: BASE_SEED + 4,
+    STEP_B128.name: BASE_SEED + 5,
 }
 
 
@@ -135,6 +158,34 @@ def ssd_inputs(shape: SSDShape, seed: int | None = None) -> dict:
         "C": _store(Cm, shape.dtype),
         "D": np.ascontiguousarray(D, np.float32),
         "h0": np.ascontiguousarray(h0, np.float32),
+    }
+
+
+def step_inputs(shape: StepShape, seed: int | None = None) -> dict:
+    """Draw one decode-step workload, with the same distributions as ssd_inputs.
+
+    Returns float32 arrays: x [b,nh,H], dt [b,nh], A [nh], B [b,G,S], C [b,G,S], D [nh] and
+    the carried state [b,nh,H,S] ~ N(0, 0.1^2).
+    """
+    if seed is None:
+        seed = WORKLOAD_SEED.get(shape.name, BASE_SEED)
+    rng = np.random.Generator(np.random.PCG64(seed))
+    b, nh, H, S, G = shape.batch, shape.nheads, shape.headdim, shape.dstate, shape.ngroups
+    x = rng.standard_normal((b, nh, H), dtype=np.float32)
+    Bm = rng.standard_normal((b, G, S), dtype=np.float32) * np.float32(1.0 / math.sqrt(S))
+    Cm = rng.standard_normal((b, G, S), dtype=np.float32) * np.float32(1.0 / math.sqrt(S))
+    dt = _softplus(rng.standard_normal((b, nh)) - shape.dt_shift)
+    A = -np.exp(rng.uniform(0.0, math.log(16.0), nh))
+    D = rng.uniform(0.5, 1.5, nh)
+    state = rng.standard_normal((b, nh, H, S), dtype=np.float32) * np.float32(0.1)
+    return {
+        "x": _store(x, shape.dtype),
+        "dt": _store(dt, shape.dtype),
+        "A": np.ascontiguousarray(A, np.float32),
+        "B": _store(Bm, shape.dtype),
+        "C": _store(Cm, shape.dtype),
+        "D": np.ascontiguousarray(D, np.float32),
+        "state": np.ascontiguousarray(state, np.float32),
     }
 
 

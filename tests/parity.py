@@ -65,3 +65,34 @@ def assert_ssd_close(dtype, y, y_ref, hf, hf_ref, what):
         assert_bf16_close(y, y_ref, f"{what} y", BF16_Y_RMS)
         if hf_ref is not None:
             assert_bf16_close(hf, hf_ref, f"{what} h_final", BF16_H_RMS)
+
+
+def assert_step_close(dtype, y, y_ref, h, h_ref, h_in, c_heads, dx, what):
+    """Per-element rule for the decode step, from its arithmetic (all f32, one token):
+
+    state: each element is one fma of exp(A dt) h and dt x B (dt x B is exact in f32 for bf16
+      inputs); with expf within a few ulp, |dh| <= 2e-6 * scale_h, scale_h = max(|h_ref|, |h_in|).
+    y: a 128-term f32 dot product (a 4-term chain and a 5-level tree) of the new state with c,
+      plus D x: |dy_i| <= 1e-5 * (sum_s |h_ref[i,s] c_s| + scale_h sum_s |c_s| + |D x_i|), and
+      for bf16 output also the rounding to bf16, u = 2^-8: + 2^-8 |y_ref_i| (each term x 1.01).
+    c_heads [b, nh, S] is C per head (its group's row), dx [b, nh, H] is D x.
+    """
+    h_ref = np.asarray(h_ref, np.float64)
+    scale_h = max(float(np.max(np.abs(h_ref))) if h_ref.size else 0.0,
+                  float(np.max(np.abs(h_in))) if h_in is not None and np.size(h_in) else 0.0, 1e-30)
+    dh = np.abs(np.asarray(h, np.float64) - h_ref)
+    if dh.size:
+        i = np.unravel_index(int(np.argmax(dh)), dh.shape)
+        assert dh[i] <= 2e-6 * scale_h, f"{what}: state max|d|={dh[i]:.3e} at {i} > 2e-6*{scale_h:.3e}"
+    ca = np.abs(np.asarray(c_heads, np.float64))
+    tol = 1e-5 * (np.einsum("bnps,bns->bnp", np.abs(h_ref), ca) + scale_h * ca.sum(-1)[..., None]
+                  + np.abs(np.asarray(dx, np.float64)))
+    if dtype == "bf16":
+        tol = tol + 2.0 ** -8 * np.abs(np.asarray(y_ref, np.float64))
+    tol = 1.01 * tol
+    dy = np.abs(np.asarray(y, np.float64) - np.asarray(y_ref, np.float64))
+    bad = dy > tol
+    if bad.any():
+        i = np.unravel_index(int(np.argmax(dy - tol)), dy.shape)
+        raise AssertionError(f"{what}: y |d|={dy[i]:.3e} at {i} (gpu {np.asarray(y)[i]!r}, oracle "
+                             f"{np.asarray(y_ref)[i]!r}) > bound {tol[i]:.3e}; {int(bad.sum())} elements over")

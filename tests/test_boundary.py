@@ -113,3 +113,29 @@ def test_product_package_does_not_import_oracle():
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), fn
             if fn.endswith((".cu", ".cuh", ".h")):
                 assert "ssm_oracle" not in open(os.path.join(root, fn)).read(), fn
+
+
+def _step(lib, **kw):
+    args = dict(x=FAKE, dt=FAKE, A=FAKE, B=FAKE, C=FAKE, D=FAKE, sin=None, sout=FAKE, y=FAKE, batch=2, nh=4, H=64,
+                S=128, G=2, dtype=1)
+    args.update(kw)
+    return lib.ssm_ssd_step(args["x"], args["dt"], args["A"], args["B"], args["C"], args["D"], args["sin"],
+                            args["sout"], args["y"], args["batch"], args["nh"], args["H"], args["S"], args["G"],
+                            args["dtype"], None)
+
+
+def test_step_host_validation(lib):
+    assert _step(lib, H=24) == _lib.SSM_ERR_UNSUPPORTED    # headdim not a multiple of 16
+    assert _step(lib, S=96) == _lib.SSM_ERR_UNSUPPORTED
+    assert _step(lib, nh=3, G=2) == _lib.SSM_ERR_INVALID_ARG
+    assert _step(lib, batch=-1) == _lib.SSM_ERR_INVALID_ARG
+    assert _step(lib, dtype=5) == _lib.SSM_ERR_INVALID_ARG
+    assert _step(lib, sout=None) == _lib.SSM_ERR_INVALID_ARG
+    assert _step(lib, y=None) == _lib.SSM_ERR_INVALID_ARG
+    assert _step(lib, B=FAKE + 2) == _lib.SSM_ERR_ALIGNMENT
+    assert _step(lib, sin=FAKE + 0x100008) == _lib.SSM_ERR_ALIGNMENT
+    state_bytes = 2 * 4 * 64 * 128 * 4
+    # in place is allowed (it would launch, so it is only checked on a GPU); partial overlap is not
+    assert _step(lib, sin=FAKE, sout=FAKE + state_bytes - 16) == _lib.SSM_ERR_INVALID_ARG
+    assert _step(lib, sin=FAKE + 16, sout=FAKE) == _lib.SSM_ERR_INVALID_ARG
+    assert _step(lib, batch=0) == _lib.SSM_OK                # nothing to enqueue
