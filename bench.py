@@ -393,7 +393,8 @@ def run_decode(args, peaks):
                         f"bf16, f32 state in place",
             "launches": args.steps, "ms_per_launch": round(ms, 5), "ms_mean": round(sum(per) / len(per), 5),
             "tokens_per_s": round(STEP.batch / (ms * 1e-3), 1), "alg_bytes": nbytes, "GB/s": round(gbs, 1),
-            "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "timing": "median of per-launch CUDA events"}
+            "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": kernel_traffic("ssd_step"),
+            "timing": "median of per-launch CUDA events"}
 
 
 def run_e2e(args):
