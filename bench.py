@@ -12,7 +12,8 @@ summed over ranks, divided by the max over ranks of the SSD device time); the sc
 per-kernel times, the roofline of the dominant kernel, clocks, the end-to-end leg through the
 public API with host buffers, and the float64 oracle timed on the host cores ride along.  The
 decode step (ssd_step: one token for each of 128 sequences of the same model shape, f32 state
-carried in place) is timed on its own and reported under "decode".
+carried in place) is timed on its own and reported under "decode", and the scan page's
+baseline levels next to the production scan under "scan_baselines".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -279,6 +280,7 @@ def run_ours(args, world, rank, local):
     if ssm.check_device_status(kind="ssd") or ssm.check_device_status(kind="linscan"):
         raise RuntimeError("device status error during the timed region")
     decode = run_decode(args, peaks)
+    scan_baselines = run_scan_baselines(args, peaks)
 
     ssd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
     scan_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
@@ -354,6 +356,7 @@ def run_ours(args, world, rank, local):
                     "alg_bytes": sbytes, "frac": round(scan_gbs / world / peaks["hbm_gbs"], 4)},
         "kernels": kernels,
         "decode": decode,
+        "scan_baselines": scan_baselines,
         "roofline": roof,
         "gpu_launches": sum(kt.launches.values()),
         "clocks": clocks.summary(t_wall0, t_wall1),
@@ -395,6 +398,59 @@ def run_decode(args, peaks):
             "tokens_per_s": round(STEP.batch / (ms * 1e-3), 1), "alg_bytes": nbytes, "GB/s": round(gbs, 1),
             "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": kernel_traffic("ssd_step"),
             "timing": "median of per-launch CUDA events"}
+
+
+# bytes each scan level moves per element (the reference page's traffic model): levels 1, 3,
+# 3b and the production scan read a, b and write h; level 2 also writes and re-reads the local
+# states and decay products
+SCAN_LEVEL_BYTES = {"blelloch": 12, "three_pass": 28, "lookback_serial": 12, "lookback_warp": 12,
+                    "linscan_fwd": 12}
+
+
+def run_scan_baselines(args, peaks):
+    """The reference page's scan levels next to the production scan, on its own study shapes:
+    96 MiB per array as 12288 rows x 2048 and 384 rows x 65536 (L2 flushed before each call,
+    median of per-call CUDA events)."""
+    import torch
+    import selective_state_space_mamba_gb300 as ssm
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    out = {}
+    for rows, length in ((12288, 2048), (SCAN.rows, SCAN.length)):
+        inp = synth.scan_inputs(rows, length, seed=synth.BASE_SEED + 6)
+        a = torch.from_numpy(inp["a"]).cuda()
+        b = torch.from_numpy(inp["b"]).cuda()
+        h = torch.empty_like(a)
+        res = {}
+        for algo in ("blelloch", "three_pass", "lookback_serial", "lookback_warp", "linscan_fwd"):
+            if algo == "blelloch" and length > 2048:
+                continue
+            if algo == "linscan_fwd":
+                def call():
+                    ssm.linscan_fwd(a, b, h=h)
+            else:
+                def call(algo=algo):
+                    ssm.linscan_baseline(a, b, algo, h=h)
+            for _ in range(max(args.warmup, 3)):
+                call()
+            torch.cuda.synchronize()
+            per = []
+            for _ in range(15):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                call()
+                e1.record()
+                torch.cuda.synchronize()
+                per.append(e0.elapsed_time(e1))
+            ms = statistics.median(per)
+            n = rows * length
+            moved = SCAN_LEVEL_BYTES[algo] * n / (ms * 1e-3) / 1e9
+            res[algo] = {"ms": round(ms, 4), "GB/s_3_array_model": round(12 * n / (ms * 1e-3) / 1e9, 1),
+                         "GB/s_moved": round(moved, 1), "hbm_frac_moved": round(moved / peaks["hbm_gbs"], 4)}
+        out[f"{rows}x{length}"] = res
+    if ssm.check_device_status(kind="scan_lookback_serial") or ssm.check_device_status(kind="scan_lookback_warp"):
+        raise RuntimeError("device status error in the baseline scans")
+    return out
 
 
 def run_e2e(args):

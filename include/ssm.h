@@ -194,6 +194,36 @@ SSM_API ssm_status ssm_linscan_fwd_noalloc(const float *a, const float *b, float
                                            ssm_stream_t stream);
 
 /*
+ * Baseline scans of the same recurrence, kept for measurement: the levels of "Selective-scan
+ * CUDA kernels", section "The five kernels" (its traffic-model study compares them), each as
+ * that page describes it, without this library's tuning.  ssm_linscan_fwd is the production
+ * scan (the page's Level 3c, redesigned); use these only to compare against it.
+ *   SSM_SCAN_BLELLOCH          Level 1: one CTA per row, up- and down-sweep in shared memory;
+ *                              len <= 2048.  No workspace.
+ *   SSM_SCAN_THREE_PASS        Level 2: local tile scans, a spine scan per row, then the
+ *                              prefix applied; three launches; len <= 4,194,304 and
+ *                              rows <= 65,535.  Workspace: a float per element plus 8 bytes
+ *                              per 2048-element tile.
+ *   SSM_SCAN_LOOKBACK_SERIAL   Level 3: single-pass decoupled look-back over 256-element tiles,
+ *                              one thread walking the predecessors.
+ *   SSM_SCAN_LOOKBACK_WARP     Level 3b: the same with a warp inspecting 32 predecessors at once.
+ *                              Both look-backs need a zero-filled workspace (left ready for the
+ *                              next call) and report timeouts through ssm_check_device_status.
+ * Arguments as ssm_linscan_fwd.  Errors: SSM_ERR_INVALID_ARG (unknown algorithm, negative
+ * size), SSM_ERR_UNSUPPORTED (a size beyond the algorithm's limit), SSM_ERR_ALIGNMENT,
+ * SSM_ERR_WORKSPACE, SSM_ERR_CUDA.
+ */
+typedef enum {
+    SSM_SCAN_BLELLOCH = 1,
+    SSM_SCAN_THREE_PASS = 2,
+    SSM_SCAN_LOOKBACK_SERIAL = 3,
+    SSM_SCAN_LOOKBACK_WARP = 4
+} ssm_scan_algo;
+SSM_API size_t ssm_linscan_baseline_workspace_bytes(ssm_scan_algo algo, int64_t rows, int64_t len);
+SSM_API ssm_status ssm_linscan_baseline(ssm_scan_algo algo, const float *a, const float *b, float *h, int64_t rows,
+                                        int64_t len, void *workspace, size_t workspace_bytes, ssm_stream_t stream);
+
+/*
  * Synchronizes `stream`, reads the device status word at the start of `workspace` (either
  * kind) and returns SSM_OK or the recorded device error (SSM_ERR_TIMEOUT when a bounded wait
  * exceeded its limit; the outputs of that call are then invalid).  After an error it also
@@ -219,10 +249,11 @@ SSM_API void ssm_debug_set_lookback_fault(int64_t stall_tile, uint64_t spin_limi
  * milliseconds and the number of launches (arrays of length SSM_PROFILE_KERNELS).
  * Kernel ids: 0 linscan_lookback, 1 ssd_chunk_cumsum, 2 ssd_chunk_state,
  * 3 ssd_state_passing, 4 ssd_chunk_scan, 5 ssd_state_fused (chunk states and state passing in
- * one pass; used instead of 2 and 3 where it applies), 6 ssd_step (ssm_ssd_step).  Host-side
- * only; process-global; not thread-safe.
+ * one pass; used instead of 2 and 3 where it applies), 6 ssd_step (ssm_ssd_step),
+ * 7 linscan_baseline (ssm_linscan_baseline, all its launches).  Host-side only;
+ * process-global; not thread-safe.
  */
-#define SSM_PROFILE_KERNELS 7
+#define SSM_PROFILE_KERNELS 8
 SSM_API ssm_status ssm_profile_begin(int max_launches);
 SSM_API ssm_status ssm_profile_end(double *ms_out, int64_t *launches_out);
 

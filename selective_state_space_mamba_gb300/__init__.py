@@ -16,7 +16,7 @@ from __future__ import annotations
 from . import _lib
 from ._lib import SSM_BF16, SSM_F32, SsmError
 
-__all__ = ["ssd_fwd", "ssd_step", "linscan_fwd", "Workspace", "check_device_status", "ssd_fwd_workspace_bytes",
+__all__ = ["ssd_fwd", "ssd_step", "linscan_fwd", "linscan_baseline", "Workspace", "check_device_status", "ssd_fwd_workspace_bytes",
            "linscan_workspace_bytes", "SsmError", "version"]
 
 
@@ -203,6 +203,33 @@ def linscan_fwd(a, b, *, h=None, workspace: Workspace | None = None):
         ws.ensure(need)
     st = lib.ssm_linscan_fwd(_ptr(a), _ptr(b), _ptr(h), rows, L, ws.ptr(), ws.nbytes, _stream_ptr(a.device))
     _lib.check(st, "ssm_linscan_fwd")
+    return h
+
+
+SCAN_BASELINES = {"blelloch": _lib.SSM_SCAN_BLELLOCH, "three_pass": _lib.SSM_SCAN_THREE_PASS,
+                  "lookback_serial": _lib.SSM_SCAN_LOOKBACK_SERIAL, "lookback_warp": _lib.SSM_SCAN_LOOKBACK_WARP}
+
+
+def linscan_baseline(a, b, algo: str, *, h=None, workspace: Workspace | None = None):
+    """The scalar scan by one of the reference page's baseline levels (see include/ssm.h,
+    ssm_linscan_baseline): "blelloch", "three_pass", "lookback_serial" or "lookback_warp"."""
+    torch = _torch()
+    lib = _lib.load()
+    _require(algo in SCAN_BASELINES, f"algo must be one of {sorted(SCAN_BASELINES)}")
+    code = SCAN_BASELINES[algo]
+    _require(a.shape == b.shape and a.dim() == 2, "a, b must be [rows, L] and equal")
+    _require(a.dtype == torch.float32 and b.dtype == torch.float32, "a, b must be float32")
+    _require(a.is_cuda and b.is_cuda and a.is_contiguous() and b.is_contiguous(), "contiguous CUDA tensors")
+    rows, L = a.shape
+    if h is None:
+        h = torch.empty_like(a)
+    need = lib.ssm_linscan_baseline_workspace_bytes(code, rows, L)
+    ws = workspace if workspace is not None else _workspace("scan_" + algo, a.device, max(need, 1))
+    if workspace is not None:
+        ws.ensure(need)
+    st = lib.ssm_linscan_baseline(code, _ptr(a), _ptr(b), _ptr(h), rows, L, ws.ptr(), ws.nbytes,
+                                  _stream_ptr(a.device))
+    _lib.check(st, "ssm_linscan_baseline")
     return h
 
 

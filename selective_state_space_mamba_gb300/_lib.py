@@ -14,14 +14,15 @@ from . import _build
 SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_ALIGNMENT, SSM_ERR_WORKSPACE, SSM_ERR_CUDA, \
     SSM_ERR_TIMEOUT = range(7)
 SSM_F32, SSM_BF16 = 0, 1
+SSM_SCAN_BLELLOCH, SSM_SCAN_THREE_PASS, SSM_SCAN_LOOKBACK_SERIAL, SSM_SCAN_LOOKBACK_WARP = 1, 2, 3, 4
 
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ("ssm_status_string", "ssm_version", "ssm_ssd_fwd_workspace_bytes", "ssm_ssd_fwd",
            "ssm_linscan_workspace_bytes", "ssm_linscan_fwd", "ssm_check_device_status",
            "ssm_debug_set_lookback_fault", "ssm_profile_begin", "ssm_profile_end", "ssm_linscan_fwd_noalloc",
-           "ssm_ssd_step")
+           "ssm_ssd_step", "ssm_linscan_baseline_workspace_bytes", "ssm_linscan_baseline")
 PROFILE_KERNELS = ("linscan_lookback", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
-                   "ssd_state_fused", "ssd_step")
+                   "ssd_state_fused", "ssd_step", "linscan_baseline")
 
 _lib = None
 _lock = threading.Lock()
@@ -45,6 +46,10 @@ def _declare(lib):
     lib.ssm_ssd_fwd.restype = i32
     lib.ssm_ssd_step.argtypes = [vp] * 9 + [i64, i32, i32, i32, i32, i32, vp]
     lib.ssm_ssd_step.restype = i32
+    lib.ssm_linscan_baseline_workspace_bytes.argtypes = [i32, i64, i64]
+    lib.ssm_linscan_baseline_workspace_bytes.restype = sz
+    lib.ssm_linscan_baseline.argtypes = [i32, vp, vp, vp, i64, i64, vp, sz, vp]
+    lib.ssm_linscan_baseline.restype = i32
     lib.ssm_linscan_workspace_bytes.argtypes = [i64, i64]
     lib.ssm_linscan_workspace_bytes.restype = sz
     lib.ssm_linscan_fwd.argtypes = [vp, vp, vp, i64, i64, vp, sz, vp]

@@ -354,6 +354,34 @@ ssm_status ssm_linscan_fwd(const float* a, const float* b, float* h, int64_t row
   return SSM_OK;
 }
 
+size_t ssm_linscan_baseline_workspace_bytes(ssm_scan_algo algo, int64_t rows, int64_t len) {
+  if (rows < 0 || len < 0 || linscan_baseline_check(algo, rows, len) == SSM_ERR_INVALID_ARG) return 0;
+  return linscan_baseline_workspace(algo, rows, len);
+}
+
+ssm_status ssm_linscan_baseline(ssm_scan_algo algo, const float* a, const float* b, float* h, int64_t rows,
+                                int64_t len, void* workspace, size_t workspace_bytes, ssm_stream_t stream) {
+  if (rows < 0 || len < 0) return SSM_ERR_INVALID_ARG;
+  const ssm_status st = linscan_baseline_check(algo, rows, len);
+  if (st == SSM_ERR_INVALID_ARG) return st;
+  if (rows == 0 || len == 0) return SSM_OK;
+  if (st != SSM_OK) return st;
+  if (!a || !b || !h) return SSM_ERR_INVALID_ARG;
+  if (!aligned(a, 16) || !aligned(b, 16) || !aligned(h, 16)) return SSM_ERR_ALIGNMENT;
+  if (rows * len / len != rows) return SSM_ERR_INVALID_ARG;
+  const size_t need = linscan_baseline_workspace(algo, rows, len);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return SSM_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return SSM_ERR_ALIGNMENT;
+  }
+  const LookbackCtl ctl = next_lookback_ctl();
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (timed_launch(7, s, [&] { return launch_linscan_baseline(algo, a, b, h, rows, len, workspace, ctl, s); }) !=
+      cudaSuccess)
+    return SSM_ERR_CUDA;
+  return SSM_OK;
+}
+
 ssm_status ssm_check_device_status(void* workspace, ssm_stream_t stream) {
   if (!workspace) return SSM_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -342,6 +342,10 @@ cudaError_t launch_ssd_state_passing(const float* h0, float* h_final, const SsdD
                                      const SsdWorkspace& ws, const LookbackCtl& ctl, cudaStream_t s);
 cudaError_t launch_ssd_chunk_scan(const void* x, const void* B, const void* C, const float* D,
                                   void* y, const SsdDims& d, const SsdWorkspace& ws, cudaStream_t s);
+size_t linscan_baseline_workspace(ssm_scan_algo algo, int64_t rows, int64_t len);
+ssm_status linscan_baseline_check(ssm_scan_algo algo, int64_t rows, int64_t len);
+cudaError_t launch_linscan_baseline(ssm_scan_algo algo, const float* a, const float* b, float* h, int64_t rows,
+                                    int64_t len, void* workspace, const LookbackCtl& ctl, cudaStream_t s);
 cudaError_t launch_ssd_step(const void* x, const void* dt, const float* A, const void* B, const void* C,
                             const float* D, const float* state_in, float* state_out, void* y, int64_t batch,
                             int nheads, int headdim, int dstate, int ngroups, ssm_dtype dtype, cudaStream_t s);

@@ -139,3 +139,20 @@ def test_step_host_validation(lib):
     assert _step(lib, sin=FAKE, sout=FAKE + state_bytes - 16) == _lib.SSM_ERR_INVALID_ARG
     assert _step(lib, sin=FAKE + 16, sout=FAKE) == _lib.SSM_ERR_INVALID_ARG
     assert _step(lib, batch=0) == _lib.SSM_OK                # nothing to enqueue
+
+
+def test_scan_baseline_host_validation(lib):
+    f = lib.ssm_linscan_baseline
+    ws = lib.ssm_linscan_baseline_workspace_bytes
+    assert f(9, FAKE, FAKE, FAKE, 3, 10, FAKE, 1 << 30, None) == _lib.SSM_ERR_INVALID_ARG   # unknown algorithm
+    assert f(_lib.SSM_SCAN_BLELLOCH, FAKE, FAKE, FAKE, 3, 2049, None, 0, None) == _lib.SSM_ERR_UNSUPPORTED
+    assert f(_lib.SSM_SCAN_THREE_PASS, FAKE, FAKE, FAKE, 1, 4194305, FAKE, 1 << 40, None) == _lib.SSM_ERR_UNSUPPORTED
+    assert f(_lib.SSM_SCAN_THREE_PASS, FAKE, FAKE, FAKE, 65536, 16, FAKE, 1 << 40, None) == _lib.SSM_ERR_UNSUPPORTED
+    assert f(_lib.SSM_SCAN_LOOKBACK_WARP, FAKE, FAKE, FAKE, -1, 10, FAKE, 1 << 30, None) == _lib.SSM_ERR_INVALID_ARG
+    assert f(_lib.SSM_SCAN_LOOKBACK_WARP, FAKE, FAKE, FAKE, 0, 10, None, 0, None) == _lib.SSM_OK
+    assert f(_lib.SSM_SCAN_LOOKBACK_SERIAL, FAKE + 4, FAKE, FAKE, 3, 10, FAKE, 1 << 30, None) == _lib.SSM_ERR_ALIGNMENT
+    assert f(_lib.SSM_SCAN_LOOKBACK_SERIAL, FAKE, FAKE, FAKE, 3, 10, FAKE, 16, None) == _lib.SSM_ERR_WORKSPACE
+    assert ws(_lib.SSM_SCAN_BLELLOCH, 3, 100) == 0
+    # three-pass: one float per element plus the tile aggregates; look-back: header + 16 B per 256 elements
+    assert ws(_lib.SSM_SCAN_THREE_PASS, 2, 5000) >= 4 * 10000 + 8 * 2 * 3
+    assert ws(_lib.SSM_SCAN_LOOKBACK_WARP, 4, 1000) >= 256 + 16 * 16
