@@ -200,13 +200,20 @@ def barrier(world):
 
 
 def max_over_ranks(world, v):
+    """The largest v over all ranks (NCCL reduces device tensors, gloo host tensors)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def weak_scaling_value(world, units_per_rank, ms_per_rank_max):
+    """Whole-job throughput: the units every rank processed, over the slowest rank's time."""
+    return world * units_per_rank / (ms_per_rank_max * 1e-3)
 
 
 def device_inputs(torch, inp, dtype):
@@ -289,7 +296,7 @@ def run_ours(args, world, rank, local):
     scan_ms_max = max_over_ranks(world, scan_ms)
     step_ms_max = max_over_ranks(world, step_ms)
     tokens = SSD.batch * SSD.seqlen
-    value = world * tokens / (ssd_ms_max * 1e-3)
+    value = weak_scaling_value(world, tokens, ssd_ms_max)
     sbytes = scan_bytes(SCAN.rows, SCAN.length)
     scan_gbs = world * sbytes / (scan_ms_max * 1e-3) / 1e9
 
