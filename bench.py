@@ -243,6 +243,10 @@ def run_ours(args, world, rank, local):
     def ssd_call():
         ssm.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], chunk=SSD.chunk, y=y, h_final=hf)
 
+    # per-shape plan, chosen by measurement once before anything is timed (as a user would)
+    plan, plan_ms = ssm.tune_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], chunk=SSD.chunk,
+                                     reps=5, y=y, h_final=hf)
+
     def scan_call():
         ssm.linscan_fwd(a, bsc, h=h)
 
@@ -355,6 +359,9 @@ def run_ours(args, world, rank, local):
             "per_kernel": "a second timed pass of the same steps with per-launch events",
             "l2": "inputs larger than L2, and L2 flushed by a 256 MiB write before each timed step",
             "parallelism": f"replicas x{world} (independent problems, no collective)",
+            "plan": {"id": plan, "fused_state_path": (plan & 3) - 1, "sequential_state_passing": ((plan >> 2) & 3) - 1,
+                     "scan_heads_per_cta": plan >> 4, "tuning_median_ms": round(plan_ms, 4),
+                     "how": "ssm_ssd_fwd_tune before the warm-up: every candidate plan timed, the fastest kept"},
         },
         "ssd": {"tokens_per_s": round(value, 1), "ms": round(ssd_ms_max, 4), "model_B_bytes": model_b,
                 "roofline_ms": round(ssd_roof_ms, 4), "roofline_frac": round(ssd_roof_ms / ssd_ms_max, 4),

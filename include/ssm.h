@@ -122,6 +122,42 @@ SSM_API ssm_status ssm_ssd_fwd(const void *x, const void *dt, const float *A, co
                        void *workspace, size_t workspace_bytes, ssm_stream_t stream);
 
 /*
+ * Per-shape plans for ssm_ssd_fwd.  "Accelerating Mamba-2 with High-Performance Forward Pass
+ * Kernels in NVIDIA CUDA Tile", section "Mamba-2 performance optimization", gets its speed
+ * across shapes from an autotuner that searches block sizes per shape; here the choices are
+ * discrete plans, picked by measurement:
+ *   - the state path: chunk states and the recurrence over chunks in one kernel (bf16, headdim
+ *     64, dstate 128, an even number of heads per group), or the two kernels chunk-state then
+ *     state-passing, the latter sequential over chunks or a decoupled look-back;
+ *   - the chunk scan's run of heads per CTA (the tensor-core path).
+ * Without a plan, ssm_ssd_fwd picks by fixed rules of thumb.  A plan id packs
+ * (fused + 1) | (sequential + 1) << 2 | heads_per_cta << 4, where fused and sequential are 1
+ * (yes), 0 (no) or -1 (rule of thumb) and heads_per_cta 0 means the rule of thumb.
+ *
+ * ssm_ssd_fwd_tune takes exactly ssm_ssd_fwd's arguments and runs every candidate plan for
+ * these sizes on the caller's buffers (y and h_final are overwritten; each candidate computes
+ * the same result up to rounding): one warm-up and `reps` timed runs each (CUDA events on
+ * `stream`), synchronizing the stream.  The plan with the smallest median time is stored for
+ * the current device and these sizes in a process-wide table that later ssm_ssd_fwd calls
+ * with the same sizes use; *plan_out and *ms_out (either may be NULL) receive it and its time.
+ * A device error recorded by a candidate (SSM_ERR_TIMEOUT) is returned and no plan is stored.
+ * ssm_ssd_fwd_set_plan stores a given plan (-1 removes the entry), ssm_ssd_fwd_get_plan reads
+ * the stored one (-1: none), ssm_ssd_fwd_clear_plans empties the table.  The table is shared
+ * by all host threads (guarded by a lock).
+ * Errors: as ssm_ssd_fwd, plus SSM_ERR_INVALID_ARG for reps < 1 or an invalid plan id.
+ */
+SSM_API ssm_status ssm_ssd_fwd_tune(const void *x, const void *dt, const float *A, const void *B, const void *C,
+                                    const float *D, const float *h0, void *y, float *h_final, int64_t batch,
+                                    int64_t seqlen, int nheads, int headdim, int dstate, int ngroups, int chunk,
+                                    ssm_dtype dtype, void *workspace, size_t workspace_bytes, ssm_stream_t stream,
+                                    int reps, int *plan_out, float *ms_out);
+SSM_API ssm_status ssm_ssd_fwd_set_plan(int64_t batch, int64_t seqlen, int nheads, int headdim, int dstate,
+                                        int ngroups, int chunk, ssm_dtype dtype, int plan);
+SSM_API ssm_status ssm_ssd_fwd_get_plan(int64_t batch, int64_t seqlen, int nheads, int headdim, int dstate,
+                                        int ngroups, int chunk, ssm_dtype dtype, int *plan);
+SSM_API void ssm_ssd_fwd_clear_plans(void);
+
+/*
  * Mamba-2 decode step: ONE new token per sequence, with the state carried between calls.
  * Definition: the recurrence above applied to a single token ("Accelerating Mamba-2 with
  * High-Performance Forward Pass Kernels in NVIDIA CUDA Tile", section "Mamba-2

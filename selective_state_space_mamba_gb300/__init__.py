@@ -16,7 +16,8 @@ from __future__ import annotations
 from . import _lib
 from ._lib import SSM_BF16, SSM_F32, SsmError
 
-__all__ = ["ssd_fwd", "ssd_step", "linscan_fwd", "linscan_baseline", "Workspace", "check_device_status", "ssd_fwd_workspace_bytes",
+__all__ = ["ssd_fwd", "ssd_step", "linscan_fwd", "linscan_baseline", "tune_ssd_fwd", "set_ssd_fwd_plan",
+           "get_ssd_fwd_plan", "clear_ssd_fwd_plans", "plan_id", "Workspace", "check_device_status", "ssd_fwd_workspace_bytes",
            "linscan_workspace_bytes", "SsmError", "version"]
 
 
@@ -148,6 +149,60 @@ def ssd_fwd(x, dt, A, B, C, D, h0=None, chunk: int = 256, *, y=None, h_final=Non
                          _ptr(h_final), b, L, nh, H, S, G, chunk, code, ws.ptr(), ws.nbytes, _stream_ptr(x.device))
     _lib.check(st, "ssm_ssd_fwd")
     return y, h_final
+
+
+def _ssd_sizes(x, B, chunk):
+    b, L, nh, H = x.shape
+    G, S = B.shape[2], B.shape[3]
+    return b, L, nh, H, S, G, chunk, _dtype_code(x)
+
+
+def plan_id(fused: int = -1, sequential: int = -1, heads_per_cta: int = 0) -> int:
+    """Pack a plan for ssd_fwd (see include/ssm.h): each flag 1, 0 or -1 (rule of thumb)."""
+    return (fused + 1) | ((sequential + 1) << 2) | (heads_per_cta << 4)
+
+
+def tune_ssd_fwd(x, dt, A, B, C, D, h0=None, chunk: int = 256, reps: int = 5, *, y=None, h_final=None,
+                 workspace: Workspace | None = None):
+    """Time every plan of ssd_fwd for these sizes on these tensors and keep the fastest for later
+    ssd_fwd calls of the same sizes (ssm_ssd_fwd_tune).  Returns (plan id, median ms)."""
+    import ctypes
+    torch = _torch()
+    lib = _lib.load()
+    b, L, nh, H, S, G, chunk, code = _ssd_sizes(x, B, chunk)
+    if y is None:
+        y = torch.empty_like(x)
+    if h_final is None:
+        h_final = torch.empty((b, nh, H, S), dtype=torch.float32, device=x.device)
+    need = lib.ssm_ssd_fwd_workspace_bytes(b, L, nh, H, S, G, chunk, code)
+    ws = workspace if workspace is not None else _workspace("ssd", x.device, max(need, 1))
+    if workspace is not None:
+        ws.ensure(need)
+    plan = ctypes.c_int(-1)
+    ms = ctypes.c_float(0.0)
+    st = lib.ssm_ssd_fwd_tune(_ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(h0), _ptr(y),
+                              _ptr(h_final), b, L, nh, H, S, G, chunk, code, ws.ptr(), ws.nbytes,
+                              _stream_ptr(x.device), int(reps), ctypes.byref(plan), ctypes.byref(ms))
+    _lib.check(st, "ssm_ssd_fwd_tune")
+    return plan.value, ms.value
+
+
+def set_ssd_fwd_plan(x, B, chunk: int, plan: int) -> None:
+    """Store `plan` (-1: remove) for ssd_fwd calls with the sizes of x and B (ssm_ssd_fwd_set_plan)."""
+    _lib.check(_lib.load().ssm_ssd_fwd_set_plan(*_ssd_sizes(x, B, chunk), int(plan)), "ssm_ssd_fwd_set_plan")
+
+
+def get_ssd_fwd_plan(x, B, chunk: int) -> int:
+    """The stored plan for these sizes, or -1 (ssm_ssd_fwd_get_plan)."""
+    import ctypes
+    plan = ctypes.c_int(-1)
+    _lib.check(_lib.load().ssm_ssd_fwd_get_plan(*_ssd_sizes(x, B, chunk), ctypes.byref(plan)),
+               "ssm_ssd_fwd_get_plan")
+    return plan.value
+
+
+def clear_ssd_fwd_plans() -> None:
+    _lib.load().ssm_ssd_fwd_clear_plans()
 
 
 def ssd_step(x, dt, A, B, C, D, state=None, *, y=None, state_out=None, inplace: bool = False):

@@ -20,7 +20,8 @@ SSM_SCAN_BLELLOCH, SSM_SCAN_THREE_PASS, SSM_SCAN_LOOKBACK_SERIAL, SSM_SCAN_LOOKB
 EXPORTS = ("ssm_status_string", "ssm_version", "ssm_ssd_fwd_workspace_bytes", "ssm_ssd_fwd",
            "ssm_linscan_workspace_bytes", "ssm_linscan_fwd", "ssm_check_device_status",
            "ssm_debug_set_lookback_fault", "ssm_profile_begin", "ssm_profile_end", "ssm_linscan_fwd_noalloc",
-           "ssm_ssd_step", "ssm_linscan_baseline_workspace_bytes", "ssm_linscan_baseline")
+           "ssm_ssd_step", "ssm_linscan_baseline_workspace_bytes", "ssm_linscan_baseline", "ssm_ssd_fwd_tune",
+           "ssm_ssd_fwd_set_plan", "ssm_ssd_fwd_get_plan", "ssm_ssd_fwd_clear_plans")
 PROFILE_KERNELS = ("linscan_lookback", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
                    "ssd_state_fused", "ssd_step", "linscan_baseline")
 
@@ -44,6 +45,14 @@ def _declare(lib):
     lib.ssm_ssd_fwd_workspace_bytes.restype = sz
     lib.ssm_ssd_fwd.argtypes = [vp] * 9 + [i64, i64, i32, i32, i32, i32, i32, i32, vp, sz, vp]
     lib.ssm_ssd_fwd.restype = i32
+    lib.ssm_ssd_fwd_tune.argtypes = [vp] * 9 + [i64, i64, i32, i32, i32, i32, i32, i32, vp, sz, vp, i32, vp, vp]
+    lib.ssm_ssd_fwd_tune.restype = i32
+    lib.ssm_ssd_fwd_set_plan.argtypes = [i64, i64, i32, i32, i32, i32, i32, i32, i32]
+    lib.ssm_ssd_fwd_set_plan.restype = i32
+    lib.ssm_ssd_fwd_get_plan.argtypes = [i64, i64, i32, i32, i32, i32, i32, i32, vp]
+    lib.ssm_ssd_fwd_get_plan.restype = i32
+    lib.ssm_ssd_fwd_clear_plans.argtypes = []
+    lib.ssm_ssd_fwd_clear_plans.restype = None
     lib.ssm_ssd_step.argtypes = [vp] * 9 + [i64, i32, i32, i32, i32, i32, vp]
     lib.ssm_ssd_step.restype = i32
     lib.ssm_linscan_baseline_workspace_bytes.argtypes = [i32, i64, i64]

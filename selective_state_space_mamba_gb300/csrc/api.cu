@@ -1,8 +1,11 @@
 // Host side of the C ABI declared in include/ssm.h: argument validation, workspace layout,
 // and the launch sequence of each operation on the caller's stream.
+#include <algorithm>
 #include <atomic>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <vector>
 
 #include "ssm_internal.cuh"
@@ -18,6 +21,7 @@ cudaError_t launch_ssd_chunk_state_tc(const void* x, const void* B, const SsdDim
                                       const LookbackCtl& ctl, cudaStream_t s);
 bool ssd_scan_tc_supported(const SsdDims& d);
 bool ssd_state_fused_supported(const SsdDims& d);
+bool ssd_state_fused_possible(const SsdDims& d);
 cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float* h0, float* h_final,
                                       const SsdDims& d, const SsdWorkspace& ws, const LookbackCtl& ctl,
                                       cudaStream_t s);
@@ -103,7 +107,60 @@ SsdDims make_dims(int64_t batch, int64_t seqlen, int nheads, int headdim, int ds
   d.nchunks = (seqlen + chunk - 1) / chunk;
   d.lpad = d.nchunks * chunk;
   d.dtype = dtype;
+  d.plan_fused = -1;
+  d.plan_seq = -1;
+  d.plan_scan_heads = 0;
   return d;
+}
+
+// ---- per-shape plans (ssm_ssd_fwd_tune / ssm_ssd_fwd_set_plan) ----
+// A plan id packs (fused + 1) | (seq + 1) << 2 | scan_heads << 4, with -1 meaning "the heuristic".
+struct PlanKey {
+  int dev;
+  int64_t batch, seqlen;
+  int nheads, headdim, dstate, ngroups, chunk, dtype;
+  bool operator<(const PlanKey& o) const {
+    return std::tie(dev, batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype) <
+           std::tie(o.dev, o.batch, o.seqlen, o.nheads, o.headdim, o.dstate, o.ngroups, o.chunk, o.dtype);
+  }
+};
+std::mutex g_plan_mu;
+std::map<PlanKey, int> g_plans;
+
+bool plan_key(const SsdDims& d, PlanKey* k) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  *k = PlanKey{dev, d.batch, d.seqlen, d.nheads, d.headdim, d.dstate, d.ngroups, d.chunk, (int)d.dtype};
+  return true;
+}
+int plan_id(int fused, int seq, int heads) { return (fused + 1) | ((seq + 1) << 2) | (heads << 4); }
+bool plan_valid(int id) { return id >= 0 && (id & 3) != 3 && ((id >> 2) & 3) != 3 && (id >> 4) <= 65535; }
+void apply_plan(SsdDims& d, int id) {
+  d.plan_fused = (id & 3) - 1;
+  d.plan_seq = ((id >> 2) & 3) - 1;
+  d.plan_scan_heads = id >> 4;
+}
+void apply_cached_plan(SsdDims& d) {
+  PlanKey k;
+  if (!plan_key(d, &k)) return;
+  std::lock_guard<std::mutex> lk(g_plan_mu);
+  const auto it = g_plans.find(k);
+  if (it != g_plans.end()) apply_plan(d, it->second);
+}
+
+// Pointer, alignment and workspace checks of an SSD forward with tokens to process.
+ssm_status check_ssd_buffers(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                             const float* D, const float* h0, const void* y, const float* h_final, const SsdDims& d,
+                             const void* workspace, size_t workspace_bytes) {
+  if (!x || !dt || !A || !B || !C || !D || !y) return SSM_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, dt, A, B, C, D, y};
+  for (const void* p : ptrs)
+    if (!aligned(p, 16)) return SSM_ERR_ALIGNMENT;
+  if ((h0 && !aligned(h0, 16)) || (h_final && !aligned(h_final, 16))) return SSM_ERR_ALIGNMENT;
+  const SsdWorkspace need = ssd_workspace_layout(d, nullptr);
+  if (!workspace || workspace_bytes < need.total_bytes) return SSM_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return SSM_ERR_ALIGNMENT;
+  return SSM_OK;
 }
 
 }  // namespace
@@ -214,6 +271,45 @@ cudaError_t encode_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, co
 
 }  // namespace ssm
 
+namespace ssm {
+namespace {
+
+// The kernel sequence of one SSD forward on validated sizes, a sized workspace and d's plan.
+ssm_status run_ssd(const void* x, const void* dt, const float* A, const void* B, const void* C, const float* D,
+                   const float* h0, void* y, float* h_final, const SsdDims& d, void* workspace, cudaStream_t s) {
+  const SsdWorkspace ws = ssd_workspace_layout(d, workspace);
+  const LookbackCtl ctl = next_lookback_ctl();
+
+  const bool state_tc = ssd_tc_supported(d);
+  const bool scan_tc = ssd_scan_tc_supported(d);
+  const bool fused = state_tc && ssd_state_fused_supported(d);
+  if (timed_launch(1, s, [&] { return launch_ssd_chunk_cumsum(dt, A, d, ws, s); }) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  if (fused) {
+    // chunk states and the recurrence over chunks in one pass: S_c never goes to memory
+    if (timed_launch(5, s, [&] { return launch_ssd_state_fused_tc(x, B, h0, h_final, d, ws, ctl, s); }) !=
+        cudaSuccess)
+      return SSM_ERR_CUDA;
+  } else {
+    if (timed_launch(2, s, [&] {
+          return state_tc ? launch_ssd_chunk_state_tc(x, B, d, ws, ctl, s)
+                          : launch_ssd_chunk_state_simt(x, B, d, ws, s);
+        }) != cudaSuccess)
+      return SSM_ERR_CUDA;
+    if (timed_launch(3, s, [&] { return launch_ssd_state_passing(h0, h_final, d, ws, ctl, s); }) != cudaSuccess)
+      return SSM_ERR_CUDA;
+  }
+  if (timed_launch(4, s, [&] {
+        return scan_tc ? launch_ssd_chunk_scan_tc(x, B, C, D, y, d, ws, ctl, s)
+                  : launch_ssd_chunk_scan_simt(x, B, C, D, y, d, ws, s);
+      }) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  return SSM_OK;
+}
+
+}  // namespace
+}  // namespace ssm
+
 using namespace ssm;
 
 extern "C" {
@@ -247,7 +343,7 @@ ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void
   ssm_status st = check_ssd_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype);
   if (st != SSM_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const SsdDims d = make_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype);
+  SsdDims d = make_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype);
   const size_t state_bytes = sizeof(float) * (size_t)batch * nheads * headdim * dstate;
   if (batch == 0 || seqlen == 0) {
     // no tokens: y is empty and the final state is the initial state
@@ -259,42 +355,128 @@ ssm_status ssm_ssd_fwd(const void* x, const void* dt, const float* A, const void
     }
     return SSM_OK;
   }
-  if (!x || !dt || !A || !B || !C || !D || !y) return SSM_ERR_INVALID_ARG;
-  const void* ptrs[] = {x, dt, A, B, C, D, y};
-  for (const void* p : ptrs)
-    if (!aligned(p, 16)) return SSM_ERR_ALIGNMENT;
-  if ((h0 && !aligned(h0, 16)) || (h_final && !aligned(h_final, 16))) return SSM_ERR_ALIGNMENT;
-  const SsdWorkspace need = ssd_workspace_layout(d, nullptr);
-  if (!workspace || workspace_bytes < need.total_bytes) return SSM_ERR_WORKSPACE;
-  if (!aligned(workspace, 256)) return SSM_ERR_ALIGNMENT;
-  const SsdWorkspace ws = ssd_workspace_layout(d, workspace);
-  const LookbackCtl ctl = next_lookback_ctl();
+  st = check_ssd_buffers(x, dt, A, B, C, D, h0, y, h_final, d, workspace, workspace_bytes);
+  if (st != SSM_OK) return st;
+  apply_cached_plan(d);
+  return run_ssd(x, dt, A, B, C, D, h0, y, h_final, d, workspace, s);
+}
 
-  const bool state_tc = ssd_tc_supported(d);
-  const bool scan_tc = ssd_scan_tc_supported(d);
-  const bool fused = state_tc && ssd_state_fused_supported(d);
-  if (timed_launch(1, s, [&] { return launch_ssd_chunk_cumsum(dt, A, d, ws, s); }) != cudaSuccess)
-    return SSM_ERR_CUDA;
-  if (fused) {
-    // chunk states and the recurrence over chunks in one pass: S_c never goes to memory
-    if (timed_launch(5, s, [&] { return launch_ssd_state_fused_tc(x, B, h0, h_final, d, ws, ctl, s); }) !=
-        cudaSuccess)
-      return SSM_ERR_CUDA;
-  } else {
-    if (timed_launch(2, s, [&] {
-          return state_tc ? launch_ssd_chunk_state_tc(x, B, d, ws, ctl, s)
-                          : launch_ssd_chunk_state_simt(x, B, d, ws, s);
-        }) != cudaSuccess)
-      return SSM_ERR_CUDA;
-    if (timed_launch(3, s, [&] { return launch_ssd_state_passing(h0, h_final, d, ws, ctl, s); }) != cudaSuccess)
-      return SSM_ERR_CUDA;
+ssm_status ssm_ssd_fwd_tune(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                            const float* D, const float* h0, void* y, float* h_final, int64_t batch, int64_t seqlen,
+                            int nheads, int headdim, int dstate, int ngroups, int chunk, ssm_dtype dtype,
+                            void* workspace, size_t workspace_bytes, ssm_stream_t stream, int reps, int* plan_out,
+                            float* ms_out) {
+  ssm_status st = check_ssd_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype);
+  if (st != SSM_OK) return st;
+  if (reps < 1) return SSM_ERR_INVALID_ARG;
+  if (plan_out) *plan_out = -1;
+  if (ms_out) *ms_out = 0.f;
+  if (batch == 0 || seqlen == 0) return SSM_OK;  // nothing to choose
+  SsdDims d = make_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype);
+  st = check_ssd_buffers(x, dt, A, B, C, D, h0, y, h_final, d, workspace, workspace_bytes);
+  if (st != SSM_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // candidates: the fused state path where it is possible, else the two state kernels with
+  // either state-passing kernel; times the chunk scan's runs of heads per CTA
+  std::vector<int> cands;
+  std::vector<int> heads = {0};
+  if (ssd_scan_tc_supported(d)) {
+    const int hpg = nheads / ngroups;
+    for (int parts : {1, 2, 3, 4, 5, 6, 8}) heads.push_back((hpg + parts - 1) / parts);
+    std::sort(heads.begin() + 1, heads.end());
+    heads.erase(std::unique(heads.begin() + 1, heads.end()), heads.end());
   }
-  if (timed_launch(4, s, [&] {
-        return scan_tc ? launch_ssd_chunk_scan_tc(x, B, C, D, y, d, ws, ctl, s)
-                  : launch_ssd_chunk_scan_simt(x, B, C, D, y, d, ws, s);
-      }) != cudaSuccess)
+  for (int hd : heads) {
+    if (ssd_tc_supported(d) && ssd_state_fused_possible(d)) cands.push_back(plan_id(1, -1, hd));
+    cands.push_back(plan_id(0, 1, hd));
+    cands.push_back(plan_id(0, 0, hd));
+  }
+  cudaEvent_t e0, e1;
+  if (cudaEventCreate(&e0) != cudaSuccess) return SSM_ERR_CUDA;
+  if (cudaEventCreate(&e1) != cudaSuccess) {
+    cudaEventDestroy(e0);
     return SSM_ERR_CUDA;
+  }
+  int best = -1;
+  float best_ms = 0.f;
+  st = SSM_OK;
+  for (int id : cands) {
+    SsdDims dc = d;
+    apply_plan(dc, id);
+    std::vector<float> t;
+    for (int r = 0; r <= reps && st == SSM_OK; ++r) {  // one warm-up, then `reps` timed runs
+      if (cudaEventRecord(e0, s) != cudaSuccess) st = SSM_ERR_CUDA;
+      if (st == SSM_OK) st = run_ssd(x, dt, A, B, C, D, h0, y, h_final, dc, workspace, s);
+      if (st == SSM_OK && cudaEventRecord(e1, s) != cudaSuccess) st = SSM_ERR_CUDA;
+      float ms = 0.f;
+      if (st == SSM_OK && (cudaEventSynchronize(e1) != cudaSuccess || cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess))
+        st = SSM_ERR_CUDA;
+      if (r > 0) t.push_back(ms);
+    }
+    if (st != SSM_OK) break;
+    // a device-side timeout in a candidate disqualifies nothing silently: report it
+    unsigned long long word = 0;
+    if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+      st = SSM_ERR_CUDA;
+      break;
+    }
+    if (word != 0) {
+      st = static_cast<ssm_status>(word & 0xffffffffu);
+      break;
+    }
+    std::sort(t.begin(), t.end());
+    const float med = t[t.size() / 2];
+    if (best < 0 || med < best_ms) {
+      best = id;
+      best_ms = med;
+    }
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (st != SSM_OK) return st;
+  PlanKey k;
+  if (!plan_key(d, &k)) return SSM_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    g_plans[k] = best;
+  }
+  if (plan_out) *plan_out = best;
+  if (ms_out) *ms_out = best_ms;
   return SSM_OK;
+}
+
+ssm_status ssm_ssd_fwd_set_plan(int64_t batch, int64_t seqlen, int nheads, int headdim, int dstate, int ngroups,
+                                int chunk, ssm_dtype dtype, int plan) {
+  const ssm_status st = check_ssd_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype);
+  if (st != SSM_OK) return st;
+  if (plan != -1 && !plan_valid(plan)) return SSM_ERR_INVALID_ARG;
+  PlanKey k;
+  if (!plan_key(make_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype), &k)) return SSM_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_plan_mu);
+  if (plan == -1)
+    g_plans.erase(k);
+  else
+    g_plans[k] = plan;
+  return SSM_OK;
+}
+
+ssm_status ssm_ssd_fwd_get_plan(int64_t batch, int64_t seqlen, int nheads, int headdim, int dstate, int ngroups,
+                                int chunk, ssm_dtype dtype, int* plan) {
+  const ssm_status st = check_ssd_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype);
+  if (st != SSM_OK) return st;
+  if (!plan) return SSM_ERR_INVALID_ARG;
+  *plan = -1;
+  PlanKey k;
+  if (!plan_key(make_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype), &k)) return SSM_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_plan_mu);
+  const auto it = g_plans.find(k);
+  if (it != g_plans.end()) *plan = it->second;
+  return SSM_OK;
+}
+
+void ssm_ssd_fwd_clear_plans(void) {
+  std::lock_guard<std::mutex> lk(g_plan_mu);
+  g_plans.clear();
 }
 
 ssm_status ssm_ssd_step(const void* x, const void* dt, const float* A, const void* B, const void* C,

@@ -589,7 +589,12 @@ cudaError_t launch_ssd_chunk_scan_tc(const void* x, const void* B, const void* C
   // per-CTA set-up, about three heads' worth).
   const int64_t tiles = d.batch * d.nchunks * d.ngroups * p.row_tiles;
   int64_t best_cost = -1;
-  for (int hpi = 1; hpi <= hpg; ++hpi) {
+  if (d.plan_scan_heads > 0) {  // the plan fixes the run length
+    p.heads_per_item = d.plan_scan_heads < hpg ? d.plan_scan_heads : hpg;
+    p.items_per_tile = (hpg + p.heads_per_item - 1) / p.heads_per_item;
+    best_cost = 0;
+  }
+  for (int hpi = 1; hpi <= hpg && best_cost != 0; ++hpi) {
     const int items = (hpg + hpi - 1) / hpi;
     if (hpi > 1 && (hpg + hpi - 2) / (hpi - 1) == items) continue;  // same split, shorter runs
     const int64_t waves = (tiles * items + sms - 1) / sms;

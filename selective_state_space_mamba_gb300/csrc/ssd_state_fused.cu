@@ -341,10 +341,17 @@ __global__ void __launch_bounds__(kSfThreads, 1)
 // spread a chain over several SMs.  It wins when all chains fit in one wave and are short
 // (b8 L2048 nh24: 42 us against ~49 us); with more chains than SMs the second wave costs a
 // whole chain (b4 L8192 nh80, 160 chains: 264 us against 211 us).
+// Shapes the fused kernel computes correctly (any number of chains and chunks).
+bool ssd_state_fused_possible(const SsdDims& d) {
+  return d.dtype == SSM_BF16 && d.headdim == 64 && d.dstate == 128 && (d.nheads / d.ngroups) % 2 == 0 &&
+         d.chunk % kSfKH == 0 && d.chunk <= 256;
+}
+
+// Whether the fused kernel is the faster state path: the plan's choice, else one wave of
+// chains and short chains (a long chain is one CTA's serial work).
 bool ssd_state_fused_supported(const SsdDims& d) {
-  if (!(d.dtype == SSM_BF16 && d.headdim == 64 && d.dstate == 128 && (d.nheads / d.ngroups) % 2 == 0 &&
-        d.chunk % kSfKH == 0 && d.chunk <= 256))
-    return false;
+  if (!ssd_state_fused_possible(d)) return false;
+  if (d.plan_fused >= 0) return d.plan_fused != 0;
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)

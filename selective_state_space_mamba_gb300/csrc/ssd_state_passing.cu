@@ -264,6 +264,7 @@ __global__ void __launch_bounds__(kSeqThreads) ssd_state_passing_seq_kernel(cons
 }  // namespace
 
 bool ssd_state_passing_sequential(const SsdDims& d) {
+  if (d.plan_seq >= 0) return d.plan_seq != 0;
   return d.batch * d.nheads * (int64_t)(d.headdim * d.dstate / 4) >= kSeqMinGroups;
 }
 

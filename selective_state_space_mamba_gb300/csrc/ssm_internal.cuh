@@ -282,6 +282,10 @@ struct SsdDims {
   int64_t nchunks;       // ceil(seqlen / chunk)
   int64_t lpad;          // nchunks * chunk
   ssm_dtype dtype;
+  // plan (ssm_ssd_fwd_tune / ssm_ssd_fwd_set_plan); -1 / 0 leave the choice to the heuristics
+  int plan_fused;        // 1: chunk states and state passing in one kernel, 0: two kernels
+  int plan_seq;          // 1: sequential state passing, 0: look-back state passing
+  int plan_scan_heads;   // chunk scan: heads per CTA (0: cost model)
 };
 
 // State passing tiling: a tile covers kSpElems state entries of one (batch, head) for up

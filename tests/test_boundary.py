@@ -156,3 +156,21 @@ def test_scan_baseline_host_validation(lib):
     # three-pass: one float per element plus the tile aggregates; look-back: header + 16 B per 256 elements
     assert ws(_lib.SSM_SCAN_THREE_PASS, 2, 5000) >= 4 * 10000 + 8 * 2 * 3
     assert ws(_lib.SSM_SCAN_LOOKBACK_WARP, 4, 1000) >= 256 + 16 * 16
+
+
+def test_plan_host_validation(lib):
+    # size checks come before any device query, so they run without a GPU
+    assert lib.ssm_ssd_fwd_set_plan(1, 256, 2, 32, 64, 1, 64, 0, 0) == _lib.SSM_ERR_UNSUPPORTED   # headdim 32
+    assert lib.ssm_ssd_fwd_set_plan(1, 256, 3, 64, 64, 2, 64, 0, 0) == _lib.SSM_ERR_INVALID_ARG   # nh % G
+    assert lib.ssm_ssd_fwd_get_plan(1, 256, 2, 64, 64, 1, 100, 0, None) == _lib.SSM_ERR_UNSUPPORTED  # chunk
+    args = [FAKE] * 9 + [1, 256, 2, 64, 64, 1, 64, 0, FAKE, 1 << 40, None]
+    assert lib.ssm_ssd_fwd_tune(*args, 0, None, None) == _lib.SSM_ERR_INVALID_ARG      # reps < 1
+    assert lib.ssm_ssd_fwd_tune(*args[:9], 1, 256, 2, 64, 64, 1, 64, 0, FAKE + 16, 1 << 40, None, 3, None,
+                                None) == _lib.SSM_ERR_ALIGNMENT                        # workspace alignment
+
+
+def test_plan_id_packing():
+    import selective_state_space_mamba_gb300 as ssm
+    assert ssm.plan_id() == 0 | (0 << 2)                    # all rules of thumb
+    assert ssm.plan_id(1, -1, 0) == 2
+    assert ssm.plan_id(0, 1, 20) == 1 | (2 << 2) | (20 << 4)

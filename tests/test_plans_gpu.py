@@ -1,0 +1,80 @@
+"""GPU tests of the per-shape plans of ssd_fwd (ssm_ssd_fwd_tune / _set_plan / _get_plan): every
+candidate plan computes the forward within the parity rules, and tuning stores a plan that
+later calls use."""
+import numpy as np
+import pytest
+
+import parity as P
+from oracle import ssd as ossd
+from selective_state_space_mamba_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def dev_inputs(inp, dtype):
+    d = {k: P.to_dev(inp[k], dtype) for k in ("x", "dt", "B", "C")}
+    d.update(A=P.to_dev(inp["A"]), D=P.to_dev(inp["D"]), h0=P.to_dev(inp["h0"]))
+    return d
+
+
+def run(ssm, d, chunk):
+    import torch
+    y, hf = ssm.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], chunk=chunk)
+    torch.cuda.synchronize()
+    assert ssm.check_device_status(kind="ssd") == 0
+    return P.to_np(y), P.to_np(hf)
+
+
+@pytest.mark.parametrize("dtype,hpg", [("bf16", 4), ("f32", 2)])
+def test_every_plan_is_correct(cuda_lib, dtype, hpg):
+    import selective_state_space_mamba_gb300 as ssm
+    G = 2
+    shape = synth.SSDShape(f"plans_{dtype}", 2, 700, G * hpg, 64, 128, G, 256, dtype, h0=True)
+    inp = synth.ssd_inputs(shape, seed=51)
+    d = dev_inputs(inp, dtype)
+    y_ref, hf_ref = ossd.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"])
+    plans = [ssm.plan_id(0, 1, 0), ssm.plan_id(0, 0, 0)]
+    if dtype == "bf16":
+        plans += [ssm.plan_id(1, -1, 0)] + [ssm.plan_id(f, 1 - f, h) for f in (0, 1) for h in (1, 2, hpg)]
+    try:
+        for plan in plans:
+            ssm.set_ssd_fwd_plan(d["x"], d["B"], shape.chunk, plan)
+            assert ssm.get_ssd_fwd_plan(d["x"], d["B"], shape.chunk) == plan
+            y, hf = run(ssm, d, shape.chunk)
+            P.assert_ssd_close(dtype, y, y_ref, hf, hf_ref, f"plan {plan}")
+        ssm.set_ssd_fwd_plan(d["x"], d["B"], shape.chunk, -1)
+        assert ssm.get_ssd_fwd_plan(d["x"], d["B"], shape.chunk) == -1
+    finally:
+        ssm.clear_ssd_fwd_plans()
+
+
+def test_tune_stores_the_fastest_plan(cuda_lib):
+    import selective_state_space_mamba_gb300 as ssm
+    shape = synth.SSD_B8_L2048
+    inp = synth.ssd_inputs(shape)
+    d = dev_inputs(inp, shape.dtype)
+    try:
+        plan, ms = ssm.tune_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], chunk=shape.chunk, reps=3)
+        assert plan >= 0 and ms > 0
+        assert ssm.get_ssd_fwd_plan(d["x"], d["B"], shape.chunk) == plan
+        y, hf = run(ssm, d, shape.chunk)
+        units = [0, 57, 191]
+        from oracle import native
+        y_ref, hf_ref = native.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"],
+                                       units=np.asarray(units))
+        nh = shape.nheads
+        P.assert_ssd_close(shape.dtype, np.stack([y[u // nh, :, u % nh] for u in units]), y_ref,
+                           np.stack([hf[u // nh, u % nh] for u in units]), hf_ref, f"tuned plan {plan}")
+    finally:
+        ssm.clear_ssd_fwd_plans()
+
+
+def test_invalid_plan_rejected(cuda_lib):
+    import selective_state_space_mamba_gb300 as ssm
+    from selective_state_space_mamba_gb300 import _lib
+    import torch
+    x = torch.zeros((1, 256, 2, 64), device="cuda", dtype=torch.bfloat16)
+    B = torch.zeros((1, 256, 1, 128), device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(ssm.SsmError) as e:
+        ssm.set_ssd_fwd_plan(x, B, 256, 3)   # fused field 3 is not a choice
+    assert e.value.status == _lib.SSM_ERR_INVALID_ARG
