@@ -243,9 +243,15 @@ def run_ours(args, world, rank, local):
     def ssd_call():
         ssm.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], chunk=SSD.chunk, y=y, h_final=hf)
 
-    # per-shape plan, chosen by measurement once before anything is timed (as a user would)
-    plan, plan_ms = ssm.tune_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], chunk=SSD.chunk,
-                                     reps=5, y=y, h_final=hf)
+    # per-shape plan, chosen by measurement once before anything is timed (as a user would);
+    # "rules" keeps the library's rules of thumb (for profiler runs, where timings are skewed)
+    if args.plan == "tune":
+        plan, plan_ms = ssm.tune_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"],
+                                         chunk=SSD.chunk, reps=5, y=y, h_final=hf)
+        plan_how = "ssm_ssd_fwd_tune before the warm-up: every candidate plan timed, the fastest kept"
+    else:
+        ssm.set_ssd_fwd_plan(d["x"], d["B"], SSD.chunk, -1)
+        plan, plan_ms, plan_how = 0, 0.0, "the library's rules of thumb (no tuning)"
 
     def scan_call():
         ssm.linscan_fwd(a, bsc, h=h)
@@ -360,8 +366,7 @@ def run_ours(args, world, rank, local):
             "l2": "inputs larger than L2, and L2 flushed by a 256 MiB write before each timed step",
             "parallelism": f"replicas x{world} (independent problems, no collective)",
             "plan": {"id": plan, "fused_state_path": (plan & 3) - 1, "sequential_state_passing": ((plan >> 2) & 3) - 1,
-                     "scan_heads_per_cta": plan >> 4, "tuning_median_ms": round(plan_ms, 4),
-                     "how": "ssm_ssd_fwd_tune before the warm-up: every candidate plan timed, the fastest kept"},
+                     "scan_heads_per_cta": plan >> 4, "tuning_median_ms": round(plan_ms, 4), "how": plan_how},
         },
         "ssd": {"tokens_per_s": round(value, 1), "ms": round(ssd_ms_max, 4), "model_B_bytes": model_b,
                 "roofline_ms": round(ssd_roof_ms, 4), "roofline_frac": round(ssd_roof_ms / ssd_ms_max, 4),
@@ -611,6 +616,8 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=15.0, help="time budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--plan", choices=("tune", "rules"), default="tune",
+                    help="ssd_fwd plan: tuned by measurement first (default) or the rules of thumb")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
