@@ -424,6 +424,12 @@ def run_decode(args, peaks):
 # states and decay products
 SCAN_LEVEL_BYTES = {"blelloch": 12, "three_pass": 28, "lookback_serial": 12, "lookback_warp": 12,
                     "linscan_fwd": 12}
+# Hillis-Steele: per pass, two arrays read at t and t - d, two written (the last pass: one)
+
+
+def hs_bytes(length):
+    passes = max(0, (length - 1).bit_length())
+    return 24 * passes - 4 if passes else 8
 
 
 def run_scan_baselines(args, peaks):
@@ -440,7 +446,7 @@ def run_scan_baselines(args, peaks):
         b = torch.from_numpy(inp["b"]).cuda()
         h = torch.empty_like(a)
         res = {}
-        for algo in ("blelloch", "three_pass", "lookback_serial", "lookback_warp", "linscan_fwd"):
+        for algo in ("blelloch", "three_pass", "lookback_serial", "lookback_warp", "hillis_steele", "linscan_fwd"):
             if algo == "blelloch" and length > 2048:
                 continue
             if algo == "linscan_fwd":
@@ -463,7 +469,8 @@ def run_scan_baselines(args, peaks):
                 per.append(e0.elapsed_time(e1))
             ms = statistics.median(per)
             n = rows * length
-            moved = SCAN_LEVEL_BYTES[algo] * n / (ms * 1e-3) / 1e9
+            per_elem = hs_bytes(length) if algo == "hillis_steele" else SCAN_LEVEL_BYTES[algo]
+            moved = per_elem * n / (ms * 1e-3) / 1e9
             res[algo] = {"ms": round(ms, 4), "GB/s_3_array_model": round(12 * n / (ms * 1e-3) / 1e9, 1),
                          "GB/s_moved": round(moved, 1), "hbm_frac_moved": round(moved / peaks["hbm_gbs"], 4)}
         out[f"{rows}x{length}"] = res

@@ -245,6 +245,9 @@ SSM_API ssm_status ssm_linscan_fwd_noalloc(const float *a, const float *b, float
  *   SSM_SCAN_LOOKBACK_WARP     Level 3b: the same with a warp inspecting 32 predecessors at once.
  *                              Both look-backs need a zero-filled workspace (left ready for the
  *                              next call) and report timeouts through ssm_check_device_status.
+ *   SSM_SCAN_HILLIS_STEELE     the page's PyTorch baseline algorithm (listed there as future
+ *                              work in CUDA): ceil(log2 len) full-array passes of the combine at
+ *                              doubling distances.  Workspace: four floats per element.
  * Arguments as ssm_linscan_fwd.  Errors: SSM_ERR_INVALID_ARG (unknown algorithm, negative
  * size), SSM_ERR_UNSUPPORTED (a size beyond the algorithm's limit), SSM_ERR_ALIGNMENT,
  * SSM_ERR_WORKSPACE, SSM_ERR_CUDA.
@@ -253,7 +256,8 @@ typedef enum {
     SSM_SCAN_BLELLOCH = 1,
     SSM_SCAN_THREE_PASS = 2,
     SSM_SCAN_LOOKBACK_SERIAL = 3,
-    SSM_SCAN_LOOKBACK_WARP = 4
+    SSM_SCAN_LOOKBACK_WARP = 4,
+    SSM_SCAN_HILLIS_STEELE = 5
 } ssm_scan_algo;
 SSM_API size_t ssm_linscan_baseline_workspace_bytes(ssm_scan_algo algo, int64_t rows, int64_t len);
 SSM_API ssm_status ssm_linscan_baseline(ssm_scan_algo algo, const float *a, const float *b, float *h, int64_t rows,

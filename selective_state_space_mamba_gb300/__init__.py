@@ -262,12 +262,14 @@ def linscan_fwd(a, b, *, h=None, workspace: Workspace | None = None):
 
 
 SCAN_BASELINES = {"blelloch": _lib.SSM_SCAN_BLELLOCH, "three_pass": _lib.SSM_SCAN_THREE_PASS,
-                  "lookback_serial": _lib.SSM_SCAN_LOOKBACK_SERIAL, "lookback_warp": _lib.SSM_SCAN_LOOKBACK_WARP}
+                  "lookback_serial": _lib.SSM_SCAN_LOOKBACK_SERIAL, "lookback_warp": _lib.SSM_SCAN_LOOKBACK_WARP,
+                  "hillis_steele": _lib.SSM_SCAN_HILLIS_STEELE}
 
 
 def linscan_baseline(a, b, algo: str, *, h=None, workspace: Workspace | None = None):
     """The scalar scan by one of the reference page's baseline levels (see include/ssm.h,
-    ssm_linscan_baseline): "blelloch", "three_pass", "lookback_serial" or "lookback_warp"."""
+    ssm_linscan_baseline): "blelloch", "three_pass", "lookback_serial", "lookback_warp" or
+    "hillis_steele"."""
     torch = _torch()
     lib = _lib.load()
     _require(algo in SCAN_BASELINES, f"algo must be one of {sorted(SCAN_BASELINES)}")

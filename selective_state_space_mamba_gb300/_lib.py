@@ -14,7 +14,8 @@ from . import _build
 SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_ALIGNMENT, SSM_ERR_WORKSPACE, SSM_ERR_CUDA, \
     SSM_ERR_TIMEOUT = range(7)
 SSM_F32, SSM_BF16 = 0, 1
-SSM_SCAN_BLELLOCH, SSM_SCAN_THREE_PASS, SSM_SCAN_LOOKBACK_SERIAL, SSM_SCAN_LOOKBACK_WARP = 1, 2, 3, 4
+SSM_SCAN_BLELLOCH, SSM_SCAN_THREE_PASS, SSM_SCAN_LOOKBACK_SERIAL, SSM_SCAN_LOOKBACK_WARP, SSM_SCAN_HILLIS_STEELE = \
+    1, 2, 3, 4, 5
 
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ("ssm_status_string", "ssm_version", "ssm_ssd_fwd_workspace_bytes", "ssm_ssd_fwd",

@@ -15,6 +15,11 @@
 //   Level 3   single pass, decoupled look-back over 256-element tiles claimed in counter
 //             order, one element per thread; thread 0 walks the predecessors one at a time.
 //   Level 3b  the same with a whole warp inspecting 32 predecessors at once.
+//   Hillis-Steele  the page's PyTorch baseline algorithm, which it lists as future work in
+//             CUDA: ceil(log2 L) passes over the whole array, pass d replacing every pair at
+//             position t >= d of its row by (pair at t - d) . (pair at t); pairs ping-pong
+//             between two workspace buffers, the last pass writes h (the b of the prefix).
+//             Work-inefficient: L log L combines, ~24 bytes per element and pass.
 //
 // Levels 3 and 3b scan all rows as one flattened sequence with a reset at each row start
 // (the combine selects the later b when its decay is 0), like linscan_lookback.  Their waits
@@ -311,6 +316,23 @@ __global__ void __launch_bounds__(kLbThreads) scan_lookback_kernel(const float* 
   if (threadIdx.x == 0) retire_tile(hdr, gridDim.x);
 }
 
+// ---------------------------------------------------------------- Hillis-Steele
+constexpr int kHsThreads = 256;
+
+// One pass at distance d: out[t] = in[t - d] . in[t] where t - d is in the same row.
+// bout == h and aout == nullptr on the last pass (only the states are needed).
+__global__ void __launch_bounds__(kHsThreads) scan_hs_pass_kernel(const float* __restrict__ ain,
+                                                                  const float* __restrict__ bin,
+                                                                  float* __restrict__ aout, float* __restrict__ bout,
+                                                                  int64_t n, int64_t len, int64_t d) {
+  const int64_t e = (int64_t)blockIdx.x * kHsThreads + threadIdx.x;
+  if (e >= n) return;
+  Aff cur{ain[e], bin[e]};
+  if (e % len >= d) cur = cat(Aff{ain[e - d], bin[e - d]}, cur);
+  if (aout) aout[e] = cur.a;
+  bout[e] = cur.b;
+}
+
 }  // namespace
 
 size_t linscan_baseline_workspace(ssm_scan_algo algo, int64_t rows, int64_t len) {
@@ -325,6 +347,8 @@ size_t linscan_baseline_workspace(ssm_scan_algo algo, int64_t rows, int64_t len)
     case SSM_SCAN_LOOKBACK_SERIAL:
     case SSM_SCAN_LOOKBACK_WARP:
       return kHeaderBytes + sizeof(LsDesc) * (size_t)((n + kLbThreads - 1) / kLbThreads);
+    case SSM_SCAN_HILLIS_STEELE:
+      return 4 * ((sizeof(float) * (size_t)n + 255) / 256 * 256);  // two ping-pong pair buffers
   }
   return 0;
 }
@@ -335,6 +359,8 @@ ssm_status linscan_baseline_check(ssm_scan_algo algo, int64_t rows, int64_t len)
     return (len + kTpTile - 1) / kTpTile <= kTpTile && rows <= 65535 ? SSM_OK : SSM_ERR_UNSUPPORTED;
   if (algo == SSM_SCAN_LOOKBACK_SERIAL || algo == SSM_SCAN_LOOKBACK_WARP)
     return (rows * len + kLbThreads - 1) / kLbThreads <= 0x7fffffffLL ? SSM_OK : SSM_ERR_UNSUPPORTED;
+  if (algo == SSM_SCAN_HILLIS_STEELE)
+    return (rows * len + kHsThreads - 1) / kHsThreads <= 0x7fffffffLL ? SSM_OK : SSM_ERR_UNSUPPORTED;
   return SSM_ERR_INVALID_ARG;
 }
 
@@ -369,6 +395,27 @@ cudaError_t launch_linscan_baseline(ssm_scan_algo algo, const float* a, const fl
         scan_lookback_kernel<false><<<(unsigned)tiles, kLbThreads, 0, s>>>(a, b, h, n, len, desc, hdr, ctl);
       else
         scan_lookback_kernel<true><<<(unsigned)tiles, kLbThreads, 0, s>>>(a, b, h, n, len, desc, hdr, ctl);
+      return cudaGetLastError();
+    }
+    case SSM_SCAN_HILLIS_STEELE: {
+      if (len == 1) return cudaMemcpyAsync(h, b, sizeof(float) * (size_t)n, cudaMemcpyDeviceToDevice, s);
+      const size_t arr = (sizeof(float) * (size_t)n + 255) / 256 * 256;
+      char* w = static_cast<char*>(workspace);
+      float* buf_a[2] = {reinterpret_cast<float*>(w), reinterpret_cast<float*>(w + 2 * arr)};
+      float* buf_b[2] = {reinterpret_cast<float*>(w + arr), reinterpret_cast<float*>(w + 3 * arr)};
+      const unsigned grid = (unsigned)((n + kHsThreads - 1) / kHsThreads);
+      const float* ain = a;
+      const float* bin = b;
+      int nb = 0;
+      for (int64_t d = 1; d < len; d <<= 1) {
+        const bool last = 2 * d >= len;
+        float* aout = last ? nullptr : buf_a[nb];
+        float* bout = last ? h : buf_b[nb];
+        scan_hs_pass_kernel<<<grid, kHsThreads, 0, s>>>(ain, bin, aout, bout, n, len, d);
+        ain = buf_a[nb];
+        bin = buf_b[nb];
+        nb ^= 1;
+      }
       return cudaGetLastError();
     }
   }

@@ -10,7 +10,7 @@ from selective_state_space_mamba_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 
-ALGOS = ["blelloch", "three_pass", "lookback_serial", "lookback_warp"]
+ALGOS = ["blelloch", "three_pass", "lookback_serial", "lookback_warp", "hillis_steele"]
 
 
 def run(algo, rows, length, seed=3, a_low=0.90):
@@ -40,7 +40,7 @@ def test_baseline_small_shapes(cuda_lib, algo):
         P.assert_rows_close(h, ref, f"{algo} {rows}x{length}")
 
 
-@pytest.mark.parametrize("algo", ["three_pass", "lookback_serial", "lookback_warp"])
+@pytest.mark.parametrize("algo", ["three_pass", "lookback_serial", "lookback_warp", "hillis_steele"])
 def test_baseline_full_workload_sampled_rows(cuda_lib, algo):
     shape = synth.SCAN_384x65536
     inp, h = run(algo, shape.rows, shape.length, seed=synth.WORKLOAD_SEED[shape.name])
