@@ -9,12 +9,14 @@
 // remainder) and both are multiplied, so the weighting costs no bf16 rounding (2^-18 instead of
 // 2^-9 relative): the chunk states feed h_final, whose tolerance a single bf16 rounding of
 // x * w exceeds.  One MMA tile covers TWO heads of the same B/C group: M = 128 rows
-// (64 p-values of each head), N = S = 128, K = the chunk's tokens.  Both operands are
-// MN-major in shared memory, exactly as TMA lands them in 128-byte swizzle: A = X (p
-// contiguous), B = the group's B (s contiguous).  The per-token weight is applied to X in
-// shared memory (the post scales B instead; B is shared by the heads of a group here, so the
-// per-head weight goes on X — the "swap A/B" idea of the post's optimisation section read the
-// other way round).
+// (64 p-values of each head), N = S = 128, K = the chunk's tokens.  B (the group's B, s
+// contiguous) is read from shared memory as TMA lands it; the weighted X is the A operand and
+// is read from TENSOR MEMORY: the scaler threads write hi and lo straight into TMEM (a thread
+// owns one row p, i.e. one TMEM lane, and packs two tokens per 32-bit column), so neither the
+// split halves nor the MMA's reads of them touch shared memory.  The per-token weight goes on
+// X (the post scales B instead; B is shared by the heads of a group here, so the per-head
+// weight goes on X — the "swap A/B" idea of the post's optimisation section read the other
+// way round).
 //
 // The weighted X and its remainder come from three bf16x2 FMAs per pair of values, each with
 // one rounding: w is split into w_hi + w_lo (bf16 each); hi = x w_hi rounded; hi - x w_hi is
@@ -28,11 +30,13 @@
 //   warp 0      TMA producer: B when the group changes; X of the pair's two heads, 64 tokens
 //               at a time, with those tokens' G and dt and the chunk's last G, into a 4-stage
 //               ring
-//   warp 1      TMEM owner and MMA issuer (one thread): 2 x 4 MMAs (hi, lo) per stage into one
-//               of two 128-column f32 accumulators; tcgen05.commit frees the stage, and after
-//               the last stage of a unit hands the accumulator to the epilogue
-//   warps 2-9   half a token row of one head per thread: w = dt 2^(G_last - G_t), then 32 of
-//               the row's 64 values of X in shared memory -> hi (in place) and lo
+//   warp 1      TMEM owner and MMA issuer (one thread): 2 x 4 MMAs (hi, lo) per stage, A from
+//               TMEM, into one of two 128-column f32 accumulators; tcgen05.commit frees the
+//               stage (its X in shared memory and its hi/lo columns in TMEM), and after the
+//               last stage of a unit hands the accumulator to the epilogue
+//   warps 2-9   one row p of one head per thread (its TMEM lane) and half the stage's tokens:
+//               64 threads first tabulate the bf16 weight pairs of the stage's token pairs,
+//               then every thread turns its 32 values of X into 16 hi and 16 lo columns
 //   warps 10-13 epilogue: TMEM -> registers -> a swizzled 32 x 32 f32 block per warp in shared
 //               memory -> TMA store into S_c; the accumulator is freed after its last TMEM load
 // Every wait is bounded; on expiry the CTA records SSM_ERR_TIMEOUT, drains, frees its TMEM
@@ -46,10 +50,12 @@ constexpr int kCsWarps = 14;  // 0 producer, 1 MMA, 2-9 scalers, 10-13 epilogue
 constexpr int kCsThreads = kCsWarps * 32;
 constexpr int kCsMaxT = 256;
 constexpr int kCsKH = 64;         // tokens per stage
-constexpr int kCsStages = 4;
+constexpr int kCsStages = 8;   // X ring in shared memory (released once the scalers have read it)
+constexpr int kCsAStages = 4;  // hi/lo ring in TMEM (released when the MMAs have read it)
 constexpr int kCsRowBytes = 128;  // 64 bf16 per swizzled row
 constexpr uint32_t kCsScaleBar = 1, kCsEpiBar = 2;
-constexpr uint32_t kCsTmemCols = 256;  // two 128-column accumulators
+constexpr uint32_t kCsTmemCols = 512;  // two 128-column accumulators, then 64 A columns per stage
+constexpr uint32_t kCsTmemA = 256;     // hi of A stage a at kCsTmemA + 64 a, lo 32 columns later
 // per stage and head: G of the stage's tokens, dt of the stage's tokens, the chunk's last 4 G
 constexpr uint32_t kCsGdHead = (2 * kCsKH + 4) * 4;
 
@@ -63,26 +69,27 @@ struct CsParams {
 };
 
 // Shared-memory layout (offsets from a 1024-byte aligned base), chunk size T:
-//   stage[4] = { hi[2 heads][64 rows][128 B], lo[2 heads][64 rows][128 B] }   swizzled
+//   stage[8] = X[2 heads][64 rows][128 B]                                      swizzled
 //   bm[s block][T rows][128 B]                                                 swizzled
 //   epi[4 warps][32 rows][128 B]   S_c staging for the TMA store (swizzled)
-//   gd[4 stages][2 heads] = { G[64], dt[64], G[T-4 .. T-1] }
+//   gd[8 stages][2 heads] = { G[64], dt[64], G[T-4 .. T-1] }
+//   wt[4 A stages][2 heads][32 token pairs] = { w_hi pair, -w_hi pair, -w_lo pair } (bf16x2)
 //   barriers, TMEM base, abort flag
 struct CsLayout {
-  uint32_t half_bytes, stage_bytes, bm0, epi0, gd0, bars, total;
+  uint32_t stage_bytes, bm0, epi0, gd0, wt0, bars, total;
   __host__ __device__ explicit CsLayout(int T) {
-    half_bytes = 2u * kCsKH * kCsRowBytes;
-    stage_bytes = 2u * half_bytes;
+    stage_bytes = 2u * kCsKH * kCsRowBytes;
     bm0 = kCsStages * stage_bytes;
     epi0 = bm0 + 2u * T * kCsRowBytes;
     gd0 = epi0 + 4u * 32 * kCsRowBytes;
-    bars = gd0 + kCsStages * 2u * kCsGdHead;
-    total = bars + 24 * 8 + 16;
+    wt0 = gd0 + kCsStages * 2u * kCsGdHead;
+    bars = wt0 + kCsAStages * 2u * (kCsKH / 2) * 16u;
+    total = bars + 32 * 8 + 16;
   }
 };
 enum CsBar {
-  kBFull = 0, kXFull = 1, kXScaled = kXFull + kCsStages, kXEmpty = kXScaled + kCsStages,
-  kAccFull = kXEmpty + kCsStages, kAccEmpty = kAccFull + 2, kDone = kAccEmpty + 2, kNumBars = kDone + 1
+  kBFull = 0, kBEmpty = 1, kXFull = 2, kXEmpty = kXFull + kCsStages, kAFull = kXEmpty + kCsStages, kAEmpty = kAFull + kCsAStages,
+  kAccFull = kAEmpty + kCsAStages, kAccEmpty = kAccFull + 2, kDone = kAccEmpty + 2, kNumBars = kDone + 1
 };
 
 // d = a * b + c on bf16 pairs, one rounding
@@ -90,10 +97,6 @@ __device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t 
   uint32_t d;
   asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
-}
-__device__ __forceinline__ uint32_t bf16_pair(float v) {
-  const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-  return h | (h << 16);
 }
 
 struct CsUnit {
@@ -123,8 +126,9 @@ __global__ void __launch_bounds__(kCsThreads, 1)
   const CsLayout L(T);
   const int nk = T / kCsKH;  // stages per unit
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bars);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.bars + 24 * 8);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.bars + 24 * 8 + 4);
+  static_assert(kNumBars <= 32, "barrier area");
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.bars + 32 * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.bars + 32 * 8 + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_launch_dependents();
@@ -155,6 +159,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
     if (lane == 0 && u_end > u_begin) {
       int64_t cur_grp = -1;
       int64_t i = 0;  // stage step
+      int nreload = 0;
       bool ok = true;
       for (int64_t u = u_begin; u < u_end && ok && !*abort_flag; ++u) {
         const CsUnit w = cs_unit(p, u);
@@ -166,12 +171,14 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             break;
           }
           if (w.grp != cur_grp) {
-            // B is read by every MMA issued so far: wait for the last of them before replacing it
-            if (i > 0 && !mbar_wait(&bars[kXEmpty + (int)((i - 1) % kCsStages)],
-                                    (uint32_t)((i - 1) / kCsStages) & 1u, ctl.spin_limit_ns)) {
+            // B is read by every MMA of the previous group: the MMA thread releases it when it
+            // moves on (this producer may be up to three rings ahead of the MMAs, so it waits on
+            // a barrier of its own rather than on a ring's)
+            if (nreload > 0 && !mbar_wait(&bars[kBEmpty], (uint32_t)(nreload - 1) & 1u, ctl.spin_limit_ns)) {
               ok = false;
               break;
             }
+            ++nreload;
             mbar_arrive_expect_tx(&bars[kBFull], 2u * T * kCsRowBytes);
             for (int sb = 0; sb < 2; ++sb)
               tc::tma_load_3d(base + L.bm0 + sb * T * kCsRowBytes, &map_b, w.g * 128 + sb * 64, (int)(w.c * T),
@@ -179,7 +186,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             cur_grp = w.grp;
           }
           unsigned char* gd = base + L.gd0 + st * 2 * kCsGdHead;
-          mbar_arrive_expect_tx(&bars[kXFull + st], L.half_bytes + 2u * kCsGdHead);
+          mbar_arrive_expect_tx(&bars[kXFull + st], L.stage_bytes + 2u * kCsGdHead);
           for (int hh = 0; hh < 2; ++hh) {
             tc::tma_load_3d(base + st * L.stage_bytes + hh * kCsKH * kCsRowBytes, &map_x, (w.h + hh) * 64,
                             (int)(w.c * T + kh * kCsKH), (int)w.bi, &bars[kXFull + st]);
@@ -198,8 +205,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ---------------------------------------------
     if (lane == 0 && u_end > u_begin) {
-      const uint32_t idesc = tc::idesc_bf16_f32(128, 128, /*a_mn=*/true, /*b_mn=*/true);
-      const uint32_t a_lbo = kCsKH * kCsRowBytes;  // head 0 block -> head 1 block (MN blocks)
+      const uint32_t idesc = tc::idesc_bf16_f32(128, 128, /*a_mn=*/false, /*b_mn=*/true);  // A from TMEM
       const uint32_t b_lbo = T * kCsRowBytes;      // s 0..63 block -> s 64..127 block
       const uint32_t sbo = 8 * kCsRowBytes;        // next 8-token group
       int64_t cur_grp = -1, i = 0;
@@ -209,29 +215,30 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         const CsUnit w = cs_unit(p, u);
         const int acc = q & 1;
         if (w.grp != cur_grp) {
+          if (nb > 0) tc::mma_commit(&bars[kBEmpty]);  // the previous group's B, once its MMAs are done
           ++nb;
           cur_grp = w.grp;
           ok = mbar_wait(&bars[kBFull], (uint32_t)(nb - 1) & 1u, ctl.spin_limit_ns);
         }
         if (ok && q >= 2) ok = mbar_wait(&bars[kAccEmpty + acc], (uint32_t)((q >> 1) - 1) & 1u, ctl.spin_limit_ns);
         for (int kh = 0; kh < nk && ok; ++kh, ++i) {
-          const int st = (int)(i % kCsStages);
-          if (!mbar_wait(&bars[kXScaled + st], (uint32_t)(i / kCsStages) & 1u, ctl.spin_limit_ns)) {
+          const int as = (int)(i % kCsAStages);
+          if (!mbar_wait(&bars[kAFull + as], (uint32_t)(i / kCsAStages) & 1u, ctl.spin_limit_ns)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          const uint32_t hi0 = smem_addr(base + st * L.stage_bytes);
-          const uint32_t lo0 = hi0 + L.half_bytes;
+          const uint32_t a_hi = tmem + kCsTmemA + 64u * as, a_lo = a_hi + 32;
           const uint32_t b0 = smem_addr(base + L.bm0) + kh * kCsKH * kCsRowBytes;
 #pragma unroll
           for (int ks = 0; ks < kCsKH / 16; ++ks) {
-            const uint32_t koff = ks * 16 * kCsRowBytes;  // 16 tokens = two 8-row groups
+            const uint32_t koff = ks * 16 * kCsRowBytes;  // 16 tokens = two 8-row groups of B
             const uint64_t bdesc = tc::sdesc_sw128(b0 + koff, b_lbo, sbo);
-            tc::mma_bf16(tmem + acc * 128, tc::sdesc_sw128(hi0 + koff, a_lbo, sbo), bdesc, idesc, kh > 0 || ks > 0);
-            tc::mma_bf16(tmem + acc * 128, tc::sdesc_sw128(lo0 + koff, a_lbo, sbo), bdesc, idesc, true);
+            // 16 tokens of A = 8 TMEM columns (two tokens per column)
+            tc::mma_bf16_ts(tmem + acc * 128, a_hi + ks * 8, bdesc, idesc, kh > 0 || ks > 0);
+            tc::mma_bf16_ts(tmem + acc * 128, a_lo + ks * 8, bdesc, idesc, true);
           }
-          tc::mma_commit(&bars[kXEmpty + st]);  // the stage may be refilled
+          tc::mma_commit(&bars[kAEmpty + as]);  // the A stage's TMEM columns may be rewritten
         }
         if (ok) tc::mma_commit(&bars[kAccFull + acc]);  // the accumulator is ready
       }
@@ -240,53 +247,69 @@ __global__ void __launch_bounds__(kCsThreads, 1)
       mbar_wait(&bars[kDone], 0, ctl.spin_limit_ns);  // every MMA has completed
     }
   } else if (warp < 10) {
-    // ---------------- scale X by w, split into bf16 hi + lo parts --------------------------
-    const int st_t = threadIdx.x - 64;  // 0..255
-    const int t = st_t >> 1;            // token row of the stage: head t / 64, token t % 64
-    const int part = st_t & 1;          // which half of the row's eight 16-byte chunks
-    const int hh = t / kCsKH, tok = t % kCsKH;
+    // ---------------- scale X by w, split into bf16 hi + lo parts, into TMEM ----------------
+    const int st_t = threadIdx.x - 64;     // 0..255
+    const int quad = warp & 3;             // TMEM lanes 32 quad .. +31
+    const int half = (warp - 2) >> 2;      // tokens 32 half .. 32 half + 31 of the stage
+    const int hh = quad >> 1;              // rows 0..63: head 0, rows 64..127: head 1
+    const int prow = (quad & 1) * 32 + lane;  // this thread's p within its head
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     int64_t i = 0;
     bool ok = true;
     for (int64_t u = u_begin; u < u_end && ok; ++u) {
       for (int kh = 0; kh < nk; ++kh, ++i) {
-        const int st = (int)(i % kCsStages);
-        const bool bad = !mbar_wait(&bars[kXFull + st], (uint32_t)(i / kCsStages) & 1u, ctl.spin_limit_ns);
+        const int st = (int)(i % kCsStages), as = (int)(i % kCsAStages);
+        // X of step i has landed, and the MMAs of step i - 4 have read this A stage's columns
+        const bool bad =
+            !mbar_wait(&bars[kXFull + st], (uint32_t)(i / kCsStages) & 1u, ctl.spin_limit_ns) ||
+            (i >= kCsAStages &&
+             !mbar_wait(&bars[kAEmpty + as], (uint32_t)((i / kCsAStages) - 1) & 1u, ctl.spin_limit_ns));
         if (named_bar_any(kCsScaleBar, 256, bad)) {  // leave together, or not at all
           if (st_t == 0) fail();
           ok = false;
           break;
         }
-        const float* gd = reinterpret_cast<const float*>(base + L.gd0 + (st * 2 + hh) * kCsGdHead);
-        const float wv = gd[kCsKH + tok] * tc::ex2_approx(gd[2 * kCsKH + 3] - gd[tok]);
-        const __nv_bfloat16 w_hi = __float2bfloat16_rn(wv);
-        const float w_lo = wv - __bfloat162float(w_hi);
-        const uint32_t whi2 = bf16_pair(__bfloat162float(w_hi));
-        const uint32_t nwhi2 = whi2 ^ 0x80008000u;
-        const uint32_t nwlo2 = bf16_pair(-w_lo);
-        unsigned char* hrow = base + st * L.stage_bytes + t * kCsRowBytes;
-        unsigned char* lrow = hrow + L.half_bytes;
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const int cc = part * 4 + c4;
-          const int off = (cc ^ (t & 7)) << 4;  // the row's chunks, spread over the banks
-          uint4 v = *reinterpret_cast<const uint4*>(hrow + off);
-          uint32_t* e = reinterpret_cast<uint32_t*>(&v);
-          uint4 r;
-          uint32_t* f = reinterpret_cast<uint32_t*>(&r);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t x2 = e[k];
-            const uint32_t h2 = fma_bf16x2(x2, whi2, 0x80008000u);  // x w_hi, rounded
-            const uint32_t d2 = fma_bf16x2(x2, nwhi2, h2);           // hi - x w_hi, exact
-            f[k] = fma_bf16x2(x2, nwlo2, d2) ^ 0x80008000u;          // x w - hi, rounded
-            e[k] = h2;
-          }
-          *reinterpret_cast<uint4*>(hrow + off) = v;
-          *reinterpret_cast<uint4*>(lrow + off) = r;
+        tc::fence_after_sync();
+        uint4* wt = reinterpret_cast<uint4*>(base + L.wt0) + as * 2 * (kCsKH / 2);
+        if (st_t < 2 * (kCsKH / 2)) {  // the bf16 weight pairs of (head, token pair)
+          const int wh = st_t / (kCsKH / 2), pr = st_t % (kCsKH / 2);
+          const float* gd = reinterpret_cast<const float*>(base + L.gd0 + (st * 2 + wh) * kCsGdHead);
+          const float glast = gd[2 * kCsKH + 3];
+          const float w0 = gd[kCsKH + 2 * pr] * tc::ex2_approx(glast - gd[2 * pr]);
+          const float w1 = gd[kCsKH + 2 * pr + 1] * tc::ex2_approx(glast - gd[2 * pr + 1]);
+          const __nv_bfloat162 whi = __floats2bfloat162_rn(w0, w1);
+          const __nv_bfloat162 nwlo =
+              __floats2bfloat162_rn(__bfloat162float(whi.x) - w0, __bfloat162float(whi.y) - w1);
+          const uint32_t whi2 = *reinterpret_cast<const uint32_t*>(&whi);
+          wt[wh * (kCsKH / 2) + pr] = make_uint4(whi2, whi2 ^ 0x80008000u, *reinterpret_cast<const uint32_t*>(&nwlo), 0u);
         }
-        fence_proxy_async_smem();
         named_bar_sync(kCsScaleBar, 256);
-        if (st_t == 0) mbar_arrive(&bars[kXScaled + st]);
+        // my row p of head hh: tokens 32 half + 2 j and + 2 j + 1 form TMEM column 16 half + j
+        const unsigned char* xh = base + st * L.stage_bytes + hh * kCsKH * kCsRowBytes;
+        const int cpos = (prow >> 3), cin = (prow & 7) * 2;  // 16-byte chunk and byte within it
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int t0 = 32 * half + 2 * j, t1 = t0 + 1;
+          const uint32_t x0 = *reinterpret_cast<const uint16_t*>(xh + t0 * kCsRowBytes + ((cpos ^ (t0 & 7)) << 4) + cin);
+          const uint32_t x1 = *reinterpret_cast<const uint16_t*>(xh + t1 * kCsRowBytes + ((cpos ^ (t1 & 7)) << 4) + cin);
+          const uint32_t x2 = x0 | (x1 << 16);
+          const uint4 w = wt[hh * (kCsKH / 2) + 16 * half + j];
+          const uint32_t h2 = fma_bf16x2(x2, w.x, 0x80008000u);  // x w_hi, rounded
+          const uint32_t d2 = fma_bf16x2(x2, w.y, h2);           // hi - x w_hi, exact
+          lo[j] = fma_bf16x2(x2, w.z, d2) ^ 0x80008000u;         // x w - hi, rounded
+          hi[j] = h2;
+        }
+        const uint32_t a_hi = tmem + lane_base + kCsTmemA + 64u * as + 16u * half;
+        tc::tmem_st16(a_hi, hi);
+        tc::tmem_st16(a_hi + 32, lo);
+        tc::tmem_st_wait();
+        tc::fence_before_sync();
+        named_bar_sync(kCsScaleBar, 256);
+        if (st_t == 0) {
+          mbar_arrive(&bars[kXEmpty + st]);  // X and G/dt of step i are read: refill the stage
+          mbar_arrive(&bars[kAFull + as]);   // hi and lo of step i are in TMEM
+        }
       }
     }
   } else {
