@@ -165,6 +165,20 @@ ssm_status check_ssd_buffers(const void* x, const void* dt, const float* A, cons
 
 }  // namespace
 
+cudaError_t ensure_smem_limit(const void* func, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  size_t& have = done[{dev, func}];
+  if (have >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) have = bytes;
+  return e;
+}
+
 LookbackCtl next_lookback_ctl() {
   LookbackCtl c;
   uint32_t e;
@@ -571,9 +585,14 @@ ssm_status ssm_check_device_status(void* workspace, ssm_stream_t stream) {
   unsigned long long word = 0;
   if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return SSM_ERR_CUDA;
   if (word == 0) return SSM_OK;
-  // a failed call may also have left the claim counters set: clear the whole header
-  const WsHeader zero{};
-  if (cudaMemcpy(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SSM_ERR_CUDA;
+  // a failed call may also have left the claim counters set: clear them, and move the flag
+  // epoch on so that the failed call's flags never count for a later one
+  WsHeader h{};
+  if (cudaMemcpy(&h, workspace, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return SSM_ERR_CUDA;
+  const uint32_t next_epoch = h.epoch + 1u;
+  h = WsHeader{};
+  h.epoch = next_epoch;
+  if (cudaMemcpy(workspace, &h, sizeof(h), cudaMemcpyHostToDevice) != cudaSuccess) return SSM_ERR_CUDA;
   const uint32_t code = (uint32_t)(word & 0xffffffffu);
   return code == 0 ? SSM_ERR_CUDA : static_cast<ssm_status>(code);
 }

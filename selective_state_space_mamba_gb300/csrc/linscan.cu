@@ -245,11 +245,12 @@ __device__ void ls_store_warp(LsShared& sh, const CUtensorMap* map_h, const Lins
 __global__ void __launch_bounds__(kLsBlock, SSM_LS_MIN_BLOCKS)
     linscan_lookback_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                             const __grid_constant__ CUtensorMap map_h, LsArgs p, LinscanWorkspace ws,
-                            LookbackCtl ctl) {
+                            LookbackCtl ctl_call) {
   extern __shared__ unsigned char ls_smem_raw[];
   // align the stage ring to the 1024-byte swizzle atom (the launch adds 1 KB of slack)
   const uint32_t raw = smem_addr(ls_smem_raw);
   LsShared& sh = *reinterpret_cast<LsShared*>(ls_smem_raw + ((1024u - (raw & 1023u)) & 1023u));
+  const LookbackCtl ctl = device_epoch(ctl_call, ws.hdr);
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int t = threadIdx.x;                           // consumer thread

@@ -283,7 +283,8 @@ template <bool kWarp>
 __global__ void __launch_bounds__(kLbThreads) scan_lookback_kernel(const float* __restrict__ a,
                                                                    const float* __restrict__ b, float* __restrict__ h,
                                                                    int64_t n, int64_t len, LsDesc* desc,
-                                                                   WsHeader* hdr, LookbackCtl ctl) {
+                                                                   WsHeader* hdr, LookbackCtl ctl_call) {
+  const LookbackCtl ctl = device_epoch(ctl_call, hdr);
   __shared__ Aff warp_tot[kLbThreads / 32];
   __shared__ int64_t s_tile;
   __shared__ float s_x;

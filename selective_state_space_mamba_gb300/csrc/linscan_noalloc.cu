@@ -5,6 +5,8 @@
 // allocation.  It launches exactly the kernel ssm_linscan_fwd launches.
 #include <mutex>
 
+#include <cstddef>
+
 #include "ssm_internal.cuh"
 
 namespace ssm {
@@ -59,9 +61,9 @@ extern "C" ssm_status ssm_linscan_fwd_noalloc(const float* a, const float* b, fl
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return SSM_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // The header (status word, claim counters) must start at zero; descriptors carry a per-call
-  // tag, so whatever an earlier call left in them is ignored.
-  if (cudaMemsetAsync(scratch, 0, sizeof(WsHeader), s) != cudaSuccess) return SSM_ERR_CUDA;
+  // The status word and claim counters must start at zero.  The flag epoch after them is left
+  // alone: each launch advances it, so descriptors an earlier call left are ignored.
+  if (cudaMemsetAsync(scratch, 0, offsetof(WsHeader, epoch), s) != cudaSuccess) return SSM_ERR_CUDA;
   const LinscanWorkspace ws = linscan_workspace_layout(n, scratch);
   if (launch_linscan(a, b, h, rows, len, ws, next_lookback_ctl(), s) != cudaSuccess) return SSM_ERR_CUDA;
   return SSM_OK;

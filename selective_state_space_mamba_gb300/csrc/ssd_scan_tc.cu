@@ -607,8 +607,7 @@ cudaError_t launch_ssd_chunk_scan_tc(const void* x, const void* B, const void* C
   }
   const ScLayout L(d.chunk);
   const size_t smem = L.total + 1024;
-  if ((e = cudaFuncSetAttribute(ssd_chunk_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-      cudaSuccess)
+  if ((e = ensure_smem_limit(reinterpret_cast<const void*>(ssd_chunk_scan_tc_kernel), smem)) != cudaSuccess)
     return e;
   const int64_t grid = tiles * p.items_per_tile;
   return launch_pdl(ssd_chunk_scan_tc_kernel, dim3((unsigned)grid), dim3(kScThreads), smem, s, map_c, map_b, map_x,

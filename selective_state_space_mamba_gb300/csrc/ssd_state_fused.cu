@@ -390,8 +390,7 @@ cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float*
   p.chunk = d.chunk;
   const SfLayout L;
   const size_t smem = L.total + 1024;
-  if ((e = cudaFuncSetAttribute(ssd_state_fused_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-      cudaSuccess)
+  if ((e = ensure_smem_limit(reinterpret_cast<const void*>(ssd_state_fused_tc_kernel), smem)) != cudaSuccess)
     return e;
   const int64_t chains = d.batch * (int64_t)(d.nheads / 2);
   return launch_pdl(ssd_state_fused_tc_kernel, dim3((unsigned)chains), dim3(kSfThreads), smem, s, map_x, map_b, p, ctl);

@@ -44,11 +44,12 @@ template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16*
 template <typename HinT>
 __global__ void __launch_bounds__(kSpThreads) ssd_state_passing_kernel(const float* __restrict__ h0,
                                                                         float* __restrict__ h_final, SsdDims d,
-                                                                        SsdWorkspace ws, LookbackCtl ctl) {
+                                                                        SsdWorkspace ws, LookbackCtl ctl_call) {
   __shared__ uint32_t s_tile;
   __shared__ int s_last, s_found;
   griddep_launch_dependents();
   griddep_wait();  // S_c, G and the claim counter come from the previous kernels
+  const LookbackCtl ctl = device_epoch(ctl_call, ws.hdr);
 
   if (threadIdx.x == 0) s_tile = claim_tile(ws.hdr);
   __syncthreads();

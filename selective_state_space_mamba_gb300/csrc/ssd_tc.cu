@@ -412,8 +412,7 @@ cudaError_t launch_ssd_chunk_state_tc(const void* x, const void* B, const SsdDim
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const CsLayout L(d.chunk);
   const size_t smem = L.total + 1024;
-  if ((e = cudaFuncSetAttribute(ssd_chunk_state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-      cudaSuccess)
+  if ((e = ensure_smem_limit(reinterpret_cast<const void*>(ssd_chunk_state_tc_kernel), smem)) != cudaSuccess)
     return e;
   // one CTA per SM (shared memory allows no second), each with an equal share of the units
   const int64_t grid = p.units < sms ? p.units : sms;

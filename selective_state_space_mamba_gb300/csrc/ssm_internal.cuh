@@ -20,12 +20,14 @@ struct WsHeader {
   unsigned long long status;  // (epoch << 32) | code
   uint32_t counter;           // look-back tile claim counter
   uint32_t done;              // tiles finished (the last one resets both counters)
+  uint32_t epoch;             // flag epoch of the next look-back launch on this workspace
+  uint32_t pad;
 };
 constexpr size_t kHeaderBytes = 256;
 
 // Look-back fault injection and wait limit (test hook), passed by value to each kernel.
 struct LookbackCtl {
-  uint32_t epoch;         // 30-bit call tag, never 0
+  uint32_t epoch;         // call tag (kernels with look-back flags replace it, see device_epoch)
   int64_t stall_tile;     // claim index that never publishes (-1: none)
   uint64_t spin_limit_ns; // per-wait limit
 };
@@ -253,14 +255,25 @@ cudaError_t encode_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dtype, co
 __device__ __forceinline__ uint32_t claim_tile(WsHeader* hdr) { return atomicAdd(&hdr->counter, 1u); }
 
 // Called by thread 0 of every CTA after its last global access: the CTA that finishes last
-// resets the claim counters so the workspace is ready for the next call.
+// resets the claim counters so the workspace is ready for the next call, and moves the flag
+// epoch on, so that the flags this launch left can never pass for the next launch's.
 __device__ __forceinline__ void retire_tile(WsHeader* hdr, uint32_t n_tiles) {
   __threadfence();
   uint32_t d = atomicAdd(&hdr->done, 1u);
   if (d == n_tiles - 1u) {
     atomicExch(&hdr->counter, 0u);
     atomicExch(&hdr->done, 0u);
+    atomicAdd(&hdr->epoch, 1u);
   }
+}
+
+// A look-back launch tags its flags with the epoch kept in the workspace, not with the host's
+// per-call tag: a launch replayed from a CUDA graph then still gets a fresh epoch (the previous
+// launch's last CTA advanced it after every CTA of that launch had read it).  Read after the
+// previous kernel has finished (griddep_wait where the launch uses programmatic dependence).
+__device__ __forceinline__ LookbackCtl device_epoch(LookbackCtl c, const WsHeader* hdr) {
+  c.epoch = *reinterpret_cast<const volatile uint32_t*>(&hdr->epoch);
+  return c;
 }
 
 __device__ __forceinline__ float to_f32(float v) { return v; }
@@ -334,6 +347,11 @@ constexpr int kLsThreads = kLsLines * kLsSplit;       // consumer threads
 constexpr int kLsTile = kLsLines * kLsRow;            // elements per tile
 constexpr int kLsStages = SSM_LS_STAGES;              // shared-memory stages of the producer ring
 LinscanWorkspace linscan_workspace_layout(int64_t n, void* base);
+
+// Raises `func`'s dynamic shared-memory limit to at least `bytes` on the current device, with
+// one attribute call per device and size: later launches (for example while a stream is
+// being captured into a CUDA graph) make none.
+cudaError_t ensure_smem_limit(const void* func, size_t bytes);
 
 // Launchers (return a CUDA error code; 0 = success).
 cudaError_t launch_linscan(const float* a, const float* b, float* h, int64_t rows, int64_t len,
