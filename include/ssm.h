@@ -44,6 +44,12 @@
  *     concurrently (different streams without ordering).
  *   - Not thread-safe per workspace; different workspaces may be used from different host
  *     threads.
+ *   - Every call can be captured into a CUDA graph and replayed (nothing is allocated or
+ *     synchronized; the look-back flags carry an epoch kept in the workspace that each launch
+ *     advances).  Make one ordinary call per device and shape before capturing, so that
+ *     one-time set-up (kernel attributes, the no-alloc scratch address) happens outside the
+ *     capture.  ssm_ssd_fwd_tune and ssm_check_device_status synchronize and cannot be
+ *     captured.
  */
 #ifndef SSM_GB300_H
 #define SSM_GB300_H
