@@ -121,3 +121,22 @@ def test_bounded_wait_timeout(cuda_lib):
     h = P.to_np(ssm.linscan_fwd(ta, tb))
     assert ssm.check_device_status(kind="linscan") == 0
     P.assert_rows_close(h, native.linscan(inp["a"], inp["b"]), "after timeout")
+
+
+def test_many_rows_bounded_wait_timeout(cuda_lib):
+    """The same on many ragged rows (400 x 5000: look-back tiles that straddle rows and stop at
+    row starts): a tile that never publishes makes its successors in the row give up after the
+    limit and report SSM_ERR_TIMEOUT, and the next call is clean."""
+    import selective_state_space_mamba_gb300 as ssm
+    from selective_state_space_mamba_gb300 import _lib
+    inp = synth.scan_inputs(400, 5000, seed=4)
+    ta, tb = P.to_dev(inp["a"]), P.to_dev(inp["b"])
+    try:
+        ssm.debug_set_lookback_fault(stall_tile=5, spin_limit_ns=20_000_000)
+        ssm.linscan_fwd(ta, tb)
+        assert ssm.check_device_status(kind="linscan") == _lib.SSM_ERR_TIMEOUT
+    finally:
+        ssm.debug_set_lookback_fault(-1, 0)
+    h = P.to_np(ssm.linscan_fwd(ta, tb))
+    assert ssm.check_device_status(kind="linscan") == 0
+    P.assert_rows_close(h, native.linscan(inp["a"], inp["b"]), "after timeout")
