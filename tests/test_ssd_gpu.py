@@ -76,6 +76,11 @@ for dtype in ("f32", "bf16"):
     for (L, T) in [(1, 64), (63, 64), (64, 64), (65, 64), (300, 128), (1000, 256), (777, 64)]:
         for S, G, nh in [(64, 1, 2), (128, 2, 4)]:
             SMALL.append(synth.SSDShape(f"{dtype}_L{L}_T{T}_S{S}_G{G}", 2, L, nh, 64, S, G, T, dtype, h0=True))
+# odd numbers of heads per group: no head pairs for the tensor-core chunk state (its FMA
+# path runs, next to the tensor-core chunk scan for bf16), and one head per group
+for dtype in ("f32", "bf16"):
+    for (L, T, S, G, nh) in [(700, 256, 128, 1, 3), (300, 128, 128, 3, 9), (129, 64, 64, 5, 5)]:
+        SMALL.append(synth.SSDShape(f"{dtype}_L{L}_T{T}_S{S}_G{G}_nh{nh}", 2, L, nh, 64, S, G, T, dtype, h0=True))
 
 
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: s.name)
