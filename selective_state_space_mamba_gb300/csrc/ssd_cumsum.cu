@@ -9,9 +9,11 @@
 //
 // One CTA per (chunk, block of 8 heads, batch): the dt tile [chunk, 8 heads] is staged
 // through shared memory so both the read (heads contiguous) and the writes (tokens
-// contiguous) are coalesced: each warp scans whole head rows in registers, and the results
-// go back through the same shared tile, so that every warp store writes 128 contiguous bytes
-// of one head row.
+// contiguous) are coalesced: each warp scans whole head rows in registers and writes each
+// row of dt^T and G straight from them.  The tile is stored head-major with one padding word after every 8 tokens
+// and a row stride of 4 (mod 32) words, so that both the scan's reads (each lane reads a run
+// of consecutive tokens of one head) and the initial writes (8 heads x 4 tokens per warp) see
+// at most 2-way bank conflicts.
 #include "ssm_internal.cuh"
 
 namespace ssm {
@@ -38,17 +40,22 @@ __device__ __forceinline__ uint32_t ld_bits(const float* p) {
   return v;
 }
 
+// shared-memory word of (token t, local head h); row stride T + T / 8 + 4
+__device__ __forceinline__ int sidx(int t, int h, int row) { return h * row + t + (t >> 3); }
+__host__ __device__ __forceinline__ int s_row(int T) { return T + T / 8 + 4; }
+
 template <typename DtT>
 __global__ void __launch_bounds__(kCsThreads) ssd_chunk_cumsum_kernel(const DtT* __restrict__ dt,
                                                                        const float* __restrict__ A, SsdDims d,
                                                                        float* __restrict__ G, float* __restrict__ dtT,
                                                                        WsHeader* hdr) {
-  extern __shared__ float s_dt[];  // [chunk][kCsHeads + 1]
+  extern __shared__ float s_dt[];  // [kCsHeads][chunk + chunk / 8 + 4], see sidx
   griddep_launch_dependents();
   griddep_wait();  // dt may come from, and G / dtT may still be read by, the previous kernel
   const int c = blockIdx.x, hblk = blockIdx.y;
   const int64_t bi = blockIdx.z;
   const int T = d.chunk, nh = d.nheads;
+  const int srow = s_row(T);
   const int h0 = hblk * kCsHeads;
   const int nhb = min(kCsHeads, nh - h0);
   const int64_t t0 = (int64_t)c * T;
@@ -83,21 +90,26 @@ __global__ void __launch_bounds__(kCsThreads) ssd_chunk_cumsum_kernel(const DtT*
 #pragma unroll
   for (int k = 0; k < kCsLoads; ++k) {
     const int t = lt + kTokStride * k;
-    if (t < T) s_dt[t * (kCsHeads + 1) + lh] = __uint_as_float(raw[k]);
+    if (t < T) s_dt[sidx(t, lh, srow)] = __uint_as_float(raw[k]);
   }
   __syncthreads();
 
+  // Each warp scans whole head rows: lane l holds tokens l * per_lane .. + per_lane - 1, so
+  // after the scan it writes its run of the dt^T row and of the G row directly (8 to 32
+  // contiguous bytes per lane, one contiguous row per warp).
   const int per_lane = T / 32;  // chunk is a multiple of 64 and at most 256
-  float gv[kCsHeadsPerWarp][8];
 #pragma unroll
   for (int q = 0; q < kCsHeadsPerWarp; ++q) {
     const int hh = warp + q * kCsWarps;
+    float dv[8], gv[8];
     float run = 0.f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
+      dv[k] = 0.f;
       if (k < per_lane) {
-        run += Ah[q] * s_dt[(lane * per_lane + k) * (kCsHeads + 1) + hh];
-        gv[q][k] = run;
+        dv[k] = s_dt[sidx(lane * per_lane + k, hh, srow)];
+        run += Ah[q] * dv[k];
+        gv[k] = run;
       }
     }
     // exclusive prefix of the lane totals
@@ -109,36 +121,23 @@ __global__ void __launch_bounds__(kCsThreads) ssd_chunk_cumsum_kernel(const DtT*
     }
     const float excl = incl - run;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) gv[q][k] = (excl + gv[q][k]) * kLog2e;
-  }
-
-  // dt^T rows, then G rows: each warp store writes 32 consecutive tokens of one head
-  auto store_rows = [&](float* dst) {
+    for (int k = 0; k < 8; ++k) gv[k] = (excl + gv[k]) * kLog2e;
+    if (hh < nhb) {
+      const int64_t off = (bi * nh + h0 + hh) * d.lpad + t0 + lane * per_lane;
+      if (per_lane == 2) {
+        *reinterpret_cast<float2*>(dtT + off) = make_float2(dv[0], dv[1]);
+        *reinterpret_cast<float2*>(G + off) = make_float2(gv[0], gv[1]);
+      } else {
 #pragma unroll
-    for (int q = 0; q < kCsHeadsPerWarp; ++q) {
-      const int hh = warp + q * kCsWarps;
-      if (hh < nhb) {
-        float* row = dst + (bi * nh + h0 + hh) * d.lpad + t0;
-        float v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = 32 * k < T ? s_dt[(lane + 32 * k) * (kCsHeads + 1) + hh] : 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (32 * k < T) row[lane + 32 * k] = v[k];
+        for (int k = 0; k < 8; k += 4) {
+          if (k < per_lane) {
+            *reinterpret_cast<float4*>(dtT + off + k) = make_float4(dv[k], dv[k + 1], dv[k + 2], dv[k + 3]);
+            *reinterpret_cast<float4*>(G + off + k) = make_float4(gv[k], gv[k + 1], gv[k + 2], gv[k + 3]);
+          }
+        }
       }
     }
-  };
-  store_rows(dtT);
-  __syncthreads();
-#pragma unroll
-  for (int q = 0; q < kCsHeadsPerWarp; ++q) {
-    const int hh = warp + q * kCsWarps;
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      if (k < per_lane) s_dt[(lane * per_lane + k) * (kCsHeads + 1) + hh] = gv[q][k];
   }
-  __syncthreads();
-  store_rows(G);
 }
 
 }  // namespace
@@ -146,7 +145,7 @@ __global__ void __launch_bounds__(kCsThreads) ssd_chunk_cumsum_kernel(const DtT*
 cudaError_t launch_ssd_chunk_cumsum(const void* dt, const float* A, const SsdDims& d, const SsdWorkspace& ws,
                                     cudaStream_t s) {
   dim3 grid((unsigned)d.nchunks, (unsigned)((d.nheads + kCsHeads - 1) / kCsHeads), (unsigned)d.batch);
-  const size_t smem = sizeof(float) * d.chunk * (kCsHeads + 1);
+  const size_t smem = sizeof(float) * kCsHeads * s_row(d.chunk);
   if (d.dtype == SSM_BF16)
     return launch_pdl(ssd_chunk_cumsum_kernel<__nv_bfloat16>, grid, dim3(kCsThreads), smem, s,
                       static_cast<const __nv_bfloat16*>(dt), A, d, ws.G, ws.dtT, ws.hdr);
