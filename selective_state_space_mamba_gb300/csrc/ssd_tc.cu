@@ -34,9 +34,11 @@
 //               TMEM, into one of two 128-column f32 accumulators; tcgen05.commit frees the
 //               stage (its X in shared memory and its hi/lo columns in TMEM), and after the
 //               last stage of a unit hands the accumulator to the epilogue
-//   warps 2-9   one row p of one head per thread (its TMEM lane) and half the stage's tokens:
-//               64 threads first tabulate the bf16 weight pairs of the stage's token pairs,
-//               then every thread turns its 32 values of X into 16 hi and 16 lo columns
+//   warps 2-9   two groups of four warps that take alternate stages, so that one group's
+//               chain (wait, table, loads, split, TMEM store) overlaps the other's; in a group
+//               one row p of one head per thread (its TMEM lane): 64 threads first tabulate
+//               the bf16 weight pairs of the stage's token pairs, then every thread turns its
+//               64 values of X into 32 hi and 32 lo columns
 //   warps 10-13 epilogue: TMEM -> registers -> a swizzled 32 x 32 f32 block per warp in shared
 //               memory -> TMA store into S_c; the accumulator is freed after its last TMEM load
 // Every wait is bounded; on expiry the CTA records SSM_ERR_TIMEOUT, drains, frees its TMEM
@@ -53,7 +55,7 @@ constexpr int kCsKH = 64;         // tokens per stage
 constexpr int kCsStages = 8;   // X ring in shared memory (released once the scalers have read it)
 constexpr int kCsAStages = 4;  // hi/lo ring in TMEM (released when the MMAs have read it)
 constexpr int kCsRowBytes = 128;  // 64 bf16 per swizzled row
-constexpr uint32_t kCsScaleBar = 1, kCsEpiBar = 2;
+constexpr uint32_t kCsScaleBar = 1, kCsEpiBar = 2;  // scaler group g uses named barrier 1 + 2 g
 constexpr uint32_t kCsTmemCols = 512;  // two 128-column accumulators, then 64 A columns per stage
 constexpr uint32_t kCsTmemA = 256;     // hi of A stage a at kCsTmemA + 64 a, lo 32 columns later
 // per stage and head: G of the stage's tokens, dt of the stage's tokens, the chunk's last 4 G
@@ -248,9 +250,10 @@ __global__ void __launch_bounds__(kCsThreads, 1)
     }
   } else if (warp < 10) {
     // ---------------- scale X by w, split into bf16 hi + lo parts, into TMEM ----------------
-    const int st_t = threadIdx.x - 64;     // 0..255
+    const int grp = (warp - 2) >> 2;       // this group takes the steps i with i % 2 == grp
+    const int gt = threadIdx.x - 64 - 128 * grp;  // 0..127 within the group
+    const uint32_t gbar = kCsScaleBar + 2 * grp;
     const int quad = warp & 3;             // TMEM lanes 32 quad .. +31
-    const int half = (warp - 2) >> 2;      // tokens 32 half .. 32 half + 31 of the stage
     const int hh = quad >> 1;              // rows 0..63: head 0, rows 64..127: head 1
     const int prow = (quad & 1) * 32 + lane;  // this thread's p within its head
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
@@ -258,21 +261,22 @@ __global__ void __launch_bounds__(kCsThreads, 1)
     bool ok = true;
     for (int64_t u = u_begin; u < u_end && ok; ++u) {
       for (int kh = 0; kh < nk; ++kh, ++i) {
+        if ((int)(i & 1) != grp) continue;
         const int st = (int)(i % kCsStages), as = (int)(i % kCsAStages);
         // X of step i has landed, and the MMAs of step i - 4 have read this A stage's columns
         const bool bad =
             !mbar_wait(&bars[kXFull + st], (uint32_t)(i / kCsStages) & 1u, ctl.spin_limit_ns) ||
             (i >= kCsAStages &&
              !mbar_wait(&bars[kAEmpty + as], (uint32_t)((i / kCsAStages) - 1) & 1u, ctl.spin_limit_ns));
-        if (named_bar_any(kCsScaleBar, 256, bad)) {  // leave together, or not at all
-          if (st_t == 0) fail();
+        if (named_bar_any(gbar, 128, bad)) {  // leave together, or not at all
+          if (gt == 0) fail();
           ok = false;
           break;
         }
         tc::fence_after_sync();
         uint4* wt = reinterpret_cast<uint4*>(base + L.wt0) + as * 2 * (kCsKH / 2);
-        if (st_t < 2 * (kCsKH / 2)) {  // the bf16 weight pairs of (head, token pair)
-          const int wh = st_t / (kCsKH / 2), pr = st_t % (kCsKH / 2);
+        if (gt < 2 * (kCsKH / 2)) {  // the bf16 weight pairs of (head, token pair)
+          const int wh = gt / (kCsKH / 2), pr = gt % (kCsKH / 2);
           const float* gd = reinterpret_cast<const float*>(base + L.gd0 + (st * 2 + wh) * kCsGdHead);
           const float glast = gd[2 * kCsKH + 3];
           const float w0 = gd[kCsKH + 2 * pr] * tc::ex2_approx(glast - gd[2 * pr]);
@@ -283,30 +287,33 @@ __global__ void __launch_bounds__(kCsThreads, 1)
           const uint32_t whi2 = *reinterpret_cast<const uint32_t*>(&whi);
           wt[wh * (kCsKH / 2) + pr] = make_uint4(whi2, whi2 ^ 0x80008000u, *reinterpret_cast<const uint32_t*>(&nwlo), 0u);
         }
-        named_bar_sync(kCsScaleBar, 256);
-        // my row p of head hh: tokens 32 half + 2 j and + 2 j + 1 form TMEM column 16 half + j
+        named_bar_sync(gbar, 128);
+        // my row p of head hh: tokens 2 j and 2 j + 1 form TMEM column j of the A stage
         const unsigned char* xh = base + st * L.stage_bytes + hh * kCsKH * kCsRowBytes;
         const int cpos = (prow >> 3), cin = (prow & 7) * 2;  // 16-byte chunk and byte within it
-        uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int t0 = 32 * half + 2 * j, t1 = t0 + 1;
-          const uint32_t x0 = *reinterpret_cast<const uint16_t*>(xh + t0 * kCsRowBytes + ((cpos ^ (t0 & 7)) << 4) + cin);
-          const uint32_t x1 = *reinterpret_cast<const uint16_t*>(xh + t1 * kCsRowBytes + ((cpos ^ (t1 & 7)) << 4) + cin);
-          const uint32_t x2 = x0 | (x1 << 16);
-          const uint4 w = wt[hh * (kCsKH / 2) + 16 * half + j];
-          const uint32_t h2 = fma_bf16x2(x2, w.x, 0x80008000u);  // x w_hi, rounded
-          const uint32_t d2 = fma_bf16x2(x2, w.y, h2);           // hi - x w_hi, exact
-          lo[j] = fma_bf16x2(x2, w.z, d2) ^ 0x80008000u;         // x w - hi, rounded
-          hi[j] = h2;
+        for (int half = 0; half < 2; ++half) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t0 = 32 * half + 2 * j, t1 = t0 + 1;
+            const uint32_t x0 = *reinterpret_cast<const uint16_t*>(xh + t0 * kCsRowBytes + ((cpos ^ (t0 & 7)) << 4) + cin);
+            const uint32_t x1 = *reinterpret_cast<const uint16_t*>(xh + t1 * kCsRowBytes + ((cpos ^ (t1 & 7)) << 4) + cin);
+            const uint32_t x2 = x0 | (x1 << 16);
+            const uint4 w = wt[hh * (kCsKH / 2) + 16 * half + j];
+            const uint32_t h2 = fma_bf16x2(x2, w.x, 0x80008000u);  // x w_hi, rounded
+            const uint32_t d2 = fma_bf16x2(x2, w.y, h2);           // hi - x w_hi, exact
+            lo[j] = fma_bf16x2(x2, w.z, d2) ^ 0x80008000u;         // x w - hi, rounded
+            hi[j] = h2;
+          }
+          const uint32_t a_hi = tmem + lane_base + kCsTmemA + 64u * as + 16u * half;
+          tc::tmem_st16(a_hi, hi);
+          tc::tmem_st16(a_hi + 32, lo);
         }
-        const uint32_t a_hi = tmem + lane_base + kCsTmemA + 64u * as + 16u * half;
-        tc::tmem_st16(a_hi, hi);
-        tc::tmem_st16(a_hi + 32, lo);
         tc::tmem_st_wait();
         tc::fence_before_sync();
-        named_bar_sync(kCsScaleBar, 256);
-        if (st_t == 0) {
+        named_bar_sync(gbar, 128);
+        if (gt == 0) {
           mbar_arrive(&bars[kXEmpty + st]);  // X and G/dt of step i are read: refill the stage
           mbar_arrive(&bars[kAFull + as]);   // hi and lo of step i are in TMEM
         }
