@@ -5,9 +5,16 @@
 //     h_in[0] = h0,   h_in[c+1] = 2^(G_last[c]) h_in[c] + X_c^T (w_c . B_c),   h_final = h_in[nc]
 // with w_t = dt_t 2^(G_last - G_t) inside chunk c.
 //
-// One CTA walks the chunks of one (batch, head pair) in order.  The pair's rows (2 heads x 64 p
-// = 128 TMEM lanes, x 128 s columns, f32) have three TMEM homes: the running state h and two
-// accumulators S[0], S[1].  The MMAs add chunk c's weighted X^T B into S[c & 1] without
+// A chain is the chunks of one (batch, head pair), walked in order.  The CTAs take contiguous,
+// equal ranges of the (chain, chunk) units, chain-major: one chain each when there are no more
+// chains than SMs, else one CTA per SM and ranges of at least one chain's length, so that a
+// range holds at most the tail of one chain, whole chains and the head of one more.  A CTA
+// runs the head first and publishes the state where it stops (f32, with a flag), then the
+// whole chains, then the tail, which starts from the state the previous CTA published for
+// that chain: the previous CTA ran that head first, and its head is shorter than what this
+// CTA runs before its tail by the range length minus the chain length, so the wait is short.
+// The pair's rows (2 heads x 64 p = 128 TMEM lanes, x 128 s columns, f32) have three TMEM
+// homes: the running state h and two accumulators S[0], S[1].  The MMAs add chunk c's weighted X^T B into S[c & 1] without
 // waiting for the state; the state warps then write h out as h_in[c] (bf16), fold S[c & 1] in
 // (h = 2^(G_last) h + S) and release the accumulator for chunk c + 2.  The weighted X is split
 // into bf16 hi + lo halves exactly as in ssd_chunk_state_tc, so the state keeps f32 accuracy.
@@ -20,8 +27,9 @@
 //   warp 1     TMEM owner and MMA issuer (one thread): per chunk, once S[c & 1] is free,
 //              2 x 4 MMAs (hi, lo) per step accumulating into it
 //   warps 2-9  scalers: half a token row per thread, x w -> hi (in place) + lo
-//   warps 10-13 state warps, one state row per thread: h0 in, h_in out per chunk, the decay and
-//              S folded in, h_final at the end
+//   warps 10-13 state warps, one state row per thread: h0 or the published state in, h_in out
+//              per chunk, the decay and S folded in, h_final at a chain's end, the state
+//              published where a head ends
 // Every wait is bounded; on expiry the CTA records SSM_ERR_TIMEOUT, drains, frees its TMEM and
 // returns.
 #include "tc_common.cuh"
@@ -43,10 +51,67 @@ struct SfParams {
   const float* h0;   // [b, nh, 64, 128] f32 or null (zeros)
   __nv_bfloat16* hin;  // [b, nc, nh, 64, 128]
   float* h_final;    // [b, nh, 64, 128] or null
+  float* carry;      // [chains][128 rows][128] f32: the state where a chain's head ends
+  unsigned long long* flags;  // [chains]: carry published (epoch-tagged)
   WsHeader* hdr;
-  int64_t lpad, nchunks;
+  int64_t lpad, nchunks, units;  // units = chains x nchunks
   int nheads, ngroups, chunk;
 };
+
+// This CTA's units [u0, u1) of (chain, chunk), chain-major, as segments in the order they run:
+// the head that ends inside the range (publishes its final state), whole chains, the tail
+// that starts inside the range (starts from the published state).  A range is never inside
+// one chain (ranges are at least one chain long where a chain is split).
+struct SfRange {
+  int64_t first_chain, last_chain, full_begin;
+  int c_first, c_last_end, nfull, nseg;
+  bool has_tail, has_head;
+};
+struct SfSeg {
+  int64_t chain;
+  int c0, c1;
+  bool from_carry, to_carry;
+};
+__device__ __forceinline__ SfRange sf_range(int64_t u0, int64_t u1, int64_t nc) {
+  SfRange r;
+  r.first_chain = u0 / nc;
+  r.c_first = (int)(u0 % nc);
+  r.last_chain = (u1 - 1) / nc;
+  r.c_last_end = (int)((u1 - 1) % nc) + 1;
+  r.has_tail = r.c_first > 0;
+  r.has_head = r.c_last_end < nc;
+  r.full_begin = r.first_chain + (r.has_tail ? 1 : 0);
+  const int64_t full_end = r.last_chain + (r.has_head ? 0 : 1);
+  r.nfull = full_end > r.full_begin ? (int)(full_end - r.full_begin) : 0;
+  r.nseg = (r.has_head ? 1 : 0) + r.nfull + (r.has_tail ? 1 : 0);
+  return r;
+}
+__device__ __forceinline__ SfSeg sf_seg(const SfRange& r, int s, int64_t nc) {
+  SfSeg g;
+  if (r.has_head) {
+    if (s == 0) {
+      g.chain = r.last_chain;
+      g.c0 = 0;
+      g.c1 = r.c_last_end;
+      g.from_carry = false;
+      g.to_carry = true;
+      return g;
+    }
+    --s;
+  }
+  if (s < r.nfull) {
+    g.chain = r.full_begin + s;
+    g.c0 = 0;
+    g.c1 = (int)nc;
+  } else {
+    g.chain = r.first_chain;
+    g.c0 = r.c_first;
+    g.c1 = (int)nc;
+  }
+  g.from_carry = s >= r.nfull;
+  g.to_carry = false;
+  return g;
+}
 
 // Shared memory (offsets from a 1024-byte aligned base):
 //   stage[2] = { hi[2 heads][64 rows][128 B], lo[2 heads][64 rows][128 B],
@@ -86,7 +151,7 @@ __device__ __forceinline__ uint32_t sf_pack(float lo, float hi) {
 
 __global__ void __launch_bounds__(kSfThreads, 1)
     ssd_state_fused_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_b,
-                              SfParams p, LookbackCtl ctl) {
+                              SfParams p, LookbackCtl ctl_call) {
   extern __shared__ unsigned char sf_raw[];
   griddep_launch_dependents();
   const uint32_t raw = smem_addr(sf_raw);
@@ -99,14 +164,15 @@ __global__ void __launch_bounds__(kSfThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.bars + 24 * 8 + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // chain -> (batch, group, pair)
   const int hpg = p.nheads / p.ngroups, ppg = hpg / 2;
-  const int pair = (int)(blockIdx.x % ppg);
-  const int g = (int)((blockIdx.x / ppg) % p.ngroups);
-  const int64_t bi = blockIdx.x / ((int64_t)ppg * p.ngroups);
-  const int h = g * hpg + 2 * pair;  // first head of the pair
   const int64_t nc = p.nchunks;
-  const int64_t nsteps = nc * nk;
+  const int64_t u0 = (int64_t)blockIdx.x * p.units / gridDim.x;
+  const int64_t u1 = (int64_t)(blockIdx.x + 1) * p.units / gridDim.x;
+  const SfRange rg = nc > 0 && u1 > u0 ? sf_range(u0, u1, nc) : SfRange{0, 0, 0, 0, 0, 0, 0, false, false};
+  // chain -> (batch, group, first head of the pair)
+  auto chain_bi = [&](int64_t z) { return z / ((int64_t)ppg * p.ngroups); };
+  auto chain_g = [&](int64_t z) { return (int)((z / ppg) % p.ngroups); };
+  auto chain_h = [&](int64_t z) { return chain_g(z) * hpg + 2 * (int)(z % ppg); };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kSfNumBars; ++i) mbar_init(&bars[i], 1);
@@ -122,6 +188,8 @@ __global__ void __launch_bounds__(kSfThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   griddep_wait();  // G and dt come from the previous kernel
+  // published states carry this launch's epoch (the last CTA to finish moves it on)
+  const LookbackCtl ctl = device_epoch(ctl_call, p.hdr);
   auto fail = [&](void) {
     record_error(p.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
     *abort_flag = 1;
@@ -132,29 +200,34 @@ __global__ void __launch_bounds__(kSfThreads, 1)
     if (lane == 0) {
       int64_t i = 0;
       bool ok = true;
-      for (; i < nsteps && ok && !*abort_flag; ++i) {
-        const int st = (int)(i % kSfStages);
-        if (i >= kSfStages &&
-            !mbar_wait(&bars[kXEmpty + st], (uint32_t)((i / kSfStages) - 1) & 1u, ctl.spin_limit_ns)) {
-          ok = false;
-          break;
-        }
-        const int64_t c = i / nk;
-        const int kh = (int)(i % nk);
-        const int tok = (int)(c * T + kh * kSfKH);
-        unsigned char* stage = base + st * L.stage_bytes;
-        unsigned char* gd = base + L.gd0 + st * 2 * kSfGdHead;
-        mbar_arrive_expect_tx(&bars[kXFull + st], L.half_bytes + 2u * kSfKH * kSfRowBytes + 2u * kSfGdHead);
-        for (int hh = 0; hh < 2; ++hh)
-          tc::tma_load_3d(stage + hh * kSfKH * kSfRowBytes, &map_x, (h + hh) * 64, tok, (int)bi, &bars[kXFull + st]);
-        for (int sb = 0; sb < 2; ++sb)
-          tc::tma_load_3d(stage + L.b_off + sb * kSfKH * kSfRowBytes, &map_b, g * 128 + sb * 64, tok, (int)bi,
-                          &bars[kXFull + st]);
-        for (int hh = 0; hh < 2; ++hh) {
-          const int64_t row = (bi * p.nheads + h + hh) * p.lpad + c * T;
-          bulk_g2s(gd + hh * kSfGdHead, p.G + row + kh * kSfKH, 4u * kSfKH, &bars[kXFull + st]);
-          bulk_g2s(gd + hh * kSfGdHead + 4u * kSfKH, p.dtT + row + kh * kSfKH, 4u * kSfKH, &bars[kXFull + st]);
-          bulk_g2s(gd + hh * kSfGdHead + 8u * kSfKH, p.G + row + T - 4, 16u, &bars[kXFull + st]);
+      for (int s = 0; s < rg.nseg && ok; ++s) {
+        const SfSeg sg = sf_seg(rg, s, nc);
+        const int64_t bi = chain_bi(sg.chain);
+        const int g = chain_g(sg.chain), h = chain_h(sg.chain);
+        for (int64_t c = sg.c0; c < sg.c1 && ok && !*abort_flag; ++c) {
+          for (int kh = 0; kh < nk; ++kh, ++i) {
+            const int st = (int)(i % kSfStages);
+            if (i >= kSfStages &&
+                !mbar_wait(&bars[kXEmpty + st], (uint32_t)((i / kSfStages) - 1) & 1u, ctl.spin_limit_ns)) {
+              ok = false;
+              break;
+            }
+            const int tok = (int)(c * T + kh * kSfKH);
+            unsigned char* stage = base + st * L.stage_bytes;
+            unsigned char* gd = base + L.gd0 + st * 2 * kSfGdHead;
+            mbar_arrive_expect_tx(&bars[kXFull + st], L.half_bytes + 2u * kSfKH * kSfRowBytes + 2u * kSfGdHead);
+            for (int hh = 0; hh < 2; ++hh)
+              tc::tma_load_3d(stage + hh * kSfKH * kSfRowBytes, &map_x, (h + hh) * 64, tok, (int)bi, &bars[kXFull + st]);
+            for (int sb = 0; sb < 2; ++sb)
+              tc::tma_load_3d(stage + L.b_off + sb * kSfKH * kSfRowBytes, &map_b, g * 128 + sb * 64, tok, (int)bi,
+                              &bars[kXFull + st]);
+            for (int hh = 0; hh < 2; ++hh) {
+              const int64_t row = (bi * p.nheads + h + hh) * p.lpad + c * T;
+              bulk_g2s(gd + hh * kSfGdHead, p.G + row + kh * kSfKH, 4u * kSfKH, &bars[kXFull + st]);
+              bulk_g2s(gd + hh * kSfGdHead + 4u * kSfKH, p.dtT + row + kh * kSfKH, 4u * kSfKH, &bars[kXFull + st]);
+              bulk_g2s(gd + hh * kSfGdHead + 8u * kSfKH, p.G + row + T - 4, 16u, &bars[kXFull + st]);
+            }
+          }
         }
       }
       if (!ok) fail();
@@ -170,11 +243,12 @@ __global__ void __launch_bounds__(kSfThreads, 1)
       const uint32_t sbo = 8 * kSfRowBytes;         // next 8-token group
       bool ok = true;
       int64_t i = 0;
-      for (int64_t c = 0; c < nc && ok && !*abort_flag; ++c) {
-        const int sb = (int)(c & 1);
+      const int64_t nq = u1 - u0;  // chunks this CTA runs, in order (the accumulators alternate)
+      for (int64_t q = 0; q < nq && ok && !*abort_flag; ++q) {
+        const int sb = (int)(q & 1);
         const uint32_t acc = tmem + 128u + 128u * sb;
-        // the state warps have folded S[sb] (chunk c - 2) into the state
-        if (c >= 2 && !mbar_wait(&bars[kSFree + sb], (uint32_t)(((c - 2) >> 1) & 1), ctl.spin_limit_ns)) {
+        // the state warps have folded S[sb] (the chunk run two before) into the state
+        if (q >= 2 && !mbar_wait(&bars[kSFree + sb], (uint32_t)(((q - 2) >> 1) & 1), ctl.spin_limit_ns)) {
           ok = false;
           break;
         }
@@ -197,7 +271,7 @@ __global__ void __launch_bounds__(kSfThreads, 1)
           }
           tc::mma_commit(&bars[kXEmpty + st]);  // the stage may be refilled
         }
-        if (ok) tc::mma_commit(&bars[kSReady + sb]);  // S[sb] holds chunk c
+        if (ok) tc::mma_commit(&bars[kSReady + sb]);  // S[sb] holds chunk q
       }
       if (!ok) fail();
       tc::mma_commit(&bars[kDone]);
@@ -209,6 +283,7 @@ __global__ void __launch_bounds__(kSfThreads, 1)
     const int t = st_t >> 1;            // token row of the step: head t / 64, token t % 64
     const int part = st_t & 1;          // which half of the row's eight 16-byte chunks
     const int hh = t / kSfKH, tok = t % kSfKH;
+    const int64_t nsteps = (u1 - u0) * nk;
     for (int64_t i = 0; i < nsteps; ++i) {
       const int st = (int)(i % kSfStages);
       const bool bad = !mbar_wait(&bars[kXFull + st], (uint32_t)(i / kSfStages) & 1u, ctl.spin_limit_ns);
@@ -254,71 +329,107 @@ __global__ void __launch_bounds__(kSfThreads, 1)
     const int m = quad * 32 + lane;  // state row: head h + m / 64, p = m % 64
     const int hh = m >> 6, pp = m & 63;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    const int64_t bh = bi * p.nheads + h + hh;
-    const float* h0r = p.h0 ? p.h0 + (bh * 64 + pp) * 128 : nullptr;
-    const float* Glast = p.G + bh * p.lpad + (T - 1);  // G_last of chunk c at Glast[c * T]
-    for (int64_t c = 0; c < nc; ++c) {
-      const int sb = (int)(c & 1);
-      const bool bad = !mbar_wait(&bars[kSReady + sb], (uint32_t)((c >> 1) & 1), ctl.spin_limit_ns);
-      if (named_bar_any(kSfStateBar, 128, bad)) {  // S[sb] holds chunk c
-        if (m == 0) fail();
-        break;
-      }
-      tc::fence_after_sync();
-      const float dec = exp2f(Glast[c * T]);  // decay over chunk c
-      __nv_bfloat16* hr = p.hin + (((bi * nc + c) * p.nheads + h + hh) * 64 + pp) * 128;
-      const bool last = c == nc - 1;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {  // 32 columns (s) at a time
-        float v[32];
-        uint32_t sv[32];
-        tc::tmem_ld32(tmem + lane_base + 128u + 128u * sb + 32 * q, sv);
-        if (c == 0) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 f = h0r ? reinterpret_cast<const float4*>(h0r + 32 * q)[j] : make_float4(0.f, 0.f, 0.f, 0.f);
-            v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
-          }
-        } else {
-          uint32_t r[32];
-          tc::tmem_ld32(tmem + lane_base + 32 * q, r);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+    int64_t q = 0;  // chunks run so far (the accumulators alternate)
+    bool ok = true;
+    for (int s = 0; s < rg.nseg && ok; ++s) {
+      const SfSeg sg = sf_seg(rg, s, nc);
+      const int64_t bi = chain_bi(sg.chain);
+      const int h = chain_h(sg.chain);
+      const int64_t bh = bi * p.nheads + h + hh;
+      const float* h0r = p.h0 ? p.h0 + (bh * 64 + pp) * 128 : nullptr;
+      float* cr = p.carry + (sg.chain * 128 + m) * 128;  // this row of the chain's published state
+      const float* Glast = p.G + bh * p.lpad + (T - 1);  // G_last of chunk c at Glast[c * T]
+      if (sg.from_carry) {
+        // the previous CTA ran this chain's head first and published where it stopped
+        bool bad = false;
+        if (m == 0) bad = wait_flag(&p.flags[sg.chain], p.hdr, ctl) != kFlagPrefix;
+        if (named_bar_any(kSfStateBar, 128, bad)) {
+          if (m == 0) fail();
+          ok = false;
+          break;
         }
-        tc::tmem_ld_wait();
-        // h_in[c] (bf16): the state entering chunk c
-        uint4* o = reinterpret_cast<uint4*>(hr + 32 * q);
+      }
+      for (int64_t c = sg.c0; c < sg.c1; ++c, ++q) {
+        const int sb = (int)(q & 1);
+        const bool bad = !mbar_wait(&bars[kSReady + sb], (uint32_t)((q >> 1) & 1), ctl.spin_limit_ns);
+        if (named_bar_any(kSfStateBar, 128, bad)) {  // S[sb] holds chunk c
+          if (m == 0) fail();
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const float dec = exp2f(Glast[c * T]);  // decay over chunk c
+        __nv_bfloat16* hr = p.hin + (((bi * nc + c) * p.nheads + h + hh) * 64 + pp) * 128;
+        const bool chain_end = c == nc - 1, publish = sg.to_carry && c == sg.c1 - 1;
+        const bool first = c == sg.c0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          o[j] = make_uint4(sf_pack(v[8 * j], v[8 * j + 1]), sf_pack(v[8 * j + 2], v[8 * j + 3]),
-                            sf_pack(v[8 * j + 4], v[8 * j + 5]), sf_pack(v[8 * j + 6], v[8 * j + 7]));
-        // the state after chunk c
+        for (int qq = 0; qq < 4; ++qq) {  // 32 columns (s) at a time
+          float v[32];
+          uint32_t sv[32];
+          tc::tmem_ld32(tmem + lane_base + 128u + 128u * sb + 32 * qq, sv);
+          if (first && !sg.from_carry) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = fmaf(dec, v[j], __uint_as_float(sv[j]));
-        if (last) {
-          if (p.h_final) {
-            float4* f = reinterpret_cast<float4*>(p.h_final + (bh * 64 + pp) * 128 + 32 * q);
+            for (int j = 0; j < 8; ++j) {
+              const float4 f = h0r ? reinterpret_cast<const float4*>(h0r + 32 * qq)[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+              v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+            }
+          } else if (first) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 f = ld_relaxed_f4(reinterpret_cast<const float4*>(cr + 32 * qq) + j);
+              v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+            }
+          } else {
+            uint32_t r[32];
+            tc::tmem_ld32(tmem + lane_base + 32 * qq, r);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          }
+          tc::tmem_ld_wait();
+          // h_in[c] (bf16): the state entering chunk c
+          uint4* o = reinterpret_cast<uint4*>(hr + 32 * qq);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            o[j] = make_uint4(sf_pack(v[8 * j], v[8 * j + 1]), sf_pack(v[8 * j + 2], v[8 * j + 3]),
+                              sf_pack(v[8 * j + 4], v[8 * j + 5]), sf_pack(v[8 * j + 6], v[8 * j + 7]));
+          // the state after chunk c
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = fmaf(dec, v[j], __uint_as_float(sv[j]));
+          if (chain_end) {
+            if (p.h_final) {
+              float4* f = reinterpret_cast<float4*>(p.h_final + (bh * 64 + pp) * 128 + 32 * qq);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) f[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            }
+          } else if (publish) {  // h_in[c + 1] for the CTA that runs the rest of this chain
+            float4* f = reinterpret_cast<float4*>(cr + 32 * qq);
 #pragma unroll
             for (int j = 0; j < 8; ++j) f[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          }
-        } else {
-          uint32_t s0[16], s1[16];
+          } else {
+            uint32_t s0[16], s1[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            s0[j] = __float_as_uint(v[j]);
-            s1[j] = __float_as_uint(v[16 + j]);
+            for (int j = 0; j < 16; ++j) {
+              s0[j] = __float_as_uint(v[j]);
+              s1[j] = __float_as_uint(v[16 + j]);
+            }
+            tc::tmem_st16(tmem + lane_base + 32 * qq, s0);
+            tc::tmem_st16(tmem + lane_base + 32 * qq + 16, s1);
           }
-          tc::tmem_st16(tmem + lane_base + 32 * q, s0);
-          tc::tmem_st16(tmem + lane_base + 32 * q + 16, s1);
+        }
+        tc::tmem_st_wait();
+        if (publish) __threadfence();  // this row of the published state, before the flag
+        tc::fence_before_sync();
+        named_bar_sync(kSfStateBar, 128);
+        if (m == 0) {
+          mbar_arrive(&bars[kSFree + sb]);  // S[sb] may take the chunk run two later
+          if (publish) st_release_u64(&p.flags[sg.chain], make_flag(ctl.epoch, kFlagPrefix));
         }
       }
-      tc::tmem_st_wait();
-      tc::fence_before_sync();
-      named_bar_sync(kSfStateBar, 128);
-      if (m == 0) mbar_arrive(&bars[kSFree + sb]);  // S[sb] may take chunk c + 2
     }
-    if (nc == 0 && p.h_final) {  // no chunks: the final state is the initial one
+    if (nc == 0 && p.h_final) {  // no chunks: the final state is the initial one (one chain per CTA)
+      const int64_t bh = chain_bi(blockIdx.x) * p.nheads + chain_h(blockIdx.x) + hh;
+      const float* h0r = p.h0 ? p.h0 + (bh * 64 + pp) * 128 : nullptr;
       float4* f = reinterpret_cast<float4*>(p.h_final + (bh * 64 + pp) * 128);
 #pragma unroll 4
       for (int j = 0; j < 32; ++j) f[j] = h0r ? reinterpret_cast<const float4*>(h0r)[j] : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -331,24 +442,26 @@ __global__ void __launch_bounds__(kSfThreads, 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kSfTmemCols);
   }
+  if (threadIdx.x == 0) retire_tile(p.hdr, gridDim.x);  // the last CTA moves the epoch on
 }
 
 }  // namespace
 
-// One CTA per (batch, head pair) walks all chunks.  Per 64-token step it does the same work as
-// ssd_chunk_state_tc, so against the chunk-state + state-passing pair it saves the f32 chunk
-// states' round trip and the second launch, but it serialises each chain's chunks and cannot
-// spread a chain over several SMs.  It wins when all chains fit in one wave and are short
-// (b8 L2048 nh24: 42 us against ~49 us); with more chains than SMs the second wave costs a
-// whole chain (b4 L8192 nh80, 160 chains: 264 us against 211 us).
+// Per 64-token step the fused pass does the same work as ssd_chunk_state_tc, so against the
+// chunk-state + state-passing pair it saves the f32 chunk states' round trip and the second
+// launch.  With no more chains than SMs each CTA runs one chain (b8 L2048 nh24: 42 us against
+// ~49 us); with more, one CTA per SM runs an equal range of chunks, splitting chains where the
+// ranges meet.
 // Shapes the fused kernel computes correctly (any number of chains and chunks).
 bool ssd_state_fused_possible(const SsdDims& d) {
   return d.dtype == SSM_BF16 && d.headdim == 64 && d.dstate == 128 && (d.nheads / d.ngroups) % 2 == 0 &&
          d.chunk % kSfKH == 0 && d.chunk <= 256;
 }
 
-// Whether the fused kernel is the faster state path: the plan's choice, else one wave of
-// chains and short chains (a long chain is one CTA's serial work).
+// Whether the fused kernel is the faster state path: the plan's choice, else either more
+// chains than SMs (ranges split across CTAs: b4 L8192 nh80, 160 chains, 158 us against 207 us
+// for chunk states + state passing), or one wave of short chains (a long chain is one CTA's
+// serial work).
 bool ssd_state_fused_supported(const SsdDims& d) {
   if (!ssd_state_fused_possible(d)) return false;
   if (d.plan_fused >= 0) return d.plan_fused != 0;
@@ -357,7 +470,7 @@ bool ssd_state_fused_supported(const SsdDims& d) {
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return false;
   const int64_t chains = d.batch * (int64_t)(d.nheads / 2);
-  return chains <= sms && d.nchunks <= 16;
+  return chains > sms || d.nchunks <= 16;
 }
 
 cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float* h0, float* h_final,
@@ -382,6 +495,8 @@ cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float*
   p.h0 = h0;
   p.hin = static_cast<__nv_bfloat16*>(ws.hin);
   p.h_final = h_final;
+  p.carry = ws.Sc;  // the chunk-state buffer is free on this path: one state per split chain
+  p.flags = ws.flags;
   p.hdr = ws.hdr;
   p.lpad = d.lpad;
   p.nchunks = d.nchunks;
@@ -393,7 +508,16 @@ cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float*
   if ((e = ensure_smem_limit(reinterpret_cast<const void*>(ssd_state_fused_tc_kernel), smem)) != cudaSuccess)
     return e;
   const int64_t chains = d.batch * (int64_t)(d.nheads / 2);
-  return launch_pdl(ssd_state_fused_tc_kernel, dim3((unsigned)chains), dim3(kSfThreads), smem, s, map_x, map_b, p, ctl);
+  p.units = chains * d.nchunks;
+  int dev = 0, sms = 148;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  // one chain per CTA, or one CTA per SM with ranges of at least one chain (chains > SMs), so
+  // that a range never lies inside one chain; every CTA is resident at once (one per SM), so
+  // a CTA can wait for the state its predecessor publishes
+  const int64_t grid = (chains <= sms || d.nchunks == 0) ? chains : sms;
+  if (grid > chains || ws.sp_tiles < chains) return cudaErrorInvalidValue;
+  return launch_pdl(ssd_state_fused_tc_kernel, dim3((unsigned)grid), dim3(kSfThreads), smem, s, map_x, map_b, p, ctl);
 }
 
 }  // namespace ssm
