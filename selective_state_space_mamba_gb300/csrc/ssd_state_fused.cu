@@ -26,7 +26,9 @@
 //              the group's B, and the step's G and dt with the chunk's last G, into a ring
 //   warp 1     TMEM owner and MMA issuer (one thread): per chunk, once S[c & 1] is free,
 //              2 x 4 MMAs (hi, lo) per step accumulating into it
-//   warps 2-9  scalers: half a token row per thread, x w -> hi (in place) + lo
+//   warps 2-9  scalers, two groups of four warps on alternate steps (one group's chain of wait,
+//              split and barrier overlaps the other's): a token row per thread, x w -> hi (in
+//              place) + lo
 //   warps 10-13 state warps, one state row per thread: h0 or the published state in, h_in out
 //              per chunk, the decay and S folded in, h_final at a chain's end, the state
 //              published where a head ends
@@ -41,7 +43,7 @@ constexpr int kSfThreads = 448;  // warps 0 producer, 1 MMA, 2-9 scalers, 10-13 
 constexpr int kSfKH = 64;         // tokens per step
 constexpr int kSfStages = 4;      // one chunk of 256 tokens in flight
 constexpr int kSfRowBytes = 128;  // 64 bf16 per swizzled row
-constexpr uint32_t kSfScaleBar = 1, kSfStateBar = 2;
+constexpr uint32_t kSfScaleBar = 1, kSfStateBar = 2;  // scaler group g: named barrier 1 + 2 g
 constexpr uint32_t kSfTmemCols = 512;  // h at 0, S[0] at 128, S[1] at 256
 constexpr uint32_t kSfGdHead = (2 * kSfKH + 4) * 4;  // G[64], dt[64], G[T-4 .. T-1] of one head
 
@@ -279,16 +281,16 @@ __global__ void __launch_bounds__(kSfThreads, 1)
     }
   } else if (warp < 10) {
     // ---------------- scale X by w, split into bf16 hi + lo parts --------------------------
-    const int st_t = threadIdx.x - 64;  // 0..255
-    const int t = st_t >> 1;            // token row of the step: head t / 64, token t % 64
-    const int part = st_t & 1;          // which half of the row's eight 16-byte chunks
+    const int grp = (warp - 2) >> 2;          // this group takes the steps i with i % 2 == grp
+    const int t = threadIdx.x - 64 - 128 * grp;  // token row of the step: head t / 64, token t % 64
+    const uint32_t gbar = kSfScaleBar + 2 * grp;
     const int hh = t / kSfKH, tok = t % kSfKH;
     const int64_t nsteps = (u1 - u0) * nk;
-    for (int64_t i = 0; i < nsteps; ++i) {
+    for (int64_t i = grp; i < nsteps; i += 2) {
       const int st = (int)(i % kSfStages);
       const bool bad = !mbar_wait(&bars[kXFull + st], (uint32_t)(i / kSfStages) & 1u, ctl.spin_limit_ns);
-      if (named_bar_any(kSfScaleBar, 256, bad)) {  // leave together, or not at all
-        if (st_t == 0) fail();
+      if (named_bar_any(gbar, 128, bad)) {  // leave together, or not at all
+        if (t == 0) fail();
         break;
       }
       const float* gd = reinterpret_cast<const float*>(base + L.gd0 + (st * 2 + hh) * kSfGdHead);
@@ -301,8 +303,7 @@ __global__ void __launch_bounds__(kSfThreads, 1)
       unsigned char* hrow = base + st * L.stage_bytes + t * kSfRowBytes;
       unsigned char* lrow = hrow + L.half_bytes;
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        const int cc = part * 4 + c4;
+      for (int cc = 0; cc < 8; ++cc) {
         const int off = (cc ^ (t & 7)) << 4;  // the row's chunks, spread over the banks
         uint4 v = *reinterpret_cast<const uint4*>(hrow + off);
         uint32_t* e = reinterpret_cast<uint32_t*>(&v);
@@ -320,8 +321,8 @@ __global__ void __launch_bounds__(kSfThreads, 1)
         *reinterpret_cast<uint4*>(lrow + off) = r;
       }
       fence_proxy_async_smem();
-      named_bar_sync(kSfScaleBar, 256);
-      if (st_t == 0) mbar_arrive(&bars[kXScaled + st]);
+      named_bar_sync(gbar, 128);
+      if (t == 0) mbar_arrive(&bars[kXScaled + st]);
     }
   } else {
     // ------------------------------ state warps --------------------------------------------
