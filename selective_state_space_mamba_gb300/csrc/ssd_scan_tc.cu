@@ -256,6 +256,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
       const uint32_t id_kk = tc::idesc_bf16_f32(128, 64, false, false);  // Y2: C, h_in both K-major
       const uint32_t id_kn = tc::idesc_bf16_f32(128, 64, false, true);   // Ya, Yt: X MN-major
       const uint32_t xlbo = (uint32_t)T * kRowB;
+      int ndone = 0;  // heads whose MMAs were committed
       for (int k = 0; k < nh_run && ok && !*abort_flag; ++k) {
         const int st = k & 1, bf = k & 1;
         if (!mbar_wait(&bars[kStFull + st], (uint32_t)(k >> 1) & 1u, ctl.spin_limit_ns) ||
@@ -292,9 +293,19 @@ __global__ void __launch_bounds__(kScThreads, 1)
         }
         tc::mma_commit(&bars[kStEmpty + st]);  // X, h_in, G, dt of this head are no longer needed
         tc::mma_commit(&bars[kMmaDone + bf]);
+        ndone = k + 1;
       }
       tc::mma_commit(&bars[kDone]);
       mbar_wait(&bars[kDone], 0, ctl.spin_limit_ns);
+      // A commit's arrive lands when its MMAs complete, in no fixed order with the others: wait
+      // for the last phase of every committed barrier, so that no arrive is still due to this
+      // CTA's shared memory when it exits.
+      for (int x = 0; x < 2; ++x)
+        if (ndone > x) {
+          mbar_wait(&bars[kStEmpty + x], (uint32_t)(((ndone - 1 - x) / 2) & 1), ctl.spin_limit_ns);
+          mbar_wait(&bars[kMmaDone + x], (uint32_t)(((ndone - 1 - x) / 2) & 1), ctl.spin_limit_ns);
+        }
+      if (ok) mbar_wait(&bars[kCbDone], 0, ctl.spin_limit_ns);
     }
   } else if (warp < 10) {
     // ------------------------------ P warps ------------------------------------------------
@@ -439,6 +450,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
       }
       tc::tmem_st_wait();
       tc::fence_before_sync();
+      fence_proxy_async_smem();  // the stage's G and dt reads, before its TMA refill
       named_bar_sync(kScMathBar, kScMath);
       if (mt == 0) mbar_arrive(&bars[kPFull + bf]);
 
@@ -478,6 +490,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
         const uint4 w = *reinterpret_cast<const uint4*>(stage + i * kRowB + ((cc ^ (i & 7)) << 4));
         xr[4 * cc] = w.x; xr[4 * cc + 1] = w.y; xr[4 * cc + 2] = w.z; xr[4 * cc + 3] = w.w;
       }
+      // these reads must be performed before the TMA (async proxy) may refill the stage
+      fence_proxy_async_smem();
       named_bar_sync(kScEpiBar, kScEpi);
       if (et == 0) {
         mbar_arrive(&bars[kXRead + st]);  // x and G of this stage are in registers

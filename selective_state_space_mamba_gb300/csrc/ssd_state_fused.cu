@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kSfThreads, 1)
       const uint32_t ab_lbo = kSfKH * kSfRowBytes;  // head 0 -> head 1 block, s 0..63 -> s 64..127 block
       const uint32_t sbo = 8 * kSfRowBytes;         // next 8-token group
       bool ok = true;
-      int64_t i = 0;
+      int64_t i = 0, nready = 0;  // steps whose MMAs were committed, chunks handed to the state warps
       const int64_t nq = u1 - u0;  // chunks this CTA runs, in order (the accumulators alternate)
       for (int64_t q = 0; q < nq && ok && !*abort_flag; ++q) {
         const int sb = (int)(q & 1);
@@ -273,11 +273,21 @@ __global__ void __launch_bounds__(kSfThreads, 1)
           }
           tc::mma_commit(&bars[kXEmpty + st]);  // the stage may be refilled
         }
-        if (ok) tc::mma_commit(&bars[kSReady + sb]);  // S[sb] holds chunk q
+        if (ok) {
+          tc::mma_commit(&bars[kSReady + sb]);  // S[sb] holds chunk q
+          ++nready;
+        }
       }
       if (!ok) fail();
       tc::mma_commit(&bars[kDone]);
       mbar_wait(&bars[kDone], 0, ctl.spin_limit_ns);  // every MMA has completed
+      // A commit's arrive lands when its MMAs complete, in no fixed order with the others: wait
+      // for the last phase of every committed barrier, so that no arrive is still due to this
+      // CTA's shared memory when it exits.
+      for (int x = 0; x < kSfStages; ++x)
+        if (i > x) mbar_wait(&bars[kXEmpty + x], (uint32_t)(((i - 1 - x) / kSfStages) & 1), ctl.spin_limit_ns);
+      for (int x = 0; x < 2; ++x)
+        if (nready > x) mbar_wait(&bars[kSReady + x], (uint32_t)(((nready - 1 - x) / 2) & 1), ctl.spin_limit_ns);
     }
   } else if (warp < 10) {
     // ---------------- scale X by w, split into bf16 hi + lo parts --------------------------

@@ -210,8 +210,8 @@ __global__ void __launch_bounds__(kCsThreads, 1)
       const uint32_t idesc = tc::idesc_bf16_f32(128, 128, /*a_mn=*/false, /*b_mn=*/true);  // A from TMEM
       const uint32_t b_lbo = T * kCsRowBytes;      // s 0..63 block -> s 64..127 block
       const uint32_t sbo = 8 * kCsRowBytes;        // next 8-token group
-      int64_t cur_grp = -1, i = 0;
-      int nb = 0, q = 0;
+      int64_t cur_grp = -1, i = 0;  // i: steps whose MMAs were committed
+      int nb = 0, q = 0, nacc = 0;  // nacc: accumulators handed to the epilogue
       bool ok = true;
       for (int64_t u = u_begin; u < u_end && ok && !*abort_flag; ++u, ++q) {
         const CsUnit w = cs_unit(p, u);
@@ -242,11 +242,22 @@ __global__ void __launch_bounds__(kCsThreads, 1)
           }
           tc::mma_commit(&bars[kAEmpty + as]);  // the A stage's TMEM columns may be rewritten
         }
-        if (ok) tc::mma_commit(&bars[kAccFull + acc]);  // the accumulator is ready
+        if (ok) {
+          tc::mma_commit(&bars[kAccFull + acc]);  // the accumulator is ready
+          ++nacc;
+        }
       }
       if (!ok) fail();
       tc::mma_commit(&bars[kDone]);
       mbar_wait(&bars[kDone], 0, ctl.spin_limit_ns);  // every MMA has completed
+      // A commit's arrive lands when its MMAs complete, in no fixed order with the others: wait
+      // for the last phase of every committed barrier, so that no arrive is still due to this
+      // CTA's shared memory when it exits.
+      for (int x = 0; x < kCsAStages; ++x)
+        if (i > x) mbar_wait(&bars[kAEmpty + x], (uint32_t)(((i - 1 - x) / kCsAStages) & 1), ctl.spin_limit_ns);
+      for (int x = 0; x < 2; ++x)
+        if (nacc > x) mbar_wait(&bars[kAccFull + x], (uint32_t)(((nacc - 1 - x) / 2) & 1), ctl.spin_limit_ns);
+      if (nb > 1) mbar_wait(&bars[kBEmpty], (uint32_t)((nb - 2) & 1), ctl.spin_limit_ns);
     }
   } else if (warp < 10) {
     // ---------------- scale X by w, split into bf16 hi + lo parts, into TMEM ----------------
@@ -312,6 +323,7 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         }
         tc::tmem_st_wait();
         tc::fence_before_sync();
+        fence_proxy_async_smem();  // the X and G/dt reads, before the stage's TMA refill
         named_bar_sync(gbar, 128);
         if (gt == 0) {
           mbar_arrive(&bars[kXEmpty + st]);  // X and G/dt of step i are read: refill the stage

@@ -184,3 +184,30 @@ def _run_raw(inp, shape):
     ssm.ssd_fwd(x, dt, P.to_dev(inp["A"]), B, C, P.to_dev(inp["D"]), P.to_dev(inp["h0"]), chunk=shape.chunk)
     torch.cuda.synchronize()
     return ssm.check_device_status(kind="ssd")
+
+
+@pytest.mark.parametrize("chunk", [128, 256])
+def test_repeated_calls_bit_identical(cuda_lib, chunk):
+    """Forty forwards of a many-head shape give bit-identical outputs.  The shared-memory stages
+    are refilled by TMA (async proxy) once the threads that read them with ordinary loads
+    release them; with the chunk size 128 and more than 300 heads (one wave of long-running
+    CTAs), about one call in ten came out wrong in a few 16-byte pieces of y while those reads
+    were not fenced against the refill."""
+    import torch
+    import selective_state_space_mamba_gb300 as ssm
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nh = 2 * (sms + 40)
+    shape = synth.SSDShape(f"repeat_T{chunk}", 1, 1000, nh, 64, 128, 1, chunk, "bf16", h0=True)
+    inp = synth.ssd_inputs(shape, seed=101)
+    x, dt, B, C = (P.to_dev(inp[k], "bf16") for k in ("x", "dt", "B", "C"))
+    A, D, h0 = P.to_dev(inp["A"]), P.to_dev(inp["D"]), P.to_dev(inp["h0"])
+    y = torch.empty_like(x)
+    hf = torch.empty((1, nh, 64, 128), device="cuda")
+    ssm.ssd_fwd(x, dt, A, B, C, D, h0, chunk=chunk, y=y, h_final=hf)
+    torch.cuda.synchronize()
+    y0, h0f = y.clone(), hf.clone()
+    compare_units(shape, inp, P.to_np(y0), P.to_np(h0f), sample_units(shape, 8), f"{shape.name} first call")
+    for rep in range(40):
+        ssm.ssd_fwd(x, dt, A, B, C, D, h0, chunk=chunk, y=y, h_final=hf)
+        assert torch.equal(y, y0) and torch.equal(hf, h0f), f"call {rep + 1} differs from the first"
+    assert ssm.check_device_status(kind="ssd") == 0
