@@ -134,7 +134,11 @@ SSM_API ssm_status ssm_ssd_fwd(const void *x, const void *dt, const float *A, co
  * discrete plans, picked by measurement:
  *   - the state path: chunk states and the recurrence over chunks in one kernel (bf16, headdim
  *     64, dstate 128, an even number of heads per group), or the two kernels chunk-state then
- *     state-passing, the latter sequential over chunks or a decoupled look-back;
+ *     state-passing, the latter sequential over chunks or a decoupled look-back.  With more
+ *     (batch, head pair) chains than SMs the one-kernel pass runs one CTA per SM on equal
+ *     ranges of chunks, and a CTA that starts inside a chain waits (bounded) for the state its
+ *     predecessor publishes; it relies on all of its CTAs being resident at once, so where
+ *     other work holds SMs for longer than the wait limit the call reports SSM_ERR_TIMEOUT;
  *   - the chunk scan's run of heads per CTA (the tensor-core path).
  * Without a plan, ssm_ssd_fwd picks by fixed rules of thumb.  A plan id packs
  * (fused + 1) | (sequential + 1) << 2 | heads_per_cta << 4, where fused and sequential are 1

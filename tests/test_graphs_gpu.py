@@ -104,3 +104,46 @@ def test_decode_step_graph_loop(cuda_lib):
     torch.cuda.synchronize()
     y_ref, h_ref = ossd.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"])
     P.assert_ssd_close("bf16", np.stack(ys, axis=1), y_ref, P.to_np(state), h_ref, "graph decode loop")
+
+
+def test_fused_split_chains_graph_replays(cuda_lib):
+    """The fused state pass with more chains than SMs inside a CUDA graph: the states a CTA
+    publishes for its successor are flagged with the epoch kept in the workspace, which every
+    launch moves on, so a replay never takes a flag of the replay before it."""
+    import torch
+    import selective_state_space_mamba_gb300 as ssm
+    from oracle import native
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nh = 2 * (sms + 8)
+    shape = synth.SSDShape("graph_fused_split", 1, 520, nh, 64, 128, 1, 64, "bf16", h0=True)
+    inp0 = synth.ssd_inputs(shape, seed=91)
+    d = {k: P.to_dev(v, "bf16" if k in ("x", "dt", "B", "C") else "f32") for k, v in inp0.items()}
+    y = torch.empty_like(d["x"])
+    hf = torch.empty((1, nh, 64, 128), device="cuda")
+
+    def call():
+        ssm.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], chunk=shape.chunk, y=y, h_final=hf)
+
+    try:
+        ssm.set_ssd_fwd_plan(d["x"], d["B"], shape.chunk, ssm.plan_id(1, -1, 0))
+        call()  # warm-up outside the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call()
+        units = np.arange(nh)
+        for rep in range(3):
+            inp = synth.ssd_inputs(shape, seed=92 + rep)
+            for k, v in inp.items():
+                d[k].copy_(P.to_dev(v, "bf16" if k in ("x", "dt", "B", "C") else "f32"))
+            g.replay()
+            torch.cuda.synchronize()
+            assert ssm.check_device_status(kind="ssd") == 0
+            y_ref, hf_ref = native.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"],
+                                           units=units)
+            yn, hn = P.to_np(y), P.to_np(hf)
+            yu = np.stack([yn[0, :, u] for u in units])
+            hu = np.stack([hn[0, u] for u in units])
+            P.assert_ssd_close("bf16", yu, y_ref, hu, hf_ref, f"{shape.name} replay {rep}")
+    finally:
+        ssm.clear_ssd_fwd_plans()
