@@ -355,8 +355,10 @@ __global__ void __launch_bounds__(kScThreads, 1)
       const float* gq = reinterpret_cast<const float*>(base + L.st0 + st * L.st_bytes + L.g_off);
       const float* dq = reinterpret_cast<const float*>(base + L.st0 + st * L.st_bytes + L.dt_off);
       float* vq = v_all + (k & 1) * kVFloats;
-      for (int e = mt; e < kVRect + i0; e += kScMath) {
-        int j, ref;
+      // at most three entries per thread, straight-line so that all their loads are issued
+      // together: entry mt (triangle below kVRect, else rectangle), entry mt + 256 (rectangle,
+      // tiles with i0 > 0) and the diagonal entry mt
+      auto entry = [&](int e, int& j, int& ref) {
         if (e < kVRect) {  // triangle: local row block I, reference row i0 + 32 I
           const int I = e < 32 ? 1 : (e < 96 ? 2 : 3);
           j = i0 + e - v_off(I);
@@ -365,9 +367,18 @@ __global__ void __launch_bounds__(kScThreads, 1)
           j = e - kVRect;
           ref = i0;
         }
-        vq[e] = dq[j] * tc::ex2_approx(gq[ref] - gq[j]);
-      }
-      if (mt < 128) vq[kVDiag + mt] = lg2_approx(dq[i0 + mt]) - gq[i0 + mt];  // dt = 0 -> -inf
+      };
+      const int e0 = mt, e1 = mt + kScMath;
+      const bool has0 = e0 < kVRect + i0, has1 = e1 < kVRect + i0, hasd = mt < 128;
+      int j0 = 0, r0 = 0, j1 = 0, r1 = 0;
+      entry(e0, j0, r0);
+      entry(e1, j1, r1);
+      const float d0 = has0 ? dq[j0] : 0.f, a0 = has0 ? gq[r0] - gq[j0] : 0.f;
+      const float d1 = has1 ? dq[j1] : 0.f, a1 = has1 ? gq[r1] - gq[j1] : 0.f;
+      const float dd = hasd ? dq[i0 + mt] : 1.f, gd = hasd ? gq[i0 + mt] : 0.f;
+      if (has0) vq[e0] = d0 * tc::ex2_approx(a0);
+      if (has1) vq[e1] = d1 * tc::ex2_approx(a1);
+      if (hasd) vq[kVDiag + mt] = lg2_approx(dd) - gd;  // dt = 0 -> -inf
       return true;
     };
 
