@@ -1,6 +1,5 @@
 """The benchmark's N > 1 path on CPU: two gloo ranks run its barrier, its max over ranks and
-its weak-scaling aggregation (the GPU runs of this build have one GPU, so the NCCL path is
-exercised with the same calls on a gloo group here)."""
+its weak-scaling aggregation, with the same calls the NCCL path makes on several GPUs."""
 import os
 import socket
 import subprocess
