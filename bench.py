@@ -532,7 +532,7 @@ def run_e2e(args):
         step(i)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n = max(4, min(args.steps, 12))
+    n = max(4, args.steps)  # the pipeline's fill and drain are inside the timed region
     start.record(s_in)
     for i in range(n):
         step(i)
