@@ -85,36 +85,50 @@ def _sm_count():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
-@pytest.mark.parametrize("extra_chains,seqlen,chunk,G", [(8, 520, 64, 1), (1, 300, 64, 1), (40, 1000, 128, 2),
-                                                        (148, 200, 64, 4)])
-def test_fused_pass_with_more_chains_than_sms(cuda_lib, extra_chains, seqlen, chunk, G):
+@pytest.mark.parametrize("extra_chains,seqlen,chunk,G,h0,final", [(8, 520, 64, 1, True, True), (1, 300, 64, 1, True, True),
+                                                                 (40, 1000, 128, 2, True, True),
+                                                                 (148, 200, 64, 4, True, True),
+                                                                 (8, 700, 128, 1, False, False),
+                                                                 (8, 200, 256, 1, True, True)])
+def test_fused_pass_with_more_chains_than_sms(cuda_lib, extra_chains, seqlen, chunk, G, h0, final):
     """The fused state pass with more (batch, head pair) chains than SMs: one CTA per SM runs an
     equal range of chunks, so chains are split between CTAs and the CTA that runs a chain's
-    tail starts from the state its predecessor publishes.  Every output is compared with the
-    float64 oracle, and a second call (a new flag epoch) gives the same result."""
+    tail starts from the state its predecessor publishes (with one chunk per chain the ranges
+    hold whole chains only).  Every output is compared with the float64 oracle, and a second
+    call (a new flag epoch) gives the same result."""
+    import torch
     import selective_state_space_mamba_gb300 as ssm
     from oracle import native
     chains = _sm_count() + extra_chains
     nh = 2 * chains
     while nh % G or (nh // G) % 2:
         nh += 2
-    shape = synth.SSDShape(f"fused_split_{chains}", 1, seqlen, nh, 64, 128, G, chunk, "bf16", h0=True)
+    shape = synth.SSDShape(f"fused_split_{chains}", 1, seqlen, nh, 64, 128, G, chunk, "bf16", h0=h0)
     inp = synth.ssd_inputs(shape, seed=61 + extra_chains)
     d = dev_inputs(inp, "bf16")
     units = np.arange(shape.batch * nh)
-    y_ref, hf_ref = native.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"],
-                                   units=units)
+    y_ref, hf_ref = native.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                                   inp["h0"] if h0 else None, units=units)
     try:
         ssm.set_ssd_fwd_plan(d["x"], d["B"], chunk, ssm.plan_id(1, -1, 0))
         first = None
         for rep in range(2):
-            y, hf = run(ssm, d, chunk)
+            y, hf = ssm.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"] if h0 else None,
+                                chunk=chunk, return_final_state=final)
+            torch.cuda.synchronize()
+            assert ssm.check_device_status(kind="ssd") == 0
+            y = P.to_np(y)
             yu = np.stack([y[u // nh, :, u % nh] for u in units])
-            hu = np.stack([hf[u // nh, u % nh] for u in units])
-            P.assert_ssd_close("bf16", yu, y_ref, hu, hf_ref, f"{shape.name} call {rep}")
+            if final:
+                hf = P.to_np(hf)
+                hu = np.stack([hf[u // nh, u % nh] for u in units])
+                P.assert_ssd_close("bf16", yu, y_ref, hu, hf_ref, f"{shape.name} call {rep}")
+            else:
+                assert hf is None
+                P.assert_ssd_close("bf16", yu, y_ref, None, None, f"{shape.name} call {rep}")
             if first is None:
                 first = (y, hf)
             else:
-                assert np.array_equal(first[0], y) and np.array_equal(first[1], hf)
+                assert np.array_equal(first[0], y) and (not final or np.array_equal(first[1], hf))
     finally:
         ssm.clear_ssd_fwd_plans()
