@@ -14,9 +14,10 @@
 // that chain: the previous CTA ran that head first, and its head is shorter than what this
 // CTA runs before its tail by the range length minus the chain length, so the wait is short.
 // The pair's rows (2 heads x 64 p = 128 TMEM lanes, x 128 s columns, f32) have three TMEM
-// homes: the running state h and two accumulators S[0], S[1].  The MMAs add chunk c's weighted X^T B into S[c & 1] without
-// waiting for the state; the state warps then write h out as h_in[c] (bf16), fold S[c & 1] in
-// (h = 2^(G_last) h + S) and release the accumulator for chunk c + 2.  The weighted X is split
+// homes: the running state h and two accumulators S[0], S[1].  The MMAs add the weighted X^T B
+// of the CTA's q-th chunk c into S[q & 1] without waiting for the state; the state warps then
+// write h out as h_in[c] (bf16), fold S[q & 1] in (h = 2^(G_last) h + S) and release the
+// accumulator for the chunk run two later.  The weighted X is split
 // into bf16 hi + lo halves exactly as in ssd_chunk_state_tc, so the state keeps f32 accuracy.
 // The per-chunk increments S_c never go to memory: against the chunk-state + state-passing
 // pair this saves writing and re-reading them (f32) entirely.
@@ -24,7 +25,7 @@
 // Warps (448 threads):
 //   warp 0     TMA producer: per 64-token step, X of the pair's two heads, the step's rows of
 //              the group's B, and the step's G and dt with the chunk's last G, into a ring
-//   warp 1     TMEM owner and MMA issuer (one thread): per chunk, once S[c & 1] is free,
+//   warp 1     TMEM owner and MMA issuer (one thread): per chunk, once S[q & 1] is free,
 //              2 x 4 MMAs (hi, lo) per step accumulating into it
 //   warps 2-9  scalers, two groups of four warps on alternate steps (one group's chain of wait,
 //              split and barrier overlaps the other's): a token row per thread, x w -> hi (in
