@@ -291,6 +291,16 @@ SSM_API ssm_status ssm_check_device_status(void *workspace, ssm_stream_t stream)
 SSM_API void ssm_debug_set_lookback_fault(int64_t stall_tile, uint64_t spin_limit_ns);
 
 /*
+ * Test hook for the fused state pass's work split (host only; no GPU call).  For `chains`
+ * (batch, head pair) chains of `nchunks` chunks on a GPU with `sms` SMs it lists, in the order
+ * each CTA runs them, the segments of every CTA: one row of six int64 per segment, (cta, chain,
+ * first chunk, end chunk, starts from the state the previous CTA publishes, publishes its final
+ * state for the next CTA).  Writes at most `cap` rows to `rows` (which may be NULL) and
+ * returns the number of segments, or -1 for a negative size or sms < 1.
+ */
+SSM_API int64_t ssm_debug_fused_schedule(int64_t chains, int64_t nchunks, int sms, int64_t *rows, int64_t cap);
+
+/*
  * Kernel timing (measurement aid; not needed in normal use).  Between ssm_profile_begin()
  * and ssm_profile_end(), every ssm_ssd_fwd / ssm_ssd_step / ssm_linscan_fwd call records a
  * CUDA event on its own stream before and after each kernel it launches (at most

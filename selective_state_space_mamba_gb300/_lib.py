@@ -22,7 +22,7 @@ EXPORTS = ("ssm_status_string", "ssm_version", "ssm_ssd_fwd_workspace_bytes", "s
            "ssm_linscan_workspace_bytes", "ssm_linscan_fwd", "ssm_check_device_status",
            "ssm_debug_set_lookback_fault", "ssm_profile_begin", "ssm_profile_end", "ssm_linscan_fwd_noalloc",
            "ssm_ssd_step", "ssm_linscan_baseline_workspace_bytes", "ssm_linscan_baseline", "ssm_ssd_fwd_tune",
-           "ssm_ssd_fwd_set_plan", "ssm_ssd_fwd_get_plan", "ssm_ssd_fwd_clear_plans")
+           "ssm_ssd_fwd_set_plan", "ssm_ssd_fwd_get_plan", "ssm_ssd_fwd_clear_plans", "ssm_debug_fused_schedule")
 PROFILE_KERNELS = ("linscan_lookback", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
                    "ssd_state_fused", "ssd_step", "linscan_baseline")
 
@@ -48,6 +48,8 @@ def _declare(lib):
     lib.ssm_ssd_fwd.restype = i32
     lib.ssm_ssd_fwd_tune.argtypes = [vp] * 9 + [i64, i64, i32, i32, i32, i32, i32, i32, vp, sz, vp, i32, vp, vp]
     lib.ssm_ssd_fwd_tune.restype = i32
+    lib.ssm_debug_fused_schedule.argtypes = [i64, i64, i32, vp, i64]
+    lib.ssm_debug_fused_schedule.restype = i64
     lib.ssm_ssd_fwd_set_plan.argtypes = [i64, i64, i32, i32, i32, i32, i32, i32, i32]
     lib.ssm_ssd_fwd_set_plan.restype = i32
     lib.ssm_ssd_fwd_get_plan.argtypes = [i64, i64, i32, i32, i32, i32, i32, i32, vp]

@@ -22,6 +22,7 @@ cudaError_t launch_ssd_chunk_state_tc(const void* x, const void* B, const SsdDim
 bool ssd_scan_tc_supported(const SsdDims& d);
 bool ssd_state_fused_supported(const SsdDims& d);
 bool ssd_state_fused_possible(const SsdDims& d);
+int64_t ssd_fused_schedule(int64_t chains, int64_t nchunks, int sms, int64_t* rows, int64_t cap);
 cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float* h0, float* h_final,
                                       const SsdDims& d, const SsdWorkspace& ws, const LookbackCtl& ctl,
                                       cudaStream_t s);
@@ -640,6 +641,10 @@ ssm_status ssm_profile_end(double* ms_out, int64_t* launches_out) {
 void ssm_debug_set_lookback_fault(int64_t stall_tile, uint64_t spin_limit_ns) {
   g_stall_tile.store(stall_tile < 0 ? -1 : stall_tile, std::memory_order_relaxed);
   g_spin_limit_ns.store(spin_limit_ns, std::memory_order_relaxed);
+}
+
+int64_t ssm_debug_fused_schedule(int64_t chains, int64_t nchunks, int sms, int64_t* rows, int64_t cap) {
+  return ssd_fused_schedule(chains, nchunks, sms, rows, cap < 0 ? 0 : cap);
 }
 
 }  // extern "C"

@@ -75,7 +75,7 @@ struct SfSeg {
   int c0, c1;
   bool from_carry, to_carry;
 };
-__device__ __forceinline__ SfRange sf_range(int64_t u0, int64_t u1, int64_t nc) {
+__host__ __device__ __forceinline__ SfRange sf_range(int64_t u0, int64_t u1, int64_t nc) {
   SfRange r;
   r.first_chain = u0 / nc;
   r.c_first = (int)(u0 % nc);
@@ -89,7 +89,7 @@ __device__ __forceinline__ SfRange sf_range(int64_t u0, int64_t u1, int64_t nc) 
   r.nseg = (r.has_head ? 1 : 0) + r.nfull + (r.has_tail ? 1 : 0);
   return r;
 }
-__device__ __forceinline__ SfSeg sf_seg(const SfRange& r, int s, int64_t nc) {
+__host__ __device__ __forceinline__ SfSeg sf_seg(const SfRange& r, int s, int64_t nc) {
   SfSeg g;
   if (r.has_head) {
     if (s == 0) {
@@ -457,7 +457,37 @@ __global__ void __launch_bounds__(kSfThreads, 1)
   if (threadIdx.x == 0) retire_tile(p.hdr, gridDim.x);  // the last CTA moves the epoch on
 }
 
+// CTAs of a launch: one per chain, or one per SM (ranges of at least one chain) when there are
+// more chains than SMs
+__host__ __forceinline__ int64_t sf_grid(int64_t chains, int64_t nchunks, int sms) {
+  return (chains <= sms || nchunks == 0) ? chains : sms;
+}
+
 }  // namespace
+
+int64_t ssd_fused_schedule(int64_t chains, int64_t nchunks, int sms, int64_t* rows, int64_t cap) {
+  if (chains < 0 || nchunks < 0 || sms < 1) return -1;
+  const int64_t grid = sf_grid(chains, nchunks, sms), units = chains * nchunks;
+  int64_t n = 0;
+  for (int64_t k = 0; k < grid; ++k) {
+    const int64_t u0 = k * units / grid, u1 = (k + 1) * units / grid;
+    if (nchunks == 0 || u1 <= u0) continue;
+    const SfRange rg = sf_range(u0, u1, nchunks);
+    for (int s = 0; s < rg.nseg; ++s, ++n) {
+      const SfSeg g = sf_seg(rg, s, nchunks);
+      if (rows && n < cap) {
+        int64_t* r = rows + 6 * n;
+        r[0] = k;
+        r[1] = g.chain;
+        r[2] = g.c0;
+        r[3] = g.c1;
+        r[4] = g.from_carry ? 1 : 0;
+        r[5] = g.to_carry ? 1 : 0;
+      }
+    }
+  }
+  return n;
+}
 
 // Per 64-token step the fused pass does the same work as ssd_chunk_state_tc, so against the
 // chunk-state + state-passing pair it saves the f32 chunk states' round trip and the second
@@ -527,7 +557,7 @@ cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float*
   // one chain per CTA, or one CTA per SM with ranges of at least one chain (chains > SMs), so
   // that a range never lies inside one chain; every CTA is resident at once (one per SM), so
   // a CTA can wait for the state its predecessor publishes
-  const int64_t grid = (chains <= sms || d.nchunks == 0) ? chains : sms;
+  const int64_t grid = sf_grid(chains, d.nchunks, sms);
   if (grid > chains || ws.sp_tiles < chains) return cudaErrorInvalidValue;
   return launch_pdl(ssd_state_fused_tc_kernel, dim3((unsigned)grid), dim3(kSfThreads), smem, s, map_x, map_b, p, ctl);
 }
