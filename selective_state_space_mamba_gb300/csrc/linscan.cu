@@ -122,6 +122,9 @@ __device__ __forceinline__ int swz(int line, int chunk) { return line * kLsRow +
 __device__ void ls_producer(LsShared& sh, const LsArgs& p, const CUtensorMap* map_a, const CUtensorMap* map_b,
                             const LinscanWorkspace& ws, const LookbackCtl& ctl) {
   int64_t tile = claim_tile(ws.hdr);
+#if SSM_LS_STREAM_HINT
+  const uint64_t pol = l2_evict_first_policy();
+#endif
   for (int i = 0;; ++i) {
     const int st = i % kLsStages;
     const int use = i / kLsStages;
@@ -139,8 +142,13 @@ __device__ void ls_producer(LsShared& sh, const LsArgs& p, const CUtensorMap* ma
     if (line0 < p.lines) {
       // the whole box counts toward the transaction, rows past the tensor are zero-filled
       mbar_arrive_expect_tx(&sh.full[st], 2u * (uint32_t)sizeof(float) * kLsTile);
+#if SSM_LS_STREAM_HINT
+      tma_load_2d_hint(sh.stage[st].a, map_a, 0, (int)line0, &sh.full[st], pol);
+      tma_load_2d_hint(sh.stage[st].b, map_b, 0, (int)line0, &sh.full[st], pol);
+#else
       tma_load_2d(sh.stage[st].a, map_a, 0, (int)line0, &sh.full[st]);
       tma_load_2d(sh.stage[st].b, map_b, 0, (int)line0, &sh.full[st]);
+#endif
     } else {
       mbar_arrive(&sh.full[st]);  // only the ragged tail: consumers read it directly
     }
@@ -224,6 +232,9 @@ __device__ void ls_lookback_warp(LsShared& sh, const LinscanWorkspace& ws, const
 // has read it, and hand the stage back to the producer; stops at the stop job.
 __device__ void ls_store_warp(LsShared& sh, const CUtensorMap* map_h, const LinscanWorkspace& ws,
                               const LookbackCtl& ctl) {
+#if SSM_LS_STREAM_HINT
+  const uint64_t pol = l2_evict_first_policy();
+#endif
   for (int j = 0;; ++j) {
     const int st = j % kLsStages;
     if (!mbar_wait(&sh.st_req[st], (uint32_t)(j / kLsStages) & 1u, ctl.spin_limit_ns)) {
@@ -233,7 +244,11 @@ __device__ void ls_store_warp(LsShared& sh, const CUtensorMap* map_h, const Lins
     const int64_t line0 = sh.st_line0[st];
     if (line0 < 0) break;
     if (line0 < (int64_t)0x7fffffff && line0 >= 0) {
+#if SSM_LS_STREAM_HINT
+      tma_store_2d_hint(map_h, sh.stage[st].a, 0, (int)line0, pol);
+#else
       tma_store_2d(map_h, sh.stage[st].a, 0, (int)line0);
+#endif
       bulk_commit();
       bulk_wait_read<0>();
     }

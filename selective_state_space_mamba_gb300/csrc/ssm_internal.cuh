@@ -225,6 +225,30 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
                "r"(smem_addr(src)), "r"(c0), "r"(c1)
                : "memory");
 }
+// L2 policy for data a kernel touches once (streamed in or out): its lines are evicted before
+// lines of normal priority, so a stream does not push other data, such as dirty lines another
+// kernel left behind, out of L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// tma_load_2d / tma_store_2d with an L2 cache policy
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar,
+                                                 uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, const void* src, int c0, int c1,
+                                                  uint64_t pol) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_addr(src)), "r"(c0), "r"(c1), "l"(pol)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N of this thread's bulk groups still READ shared memory.
 template <int N>
@@ -335,6 +359,9 @@ struct LinscanWorkspace {
 #endif
 #ifndef SSM_LS_STAGES
 #define SSM_LS_STAGES 3
+#endif
+#ifndef SSM_LS_STREAM_HINT  // a, b and h streamed through L2 with evict-first priority
+#define SSM_LS_STREAM_HINT 1
 #endif
 #ifndef SSM_LS_MIN_BLOCKS
 #define SSM_LS_MIN_BLOCKS 2
