@@ -15,12 +15,17 @@
 //     quarter-warp: conflict-free), and h goes back to the same swizzled buffer and out with
 //     a TMA tensor store.  Loads and stores are fully coalesced and asynchronous.
 //   * persistent, warp-specialised CTAs: one producer warp claims tiles (atomic counter) and
-//     fills a ring of shared-memory stages ("full" / "empty" mbarriers); the consumer warps
-//     scan; one look-back warp resolves tile i's prefix while the consumers already run the
-//     first pass of tile i+1 (the second pass re-reads tile i from its stage), so the
-//     look-back latency is off the consumers' path; one store warp issues the TMA store of
-//     each finished tile and hands its stage back to the producer once the store has read it.  Claims stay in counter order and each CTA consumes its
-//     claims in order, so the page's forward-progress argument holds: the smallest
+//     fills a ring of shared-memory stages ("full" / "empty" mbarriers).  For rows of several
+//     tiles (one CTA per SM, 6 stages) two groups of consumer warps take the CTA's tiles in
+//     turn (for short rows, two CTAs per SM, 3 stages and one group); one look-back
+//     warp resolves tile i's prefix while the group that owns it runs the first pass of its
+//     next tile, i + 2 (its second pass then re-reads tile i from its stage), so the
+//     look-back has two tiles' time and is off the consumers' path, and the two groups'
+//     chains of waits overlap; one store warp issues the TMA store of each finished tile and
+//     hands its stage back to the producer once the store has read it.  Claims stay in
+//     counter order and each CTA consumes its claims in order (the groups alternate, the
+//     look-back and store warps serve tiles in order), so the page's forward-progress
+//     argument holds: the smallest
 //     unfinished tile is always some CTA's current tile (its data arrives without waiting on
 //     anything) and it waits only on smaller tiles.
 //   * a tile's flag and value share one 16-byte descriptor (no fence between value and flag),
@@ -66,30 +71,42 @@ struct LsStage {  // two [kLsLines x 32] float boxes in 128-byte swizzled layout
   float b[kLsTile];  // h is written back over a
 };
 static_assert(kLsRow % (4 * kLsSplit) == 0, "a thread owns whole 16-byte chunks");
-struct LsJob {        // consumer -> look-back warp, double-buffered by tile parity
+struct LsJob {        // consumer -> look-back warp, 2 x groups slots by tile index
   int64_t tile;      // >= tiles: stop
   int64_t r0;
   Pair agg;          // tile aggregate
   float prefix;      // look-back warp -> consumers: state before the tile
   int absolute;
 };
+// The CTA's shape: G consumer groups taking tiles in turn, an S-stage ring.  With one group a
+// tile's second pass runs while the same warps scan the next tile; with two, while they scan
+// the tile after that, so the look-back of a tile has two tiles' time.
+template <int G, int S, int kCtasPerSm>
+struct LsCfg {
+  static constexpr int kGroups = G, kStages = S, kJobs = 2 * G, kMinBlocks = kCtasPerSm;
+  static constexpr int kConsumers = G * kLsThreads;
+  static constexpr int kBlock = kConsumers + 96;  // consumer warps + producer, look-back and store warps
+};
+using LsLongRows = LsCfg<2, 6, 1>;   // one CTA per SM (192 KB of stages)
+using LsShortRows = LsCfg<1, 3, 2>;  // two CTAs per SM (96 KB of stages each)
+
+template <class Cfg>
 struct LsShared {
-  LsStage stage[kLsStages];   // first member: 1024-byte aligned (swizzle atom)
-  uint64_t full[kLsStages];   // producer -> consumers: tile id written, data landed
-  uint64_t empty[kLsStages];  // consumers -> producer: stage read and stored, may be refilled
-  uint64_t lb_req[2];         // consumers -> look-back warp: job posted
-  uint64_t lb_done[2];        // look-back warp -> consumers: prefix posted
-  uint64_t st_req[kLsStages]; // consumers -> store warp: stage holds a finished tile (or stop)
-  int64_t st_line0[kLsStages];// first line of that tile (< 0: stop)
-  int64_t tile[kLsStages];
-  int64_t r0[kLsStages];      // position of the tile's first element within its row
-  LsJob job[2];
-  Pair warp_agg[2][kLsThreads / 32];
+  LsStage stage[Cfg::kStages];   // first member: 1024-byte aligned (swizzle atom)
+  uint64_t full[Cfg::kStages];   // producer -> consumers: tile id written, data landed
+  uint64_t empty[Cfg::kStages];  // consumers -> producer: stage read and stored, may be refilled
+  uint64_t lb_req[Cfg::kJobs];   // consumers -> look-back warp: job posted
+  uint64_t lb_done[Cfg::kJobs];  // look-back warp -> consumers: prefix posted
+  uint64_t st_req[Cfg::kStages]; // consumers -> store warp: stage holds a finished tile (or stop)
+  int64_t st_line0[Cfg::kStages];// first line of that tile (< 0: stop)
+  int64_t tile[Cfg::kStages];
+  int64_t r0[Cfg::kStages];      // position of the tile's first element within its row
+  LsJob job[Cfg::kJobs];
+  Pair warp_agg[Cfg::kGroups][2][kLsThreads / 32];
 };
 static_assert(sizeof(LsStage) % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
 
-constexpr int kLsBlock = kLsThreads + 96;  // consumer warps + producer, look-back and store warps
-constexpr uint32_t kLsConsumerBar = 1;      // named barrier of the consumer warps
+constexpr uint32_t kLsConsumerBar = 1;       // named barrier of consumer group g: 1 + g
 
 struct LsArgs {
   const float* a;
@@ -115,19 +132,21 @@ __device__ __forceinline__ int64_t row_pos(int64_t r0, int e0, int64_t len) {
 __device__ __forceinline__ int swz(int line, int chunk) { return line * kLsRow + ((chunk ^ (line & 7)) << 2); }
 
 // Producer (one thread): claim tiles in counter order and fill the stage ring; it ends after
-// the first claim past the last tile, which it hands on as a sentinel.  Each claim is made
+// the first claim past the last tile, which it hands on as one sentinel per consumer group.  Each claim is made
 // one tile ahead, so the atomic's round trip overlaps the wait for a free stage.  Progress is
 // unchanged: the smallest unfinished tile, if it is only claimed, waits for a stage that
 // holds smaller tiles, all of which are finished.
-__device__ void ls_producer(LsShared& sh, const LsArgs& p, const CUtensorMap* map_a, const CUtensorMap* map_b,
+template <class Cfg>
+__device__ void ls_producer(LsShared<Cfg>& sh, const LsArgs& p, const CUtensorMap* map_a, const CUtensorMap* map_b,
                             const LinscanWorkspace& ws, const LookbackCtl& ctl) {
   int64_t tile = claim_tile(ws.hdr);
+  int stops = 0;
 #if SSM_LS_STREAM_HINT
   const uint64_t pol = l2_evict_first_policy();
 #endif
   for (int i = 0;; ++i) {
-    const int st = i % kLsStages;
-    const int use = i / kLsStages;
+    const int st = i % Cfg::kStages;
+    const int use = i / Cfg::kStages;
     if (use > 0 && !mbar_wait(&sh.empty[st], (uint32_t)(use - 1) & 1u, ctl.spin_limit_ns)) {
       record_error(ws.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
       return;  // the consumers give up on their own bounded wait
@@ -135,7 +154,8 @@ __device__ void ls_producer(LsShared& sh, const LsArgs& p, const CUtensorMap* ma
     sh.tile[st] = tile;
     if (tile >= ws.tiles) {
       mbar_arrive(&sh.full[st]);  // sentinel, no data
-      return;
+      if (++stops == Cfg::kGroups) return;  // every consumer group takes one
+      continue;
     }
     sh.r0[st] = (tile * kLsTile) % p.len;
     const int64_t line0 = tile * kLsLines;
@@ -207,13 +227,14 @@ __device__ __forceinline__ float lookback(int64_t tile, const LinscanWorkspace& 
 }
 
 // Look-back warp: serve the consumers' jobs in order until the stop job.
-__device__ void ls_lookback_warp(LsShared& sh, const LinscanWorkspace& ws, const LookbackCtl& ctl, int lane) {
+template <class Cfg>
+__device__ void ls_lookback_warp(LsShared<Cfg>& sh, const LinscanWorkspace& ws, const LookbackCtl& ctl, int lane) {
   for (int j = 0;; ++j) {
-    if (!mbar_wait(&sh.lb_req[j & 1], (uint32_t)(j >> 1) & 1u, ctl.spin_limit_ns)) {
+    if (!mbar_wait(&sh.lb_req[j % Cfg::kJobs], (uint32_t)(j / Cfg::kJobs) & 1u, ctl.spin_limit_ns)) {
       if (lane == 0) record_error(ws.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
       return;
     }
-    LsJob& job = sh.job[j & 1];
+    LsJob& job = sh.job[j % Cfg::kJobs];
     const int64_t tile = job.tile;
     if (tile >= ws.tiles) return;
     const bool need_prefix = (tile != 0) && (job.r0 != 0);
@@ -222,7 +243,7 @@ __device__ void ls_lookback_warp(LsShared& sh, const LinscanWorkspace& ws, const
       if (tile != ctl.stall_tile && !job.absolute)
         st_relaxed_desc(&ws.desc[tile], make_flag(ctl.epoch, kFlagPrefix), 0.f, apply(job.agg, x));
       job.prefix = x;
-      mbar_arrive(&sh.lb_done[j & 1]);
+      mbar_arrive(&sh.lb_done[j % Cfg::kJobs]);
     }
     __syncwarp();
   }
@@ -230,14 +251,15 @@ __device__ void ls_lookback_warp(LsShared& sh, const LinscanWorkspace& ws, const
 
 // Store warp (one thread): in tile order, TMA-store each finished stage, wait until the store
 // has read it, and hand the stage back to the producer; stops at the stop job.
-__device__ void ls_store_warp(LsShared& sh, const CUtensorMap* map_h, const LinscanWorkspace& ws,
+template <class Cfg>
+__device__ void ls_store_warp(LsShared<Cfg>& sh, const CUtensorMap* map_h, const LinscanWorkspace& ws,
                               const LookbackCtl& ctl) {
 #if SSM_LS_STREAM_HINT
   const uint64_t pol = l2_evict_first_policy();
 #endif
   for (int j = 0;; ++j) {
-    const int st = j % kLsStages;
-    if (!mbar_wait(&sh.st_req[st], (uint32_t)(j / kLsStages) & 1u, ctl.spin_limit_ns)) {
+    const int st = j % Cfg::kStages;
+    if (!mbar_wait(&sh.st_req[st], (uint32_t)(j / Cfg::kStages) & 1u, ctl.spin_limit_ns)) {
       record_error(ws.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
       break;
     }
@@ -257,43 +279,46 @@ __device__ void ls_store_warp(LsShared& sh, const CUtensorMap* map_h, const Lins
   bulk_wait<0>();  // every store of this CTA has completed
 }
 
-__global__ void __launch_bounds__(kLsBlock, SSM_LS_MIN_BLOCKS)
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::kBlock, Cfg::kMinBlocks)
     linscan_lookback_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                             const __grid_constant__ CUtensorMap map_h, LsArgs p, LinscanWorkspace ws,
                             LookbackCtl ctl_call) {
   extern __shared__ unsigned char ls_smem_raw[];
   // align the stage ring to the 1024-byte swizzle atom (the launch adds 1 KB of slack)
   const uint32_t raw = smem_addr(ls_smem_raw);
-  LsShared& sh = *reinterpret_cast<LsShared*>(ls_smem_raw + ((1024u - (raw & 1023u)) & 1023u));
+  LsShared<Cfg>& sh = *reinterpret_cast<LsShared<Cfg>*>(ls_smem_raw + ((1024u - (raw & 1023u)) & 1023u));
   const LookbackCtl ctl = device_epoch(ctl_call, ws.hdr);
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int t = threadIdx.x;                           // consumer thread
+  const int grp = threadIdx.x / kLsThreads;            // consumer group: tiles it with it % Cfg::kGroups == grp
+  const int t = threadIdx.x % kLsThreads;              // consumer thread within its group
+  const uint32_t cbar = kLsConsumerBar + grp;
   const int my_line = t / kLsSplit;                    // line within the tile
   const int my_chunk0 = (t % kLsSplit) * (kLsElems / 4);  // first 16-byte chunk of the line
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kLsStages; ++s) {
+    for (int s = 0; s < Cfg::kStages; ++s) {
       mbar_init(&sh.full[s], 1);
       mbar_init(&sh.empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < Cfg::kJobs; ++s) {
       mbar_init(&sh.lb_req[s], 1);
       mbar_init(&sh.lb_done[s], 1);
     }
-    for (int s = 0; s < kLsStages; ++s) mbar_init(&sh.st_req[s], 1);
+    for (int s = 0; s < Cfg::kStages; ++s) mbar_init(&sh.st_req[s], 1);
     fence_mbar_init();
   }
   __syncthreads();
-  if (warp == kLsThreads / 32) {  // producer warp
+  if (warp == Cfg::kConsumers / 32) {  // producer warp
     if (lane == 0) ls_producer(sh, p, &map_a, &map_b, ws, ctl);
     return;
   }
-  if (warp == kLsThreads / 32 + 1) {  // look-back warp
+  if (warp == Cfg::kConsumers / 32 + 1) {  // look-back warp
     ls_lookback_warp(sh, ws, ctl, lane);
     return;
   }
-  if (warp == kLsThreads / 32 + 2) {  // store warp
+  if (warp == Cfg::kConsumers / 32 + 2) {  // store warp
     if (lane == 0) ls_store_warp(sh, &map_h, ws, ctl);
     return;
   }
@@ -301,13 +326,13 @@ __global__ void __launch_bounds__(kLsBlock, SSM_LS_MIN_BLOCKS)
   // per-thread results of pass 1 of the previous tile, consumed by its pass 2
   Pair prev_excl{1.f, 0.f}, prev_wp{1.f, 0.f};
   int64_t prev_tile = -1, prev_r0 = 0;
-  for (int it = 0;; ++it) {
-    const int st = it % kLsStages;
+  for (int it = grp;; it += Cfg::kGroups) {
+    const int st = it % Cfg::kStages;
     // A wait that gave up in any consumer stops all of them, so that none is left behind in
     // a later barrier.
-    const bool got = mbar_wait(&sh.full[st], (uint32_t)(it / kLsStages) & 1u, ctl.spin_limit_ns);
-    const bool gave_up = named_bar_any(kLsConsumerBar, kLsThreads, !got);
-    if (gave_up && threadIdx.x == 0) record_error(ws.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
+    const bool got = mbar_wait(&sh.full[st], (uint32_t)(it / Cfg::kStages) & 1u, ctl.spin_limit_ns);
+    const bool gave_up = named_bar_any(cbar, kLsThreads, !got);
+    if (gave_up && t == 0) record_error(ws.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
     const int64_t tile = gave_up ? ws.tiles : sh.tile[st];  // ws.tiles: stop
     const bool valid = tile < ws.tiles;  // uniform across the consumers
     Pair cur_excl{1.f, 0.f}, cur_wp{1.f, 0.f};
@@ -365,39 +390,41 @@ __global__ void __launch_bounds__(kLsBlock, SSM_LS_MIN_BLOCKS)
       }
       cur_excl = shfl_up(inc, 1);
       if (lane == 0) cur_excl = Pair{1.f, 0.f};
-      if (lane == 31) sh.warp_agg[it & 1][warp] = inc;
-      named_bar_sync(kLsConsumerBar, kLsThreads);
+      const int gw = t >> 5;  // warp within the group
+      if (lane == 31) sh.warp_agg[grp][(it / Cfg::kGroups) & 1][gw] = inc;
+      named_bar_sync(cbar, kLsThreads);
       Pair tile_agg{1.f, 0.f};
 #pragma unroll
       for (int w = 0; w < kLsThreads / 32; ++w) {
-        if (w == warp) cur_wp = tile_agg;
-        tile_agg = combine(tile_agg, sh.warp_agg[it & 1][w]);
+        if (w == gw) cur_wp = tile_agg;
+        tile_agg = combine(tile_agg, sh.warp_agg[grp][(it / Cfg::kGroups) & 1][w]);
       }
-      if (threadIdx.x == 0) {
+      if (t == 0) {
         const bool absolute = (tile == 0) || (tile_agg.a == 0.f);
         if (tile != ctl.stall_tile)
           st_relaxed_desc(&ws.desc[tile], make_flag(ctl.epoch, absolute ? kFlagPrefix : kFlagAggregate),
                           absolute ? 0.f : tile_agg.a, tile_agg.b);
-        LsJob& job = sh.job[it & 1];
+        LsJob& job = sh.job[it % Cfg::kJobs];
         job.tile = tile;
         job.r0 = cur_r0;
         job.agg = tile_agg;
         job.absolute = absolute;
-        mbar_arrive(&sh.lb_req[it & 1]);
+        mbar_arrive(&sh.lb_req[it % Cfg::kJobs]);
       }
-    } else if (threadIdx.x == 0) {
-      sh.job[it & 1].tile = ws.tiles;  // stop the look-back warp
-      mbar_arrive(&sh.lb_req[it & 1]);
+    } else if (t == 0) {
+      sh.job[it % Cfg::kJobs].tile = ws.tiles;  // stop the look-back warp
+      mbar_arrive(&sh.lb_req[it % Cfg::kJobs]);
     }
 
-    // ================= pass 2 of the previous tile: apply its prefix, store ================
+    // ======= pass 2 of this group's previous tile: apply its prefix, store ===================
     if (prev_tile >= 0) {
-      const int ps = (it - 1) % kLsStages;
-      const int pj = (it - 1) & 1;
+      const int pit = it - Cfg::kGroups;
+      const int ps = pit % Cfg::kStages;
+      const int pj = pit % Cfg::kJobs;
       float x = __int_as_float(0x7fc00000);
-      if (mbar_wait(&sh.lb_done[pj], (uint32_t)((it - 1) >> 1) & 1u, ctl.spin_limit_ns)) {
+      if (mbar_wait(&sh.lb_done[pj], (uint32_t)(pit / Cfg::kJobs) & 1u, ctl.spin_limit_ns)) {
         x = sh.job[pj].prefix;
-      } else if (threadIdx.x == 0) {
+      } else if (t == 0) {
         record_error(ws.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
       }
       const int64_t tile_base = prev_tile * kLsTile;
@@ -450,14 +477,14 @@ __global__ void __launch_bounds__(kLsBlock, SSM_LS_MIN_BLOCKS)
         }
       }
       if (in_map) fence_proxy_async_smem();
-      named_bar_sync(kLsConsumerBar, kLsThreads);
-      if (threadIdx.x == 0) {  // hand the stage to the store warp (no store for the tail-only tile)
+      named_bar_sync(cbar, kLsThreads);
+      if (t == 0) {  // hand the stage to the store warp (no store for the tail-only tile)
         sh.st_line0[ps] = line0 < p.lines ? line0 : (int64_t)0x7fffffff;
         mbar_arrive(&sh.st_req[ps]);
       }
     }
     if (!valid) {
-      if (threadIdx.x == 0) {  // stop the store warp through the (dataless) sentinel stage
+      if (t == 0) {  // stop the store warp through the (dataless) sentinel stage
         sh.st_line0[st] = -1;
         mbar_arrive(&sh.st_req[st]);
       }
@@ -468,12 +495,43 @@ __global__ void __launch_bounds__(kLsBlock, SSM_LS_MIN_BLOCKS)
     prev_excl = cur_excl;
     prev_wp = cur_wp;
   }
+  named_bar_sync(kLsConsumerBar + Cfg::kGroups, Cfg::kConsumers);  // every group is done
   if (threadIdx.x == 0) retire_tile(ws.hdr, gridDim.x);
 }
 
-int g_ls_grid[64] = {0};
+// Grid (resident CTAs: every CTA of a launch runs at once) per device and CTA shape.
+int g_ls_grid[2][64] = {};
+
+template <class Cfg>
+cudaError_t launch_cfg(int slot, int dev, const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_h,
+                       const LsArgs& p, const LinscanWorkspace& ws, const LookbackCtl& ctl, cudaStream_t s) {
+  cudaError_t e;
+  const size_t smem = sizeof(LsShared<Cfg>) + 1024;  // + alignment slack
+  if (g_ls_grid[slot][dev] == 0) {
+    e = cudaFuncSetAttribute(linscan_lookback_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int sms = 0, per_sm = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, linscan_lookback_kernel<Cfg>, Cfg::kBlock,
+                                                           smem)) != cudaSuccess)
+      return e;
+    g_ls_grid[slot][dev] = sms * (per_sm > 0 ? per_sm : 1);
+  }
+  const int64_t cap = g_ls_grid[slot][dev];
+  const unsigned grid = (unsigned)(ws.tiles < cap ? ws.tiles : cap);
+  linscan_lookback_kernel<Cfg><<<grid, Cfg::kBlock, smem, s>>>(map_a, map_b, map_h, p, ws, ctl);
+  return cudaGetLastError();
+}
 
 }  // namespace
+
+// Rows of at least this many tiles take the long-row CTA shape.  Where rows hold several
+// tiles, a tile's prefix comes from look-back over tiles that other CTAs are still scanning,
+// and two tiles' time for it pays; where most tiles hold a row start, their prefixes are
+// absolute at once and two CTAs per SM hide the loads better.
+#ifndef SSM_LS_LONG_ROW_TILES
+#define SSM_LS_LONG_ROW_TILES 4
+#endif
 
 cudaError_t launch_linscan(const float* a, const float* b, float* h, int64_t rows, int64_t len,
                            const LinscanWorkspace& ws, const LookbackCtl& ctl, cudaStream_t s) {
@@ -497,21 +555,9 @@ cudaError_t launch_linscan(const float* a, const float* b, float* h, int64_t row
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64) return cudaErrorInvalidDevice;
-  const size_t smem = sizeof(LsShared) + 1024;  // + alignment slack
-  if (g_ls_grid[dev] == 0) {
-    e = cudaFuncSetAttribute(linscan_lookback_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    int sms = 0, per_sm = 0;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, linscan_lookback_kernel, kLsBlock, smem)) !=
-        cudaSuccess)
-      return e;
-    g_ls_grid[dev] = sms * (per_sm > 0 ? per_sm : 1);
-  }
-  const int64_t cap = g_ls_grid[dev];
-  const unsigned grid = (unsigned)(ws.tiles < cap ? ws.tiles : cap);
-  linscan_lookback_kernel<<<grid, kLsBlock, smem, s>>>(map_a, map_b, map_h, p, ws, ctl);
-  return cudaGetLastError();
+  if (len >= (int64_t)SSM_LS_LONG_ROW_TILES * kLsTile)
+    return launch_cfg<LsLongRows>(0, dev, map_a, map_b, map_h, p, ws, ctl, s);
+  return launch_cfg<LsShortRows>(1, dev, map_a, map_b, map_h, p, ws, ctl, s);
 }
 
 }  // namespace ssm

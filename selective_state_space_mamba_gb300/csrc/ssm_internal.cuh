@@ -357,14 +357,8 @@ struct LinscanWorkspace {
 #ifndef SSM_LS_SPLIT
 #define SSM_LS_SPLIT 2
 #endif
-#ifndef SSM_LS_STAGES
-#define SSM_LS_STAGES 3
-#endif
 #ifndef SSM_LS_STREAM_HINT  // a, b and h streamed through L2 with evict-first priority
 #define SSM_LS_STREAM_HINT 1
-#endif
-#ifndef SSM_LS_MIN_BLOCKS
-#define SSM_LS_MIN_BLOCKS 2
 #endif
 constexpr int kLsLines = SSM_LS_LINES;                // 128-byte lines (32 floats) per tile
 constexpr int kLsRow = 32;                            // elements per line
@@ -372,7 +366,6 @@ constexpr int kLsSplit = SSM_LS_SPLIT;                // consumer threads per li
 constexpr int kLsElems = kLsRow / kLsSplit;           // consecutive elements per consumer thread
 constexpr int kLsThreads = kLsLines * kLsSplit;       // consumer threads
 constexpr int kLsTile = kLsLines * kLsRow;            // elements per tile
-constexpr int kLsStages = SSM_LS_STAGES;              // shared-memory stages of the producer ring
 LinscanWorkspace linscan_workspace_layout(int64_t n, void* base);
 
 // Raises `func`'s dynamic shared-memory limit to at least `bytes` on the current device, with

@@ -47,7 +47,8 @@ def test_ragged_workloads(cuda_lib, shape):
 
 
 @pytest.mark.parametrize("rows,length", [(1, 1), (7, 3), (5, TILE - 1), (5, TILE), (5, TILE + 1), (2, 2 * TILE - 1),
-                                         (3, 3 * TILE + 17), (1, 12345), (33, 1000), (2, 64 * TILE + 5)])
+                                         (3, 3 * TILE + 17), (4, 4 * TILE - 1), (3, 4 * TILE + 17), (1, 12345),
+                                         (33, 1000), (2, 64 * TILE + 5)])
 def test_small_and_ragged(cuda_lib, rows, length):
     inp = synth.scan_inputs(rows, length, seed=rows * 1000003 + length)
     h = gpu_scan(inp["a"], inp["b"])
