@@ -16,7 +16,7 @@
 //     a TMA tensor store.  Loads and stores are fully coalesced and asynchronous.
 //   * persistent, warp-specialised CTAs: one producer warp claims tiles (atomic counter) and
 //     fills a ring of shared-memory stages ("full" / "empty" mbarriers).  For rows of several
-//     tiles (one CTA per SM, 6 stages) two groups of consumer warps take the CTA's tiles in
+//     tiles (one CTA per SM, 7 stages) two groups of consumer warps take the CTA's tiles in
 //     turn (for short rows, two CTAs per SM, 3 stages and one group); one look-back
 //     warp resolves tile i's prefix while the group that owns it runs the first pass of its
 //     next tile, i + 2 (its second pass then re-reads tile i from its stage), so the
@@ -87,7 +87,10 @@ struct LsCfg {
   static constexpr int kConsumers = G * kLsThreads;
   static constexpr int kBlock = kConsumers + 96;  // consumer warps + producer, look-back and store warps
 };
-using LsLongRows = LsCfg<2, 6, 1>;   // one CTA per SM (192 KB of stages)
+#ifndef SSM_LS_LONG_STAGES
+#define SSM_LS_LONG_STAGES 7
+#endif
+using LsLongRows = LsCfg<2, SSM_LS_LONG_STAGES, 1>;  // one CTA per SM (224 KB of stages)
 using LsShortRows = LsCfg<1, 3, 2>;  // two CTAs per SM (96 KB of stages each)
 
 template <class Cfg>
@@ -105,6 +108,7 @@ struct LsShared {
   Pair warp_agg[Cfg::kGroups][2][kLsThreads / 32];
 };
 static_assert(sizeof(LsStage) % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+static_assert(sizeof(LsShared<LsLongRows>) + 1024 <= 227 * 1024, "the long-row ring must fit one CTA's shared memory");
 
 constexpr uint32_t kLsConsumerBar = 1;       // named barrier of consumer group g: 1 + g
 

@@ -36,6 +36,10 @@
 // math warps leave together; the CTA then drains, frees its TMEM and returns.
 #include "tc_common.cuh"
 
+#ifndef SSM_SCAN_Y_EVICT_FIRST  // y is written once: evict-first priority in L2
+#define SSM_SCAN_Y_EVICT_FIRST 1
+#endif
+
 namespace ssm {
 namespace {
 
@@ -547,7 +551,11 @@ __global__ void __launch_bounds__(kScThreads, 1)
       named_bar_sync(kScEpiBar, kScEpi);
       if (et == 0) {
         mbar_arrive(&bars[kYFree + b]);  // accumulator set b may be overwritten
+#if SSM_SCAN_Y_EVICT_FIRST
+        tc::tma_store_3d_hint(&map_y, base + L.y0, h * 64, tok0 + i0, (int)bi, l2_evict_first_policy());
+#else
         tc::tma_store_3d(&map_y, base + L.y0, h * 64, tok0 + i0, (int)bi);
+#endif
         bulk_commit();
       }
     }
