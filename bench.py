@@ -359,8 +359,7 @@ def run_ours(args, world, rank, local):
         "dtype": "bf16",
         "data": "synthetic (seeded numpy PCG64; distributions of the pages' workloads)",
         "config": {
-            "workload": (f"ssd_fwd b{SSD.batch} L{SSD.seqlen} nh{SSD.nheads} H{SSD.headdim} S{SSD.dstate} "
-                         f"G{SSD.ngroups} chunk{SSD.chunk} bf16/fp32-acc + linscan {SCAN.rows}x{SCAN.length} f32"),
+            "workload": workload_name(),
             "step": "ssd_fwd (4 kernels) then linscan_fwd (1 kernel); value from the ssd_fwd events",
             "per_kernel": "a second timed pass of the same steps with per-launch events",
             "l2": "inputs larger than L2, and L2 flushed by a 256 MiB write before each timed step",
@@ -581,11 +580,16 @@ def oracle_sample(ssd_np, scan_np, budget_s, unit_batch):
     }
 
 
+def workload_name() -> str:
+    """The one workload string both arms report."""
+    return (f"ssd_fwd b{SSD.batch} L{SSD.seqlen} nh{SSD.nheads} H{SSD.headdim} S{SSD.dstate} "
+            f"G{SSD.ngroups} chunk{SSD.chunk} bf16/fp32-acc + linscan {SCAN.rows}x{SCAN.length} f32")
+
+
 def run_reference(args):
     """The float64 oracle timed on the host cores, on this bench's workload, metric and unit:
     each step is a bounded sample (a few whole (batch, head) units of the SSD workload)."""
     ssd_np = synth.ssd_inputs(SSD)
-    scan_np = synth.scan_inputs(SCAN.rows, SCAN.length, seed=synth.WORKLOAD_SEED[SCAN.name])
     from oracle import native
     threads = native.max_threads()
     per_step = max(1, threads)
@@ -607,8 +611,9 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded numpy PCG64)",
-            "config": {"workload": f"ssd_fwd b{SSD.batch} L{SSD.seqlen} nh{SSD.nheads} H{SSD.headdim} "
-                                   f"S{SSD.dstate} G{SSD.ngroups} (float64 oracle, sampled units)"},
+            "config": {"workload": workload_name(),
+                       "timed": "float64 oracle on sampled whole (batch, head) units of the ssd_fwd part; "
+                                "value is the ssd_fwd tokens/s, as in the CUDA arm"},
             "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
