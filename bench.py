@@ -619,6 +619,54 @@ def run_reference(args):
             "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_ssd_configs(args):
+    """Context beside the headline: every bf16 SSD workload (b8 L2048 nh24, b4 L8192 nh80,
+    b1 L131072 nh32 G8) timed alone with its tuned plan, L2 flushed before each forward, one
+    JSON line each.  Median of `steps` forwards; per-kernel times from the library's events."""
+    import torch
+    import selective_state_space_mamba_gb300 as ssm
+    peaks, _ = load_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for shape in (synth.SSD_B8_L2048, synth.SSD_B4_L8192, synth.SSD_B1_L131072):
+        d = device_inputs(torch, synth.ssd_inputs(shape), shape.dtype)
+        y = torch.empty_like(d["x"])
+        hf = torch.empty(shape.batch, shape.nheads, shape.headdim, shape.dstate, dtype=torch.float32, device="cuda")
+
+        def call():
+            ssm.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], chunk=shape.chunk, y=y, h_final=hf)
+
+        plan, _ = ssm.tune_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], chunk=shape.chunk,
+                                   reps=5, y=y, h_final=hf)
+        for _ in range(max(3, args.warmup)):
+            flush.fill_(1)
+            call()
+        ms = []
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            call()
+            e1.record()
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        with ssm.KernelTimer(max_launches=8 * args.steps + 8) as kt:
+            for i in range(args.steps):
+                flush.fill_(i & 0xff)
+                call()
+            torch.cuda.synchronize()
+        if ssm.check_device_status(kind="ssd"):
+            raise RuntimeError(f"device status error in {shape.name}")
+        med = float(np.median(ms))
+        roof_ms = ssd_model_b_bytes(shape) / (peaks["hbm_gbs"] * 1e9) * 1e3
+        print(json.dumps({"workload": shape.name, "plan": plan, "ms": round(med, 4),
+                          "tokens_per_s": round(shape.batch * shape.seqlen / (med * 1e-3), 1),
+                          "model_B_roofline_ms": round(roof_ms, 4), "roofline_frac": round(roof_ms / med, 4),
+                          "per_kernel_us": {k: round(kt.ms[k] / kt.launches[k] * 1e3, 1)
+                                            for k in kt.ms if kt.launches.get(k)}}), flush=True)
+        del d, y, hf
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -628,6 +676,8 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=15.0, help="time budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ssd-configs", action="store_true",
+                    help="instead of the bench line: time every bf16 SSD workload alone, one JSON line each")
     ap.add_argument("--plan", choices=("tune", "rules"), default="tune",
                     help="ssd_fwd plan: tuned by measurement first (default) or the rules of thumb")
     args = ap.parse_args()
@@ -640,6 +690,9 @@ def main():
         print(json.dumps(run_reference(args)))
         return
 
+    if args.ssd_configs:
+        run_ssd_configs(args)
+        return
     world, rank, local = dist_setup(args)
     out, ssd_np, scan_np = run_ours(args, world, rank, local)
     if not args.no_e2e:
