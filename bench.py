@@ -621,13 +621,16 @@ def run_reference(args):
 
 def run_ssd_configs(args):
     """Context beside the headline: every bf16 SSD workload (b8 L2048 nh24, b4 L8192 nh80,
-    b1 L131072 nh32 G8) timed alone with its tuned plan, L2 flushed before each forward, one
-    JSON line each.  Median of `steps` forwards; per-kernel times from the library's events."""
+    b1 L131072 nh32 G8) timed alone with its tuned plan (or --plan rules / --plan-id), L2
+    flushed before each forward, one JSON line each.  Median of `steps` forwards; per-kernel
+    times from the library's events."""
     import torch
     import selective_state_space_mamba_gb300 as ssm
     peaks, _ = load_peaks()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     for shape in (synth.SSD_B8_L2048, synth.SSD_B4_L8192, synth.SSD_B1_L131072):
+        if args.ssd_workload and shape.name != args.ssd_workload:
+            continue
         d = device_inputs(torch, synth.ssd_inputs(shape), shape.dtype)
         y = torch.empty_like(d["x"])
         hf = torch.empty(shape.batch, shape.nheads, shape.headdim, shape.dstate, dtype=torch.float32, device="cuda")
@@ -635,8 +638,15 @@ def run_ssd_configs(args):
         def call():
             ssm.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], chunk=shape.chunk, y=y, h_final=hf)
 
-        plan, _ = ssm.tune_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], chunk=shape.chunk,
-                                   reps=5, y=y, h_final=hf)
+        if args.plan_id is not None:  # a fixed plan (profiler runs of one path)
+            plan = args.plan_id
+            ssm.set_ssd_fwd_plan(d["x"], d["B"], shape.chunk, plan)
+        elif args.plan == "tune":
+            plan, _ = ssm.tune_ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], chunk=shape.chunk,
+                                       reps=5, y=y, h_final=hf)
+        else:
+            plan = -1
+            ssm.set_ssd_fwd_plan(d["x"], d["B"], shape.chunk, -1)
         for _ in range(max(3, args.warmup)):
             flush.fill_(1)
             call()
@@ -678,6 +688,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ssd-configs", action="store_true",
                     help="instead of the bench line: time every bf16 SSD workload alone, one JSON line each")
+    ap.add_argument("--ssd-workload", default=None, help="with --ssd-configs: only the workload of this name")
+    ap.add_argument("--plan-id", type=int, default=None,
+                    help="with --ssd-configs: this ssd_fwd plan id instead of tuning (see ssm_ssd_fwd_set_plan)")
     ap.add_argument("--plan", choices=("tune", "rules"), default="tune",
                     help="ssd_fwd plan: tuned by measurement first (default) or the rules of thumb")
     args = ap.parse_args()

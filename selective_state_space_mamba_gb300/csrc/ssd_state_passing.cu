@@ -102,18 +102,15 @@ __global__ void __launch_bounds__(kSpThreads) ssd_state_passing_kernel(const flo
   float4 X;  // state entering the tile's first chunk
   if (ctile == 0) {
     X = h0 ? *reinterpret_cast<const float4*>(h0 + bh * HS + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-    if (!stalled) {
-      *reinterpret_cast<float4*>(my_inc) = f4_fma(exp2f(lg_tile), X, agg);
-      __threadfence();
-    }
+    if (!stalled) *reinterpret_cast<float4*>(my_inc) = f4_fma(exp2f(lg_tile), X, agg);
+    // The CTA barrier orders every thread's store before thread 0's release store of the flag,
+    // and a release is cumulative: a reader that acquires the flag sees all of them.  (No
+    // fence per thread: each would wait for its own store to reach L2.)
     __syncthreads();
     if (threadIdx.x == 0 && !stalled) st_release_u64(&ws.flags[tile], make_flag(ctl.epoch, kFlagPrefix));
   } else {
-    if (!stalled) {
-      *reinterpret_cast<float4*>(my_agg) = agg;
-      __threadfence();
-    }
-    __syncthreads();
+    if (!stalled) *reinterpret_cast<float4*>(my_agg) = agg;
+    __syncthreads();  // as above: barrier, then one release store
     if (threadIdx.x == 0 && !stalled) st_release_u64(&ws.flags[tile], make_flag(ctl.epoch, kFlagAggregate));
 
     // ---- look-back: compose predecessors newest to oldest until a published prefix ----
@@ -168,11 +165,8 @@ __global__ void __launch_bounds__(kSpThreads) ssd_state_passing_kernel(const flo
       __syncthreads();  // warp 0 rewrites s_last / s_found
     }
     X = acc_b;
-    if (!stalled) {
-      *reinterpret_cast<float4*>(my_inc) = f4_fma(exp2f(lg_tile), X, agg);
-      __threadfence();
-    }
-    __syncthreads();
+    if (!stalled) *reinterpret_cast<float4*>(my_inc) = f4_fma(exp2f(lg_tile), X, agg);
+    __syncthreads();  // as above: barrier, then one release store
     if (threadIdx.x == 0 && !stalled) st_release_u64(&ws.flags[tile], make_flag(ctl.epoch, kFlagPrefix));
   }
 
