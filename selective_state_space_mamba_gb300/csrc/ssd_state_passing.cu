@@ -9,11 +9,12 @@
 //
 // Here the loop over chunks is a scan under the same affine pair combine as the scalar scan
 // ("Selective-scan CUDA kernels", "The problem"), run as a decoupled look-back: each tile is
-// kSpElems state entries of one (batch, head) across up to kSpChunks chunks.  A tile
-// publishes its aggregate state vector (flag A), looks back over predecessor tiles of the
-// same chain (a warp inspects 32 flags at once, atomic claim order guarantees progress),
-// publishes its inclusive state (flag P), then writes h_in for each of its chunks.  The
-// decay of an aggregate is not published: every tile recomputes it from G.
+// kSpElems state entries of one (batch, head) across up to kSpChunks chunks, whose increments
+// it stages in shared memory.  A tile publishes its aggregate state vector (flag A), looks
+// back over predecessor tiles of the same chain (a warp inspects 32 flags at once, atomic
+// claim order guarantees progress), publishes its inclusive state (flag P), then writes h_in
+// for each of its chunks.  The decay of an aggregate is not published: every tile recomputes
+// it from G.
 //
 // When there are enough state entries to fill the GPU without splitting the chunk axis (the
 // usual case: batch x heads x H x S in the millions), the recurrence runs as written instead:
@@ -41,17 +42,29 @@ template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16*
   *reinterpret_cast<uint2*>(p) = u;
 }
 
+// The tile's chunk increments (kSpChunks rows of kSpElems floats, 64 KB) are staged in shared
+// memory by bulk copies rather than held in registers, so three CTAs fit an SM and their
+// copies, look-backs and h_in stores overlap.
+constexpr int kSpMinBlocks = 3;
+constexpr size_t kSpSmem = sizeof(float) * kSpChunks * kSpElems;
+
 template <typename HinT>
-__global__ void __launch_bounds__(kSpThreads) ssd_state_passing_kernel(const float* __restrict__ h0,
-                                                                        float* __restrict__ h_final, SsdDims d,
-                                                                        SsdWorkspace ws, LookbackCtl ctl_call) {
+__global__ void __launch_bounds__(kSpThreads, kSpMinBlocks)
+    ssd_state_passing_kernel(const float* __restrict__ h0, float* __restrict__ h_final, SsdDims d, SsdWorkspace ws,
+                             LookbackCtl ctl_call) {
+  extern __shared__ float4 sp_sc[];  // [kSpChunks][kSpThreads]: chunk k, this thread's 4 entries
+  __shared__ uint64_t s_bar;
   __shared__ uint32_t s_tile;
   __shared__ int s_last, s_found;
   griddep_launch_dependents();
   griddep_wait();  // S_c, G and the claim counter come from the previous kernels
   const LookbackCtl ctl = device_epoch(ctl_call, ws.hdr);
 
-  if (threadIdx.x == 0) s_tile = claim_tile(ws.hdr);
+  if (threadIdx.x == 0) {
+    s_tile = claim_tile(ws.hdr);
+    mbar_init(&s_bar, 1);
+    fence_mbar_init();
+  }
   __syncthreads();
   const int64_t tile = s_tile;
   if (tile >= ws.sp_tiles) {  // claim counter not reset: refuse rather than index past the workspace
@@ -75,23 +88,28 @@ __global__ void __launch_bounds__(kSpThreads) ssd_state_passing_kernel(const flo
   const int e = slice * kSpElems + threadIdx.x * 4;
   const float* Grow = ws.G + bh * d.lpad + (d.chunk - 1);  // G_last of chunk c at Grow[c * chunk]
 
-  // ---- load this tile's chunk increments and decays ----
-  float4 sc[kSpChunks];
+  // ---- this tile's chunk increments (shared memory) and decays (registers) ----
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&s_bar, (uint32_t)(nk * kSpElems * sizeof(float)));
+    for (int k = 0; k < nk; ++k)
+      bulk_g2s(sp_sc + k * kSpThreads, ws.Sc + ((bi * nc + c0 + k) * d.nheads + h) * HS + slice * kSpElems,
+               (uint32_t)(kSpElems * sizeof(float)), &s_bar);
+  }
   float lg[kSpChunks];
 #pragma unroll
-  for (int k = 0; k < kSpChunks; ++k) {
-    if (k < nk) {
-      const int64_t c = c0 + k;
-      sc[k] = __ldcs(reinterpret_cast<const float4*>(ws.Sc + ((bi * nc + c) * d.nheads + h) * HS + e));
-      lg[k] = Grow[c * d.chunk];
-    }
+  for (int k = 0; k < kSpChunks; ++k)
+    if (k < nk) lg[k] = Grow[(c0 + k) * d.chunk];
+  if (!mbar_wait(&s_bar, 0, ctl.spin_limit_ns)) {
+    record_error(ws.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
+    mbar_wait(&s_bar, 0, ctl.spin_limit_ns);  // the copies land in this CTA's shared memory: wait for them
   }
+  const float4* sc = sp_sc + threadIdx.x;  // chunk k at sc[k * kSpThreads]
   float4 agg = make_float4(0.f, 0.f, 0.f, 0.f);
   float lg_tile = 0.f;
 #pragma unroll
   for (int k = 0; k < kSpChunks; ++k) {
     if (k < nk) {
-      agg = f4_fma(exp2f(lg[k]), agg, sc[k]);
+      agg = f4_fma(exp2f(lg[k]), agg, sc[k * kSpThreads]);
       lg_tile += lg[k];
     }
   }
@@ -177,7 +195,7 @@ __global__ void __launch_bounds__(kSpThreads) ssd_state_passing_kernel(const flo
     if (k < nk) {
       const int64_t c = c0 + k;
       store4<HinT>(hin + ((bi * nc + c) * d.nheads + h) * HS + e, X);
-      X = f4_fma(exp2f(lg[k]), X, sc[k]);
+      X = f4_fma(exp2f(lg[k]), X, sc[k * kSpThreads]);
     }
   }
   if (h_final && c0 + nk == nc) *reinterpret_cast<float4*>(h_final + bh * HS + e) = X;
@@ -273,10 +291,17 @@ cudaError_t launch_ssd_state_passing(const float* h0, float* h_final, const SsdD
                         d, ws);
     return launch_pdl(ssd_state_passing_seq_kernel<float>, dim3(grid), dim3(kSeqThreads), 0, s, h0, h_final, d, ws);
   }
-  if (d.dtype == SSM_BF16)
-    return launch_pdl(ssd_state_passing_kernel<__nv_bfloat16>, dim3((unsigned)ws.sp_tiles), dim3(kSpThreads), 0, s,
-                      h0, h_final, d, ws, ctl);
-  return launch_pdl(ssd_state_passing_kernel<float>, dim3((unsigned)ws.sp_tiles), dim3(kSpThreads), 0, s, h0,
+  cudaError_t e;
+  if (d.dtype == SSM_BF16) {
+    if ((e = ensure_smem_limit(reinterpret_cast<const void*>(ssd_state_passing_kernel<__nv_bfloat16>), kSpSmem)) !=
+        cudaSuccess)
+      return e;
+    return launch_pdl(ssd_state_passing_kernel<__nv_bfloat16>, dim3((unsigned)ws.sp_tiles), dim3(kSpThreads), kSpSmem,
+                      s, h0, h_final, d, ws, ctl);
+  }
+  if ((e = ensure_smem_limit(reinterpret_cast<const void*>(ssd_state_passing_kernel<float>), kSpSmem)) != cudaSuccess)
+    return e;
+  return launch_pdl(ssd_state_passing_kernel<float>, dim3((unsigned)ws.sp_tiles), dim3(kSpThreads), kSpSmem, s, h0,
                     h_final, d, ws, ctl);
 }
 
