@@ -204,7 +204,12 @@ __global__ void __launch_bounds__(kSpThreads, kSpMinBlocks)
 
 constexpr int kSeqThreads = 256;
 constexpr int kSeqAhead = 8;             // chunk increments in flight per thread
-constexpr int64_t kSeqMinGroups = 32768;  // fewer four-entry groups than this: the look-back kernel
+// Fewer four-entry groups than this: the look-back kernel.  A thread of the sequential kernel
+// takes about 0.5 us per chunk (its chain of dependent steps), so the kernel needs about
+// 6.8 TB/s x 0.5 us / 24 B (S_c read + h_in written per entry and chunk) ~ 140 K groups to
+// run at HBM speed; with fewer it is latency bound (b1 L131072 nh32: 65,536 groups, 268 us
+// against 178 us for the look-back kernel).
+constexpr int64_t kSeqMinGroups = 131072;
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gsrc) : "memory");
