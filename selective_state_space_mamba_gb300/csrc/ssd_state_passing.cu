@@ -153,9 +153,10 @@ __global__ void __launch_bounds__(kSpThreads, kSpMinBlocks)
         }
       }
       __syncthreads();
+      // The lanes of warp 0 acquired the flags; the CTA barrier above carries that ordering to
+      // every thread of the CTA, whose loads below then see the published vectors.
       const int last = s_last;
       const int found = s_found;  // 0: all 32 were aggregates, 2: prefix, 3: gave up
-      __threadfence();
       for (int l = 0; l <= last; ++l) {
         const int64_t ct = newest - l;
         const int64_t t = ct * ws.sp_chains + chain;
