@@ -27,7 +27,8 @@
 // range per CTA (one CTA per SM, so every SM gets the same number of units, give or take
 // one); a CTA reloads B only where its range crosses into the next (batch, chunk, group).
 // CTA warps:
-//   warp 0      TMA producer: B when the group changes; X of the pair's two heads, 64 tokens
+//   warp 0      TMA producer: B when the group changes (two buffers, so the next group's B
+//               lands while the current group's MMAs run); X of the pair's two heads, 64 tokens
 //               at a time, with those tokens' G and dt and the chunk's last G, into a 4-stage
 //               ring
 //   warp 1      TMEM owner and MMA issuer (one thread): 2 x 4 MMAs (hi, lo) per stage, A from
@@ -52,7 +53,8 @@ constexpr int kCsWarps = 14;  // 0 producer, 1 MMA, 2-9 scalers, 10-13 epilogue
 constexpr int kCsThreads = kCsWarps * 32;
 constexpr int kCsMaxT = 256;
 constexpr int kCsKH = 64;         // tokens per stage
-constexpr int kCsStages = 8;   // X ring in shared memory (released once the scalers have read it)
+constexpr int kCsStages = 4;   // X ring in shared memory (released once the scalers have read it)
+constexpr int kCsBBufs = 2;    // B of two groups: the next group's B lands while this one's MMAs run
 constexpr int kCsAStages = 4;  // hi/lo ring in TMEM (released when the MMAs have read it)
 constexpr int kCsRowBytes = 128;  // 64 bf16 per swizzled row
 constexpr uint32_t kCsScaleBar = 1, kCsEpiBar = 2;  // scaler group g uses named barrier 1 + 2 g
@@ -82,7 +84,7 @@ struct CsLayout {
   __host__ __device__ explicit CsLayout(int T) {
     stage_bytes = 2u * kCsKH * kCsRowBytes;
     bm0 = kCsStages * stage_bytes;
-    epi0 = bm0 + 2u * T * kCsRowBytes;
+    epi0 = bm0 + kCsBBufs * 2u * T * kCsRowBytes;
     gd0 = epi0 + 4u * 32 * kCsRowBytes;
     wt0 = gd0 + kCsStages * 2u * kCsGdHead;
     bars = wt0 + kCsAStages * 2u * (kCsKH / 2) * 16u;
@@ -90,7 +92,7 @@ struct CsLayout {
   }
 };
 enum CsBar {
-  kBFull = 0, kBEmpty = 1, kXFull = 2, kXEmpty = kXFull + kCsStages, kAFull = kXEmpty + kCsStages, kAEmpty = kAFull + kCsAStages,
+  kBFull = 0, kBEmpty = kBFull + kCsBBufs, kXFull = kBEmpty + kCsBBufs, kXEmpty = kXFull + kCsStages, kAFull = kXEmpty + kCsStages, kAEmpty = kAFull + kCsAStages,
   kAccFull = kAEmpty + kCsAStages, kAccEmpty = kAccFull + 2, kDone = kAccEmpty + 2, kNumBars = kDone + 1
 };
 
@@ -176,15 +178,19 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             // B is read by every MMA of the previous group: the MMA thread releases it when it
             // moves on (this producer may be up to three rings ahead of the MMAs, so it waits on
             // a barrier of its own rather than on a ring's)
-            if (nreload > 0 && !mbar_wait(&bars[kBEmpty], (uint32_t)(nreload - 1) & 1u, ctl.spin_limit_ns)) {
+            // buffer nreload % 2 last held the B of reload nreload - 2
+            const int bb = nreload % kCsBBufs;
+            if (nreload >= kCsBBufs && !mbar_wait(&bars[kBEmpty + bb], (uint32_t)((nreload / kCsBBufs) - 1) & 1u,
+                                                  ctl.spin_limit_ns)) {
               ok = false;
               break;
             }
             ++nreload;
-            mbar_arrive_expect_tx(&bars[kBFull], 2u * T * kCsRowBytes);
+            unsigned char* bdst = base + L.bm0 + bb * 2u * T * kCsRowBytes;
+            mbar_arrive_expect_tx(&bars[kBFull + bb], 2u * T * kCsRowBytes);
             for (int sb = 0; sb < 2; ++sb)
-              tc::tma_load_3d(base + L.bm0 + sb * T * kCsRowBytes, &map_b, w.g * 128 + sb * 64, (int)(w.c * T),
-                              (int)w.bi, &bars[kBFull]);
+              tc::tma_load_3d(bdst + sb * T * kCsRowBytes, &map_b, w.g * 128 + sb * 64, (int)(w.c * T), (int)w.bi,
+                              &bars[kBFull + bb]);
             cur_grp = w.grp;
           }
           unsigned char* gd = base + L.gd0 + st * 2 * kCsGdHead;
@@ -217,10 +223,12 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         const CsUnit w = cs_unit(p, u);
         const int acc = q & 1;
         if (w.grp != cur_grp) {
-          if (nb > 0) tc::mma_commit(&bars[kBEmpty]);  // the previous group's B, once its MMAs are done
+          // the previous group's B buffer, once its MMAs are done
+          if (nb > 0) tc::mma_commit(&bars[kBEmpty + (nb - 1) % kCsBBufs]);
           ++nb;
           cur_grp = w.grp;
-          ok = mbar_wait(&bars[kBFull], (uint32_t)(nb - 1) & 1u, ctl.spin_limit_ns);
+          ok = mbar_wait(&bars[kBFull + (nb - 1) % kCsBBufs], (uint32_t)((nb - 1) / kCsBBufs) & 1u,
+                         ctl.spin_limit_ns);
         }
         if (ok && q >= 2) ok = mbar_wait(&bars[kAccEmpty + acc], (uint32_t)((q >> 1) - 1) & 1u, ctl.spin_limit_ns);
         for (int kh = 0; kh < nk && ok; ++kh, ++i) {
@@ -231,7 +239,8 @@ __global__ void __launch_bounds__(kCsThreads, 1)
           }
           tc::fence_after_sync();
           const uint32_t a_hi = tmem + kCsTmemA + 64u * as, a_lo = a_hi + 32;
-          const uint32_t b0 = smem_addr(base + L.bm0) + kh * kCsKH * kCsRowBytes;
+          const uint32_t b0 =
+              smem_addr(base + L.bm0) + ((nb - 1) % kCsBBufs) * 2u * T * kCsRowBytes + kh * kCsKH * kCsRowBytes;
 #pragma unroll
           for (int ks = 0; ks < kCsKH / 16; ++ks) {
             const uint32_t koff = ks * 16 * kCsRowBytes;  // 16 tokens = two 8-row groups of B
@@ -257,7 +266,11 @@ __global__ void __launch_bounds__(kCsThreads, 1)
         if (i > x) mbar_wait(&bars[kAEmpty + x], (uint32_t)(((i - 1 - x) / kCsAStages) & 1), ctl.spin_limit_ns);
       for (int x = 0; x < 2; ++x)
         if (nacc > x) mbar_wait(&bars[kAccFull + x], (uint32_t)(((nacc - 1 - x) / 2) & 1), ctl.spin_limit_ns);
-      if (nb > 1) mbar_wait(&bars[kBEmpty], (uint32_t)((nb - 2) & 1), ctl.spin_limit_ns);
+      // kBEmpty commits were made for groups 0 .. nb - 2, group j's on buffer j % 2
+      for (int x = 0; x < kCsBBufs; ++x) {
+        const int j = (nb - 2) - (((nb - 2) - x) % kCsBBufs + kCsBBufs) % kCsBBufs;
+        if (nb >= 2 && j >= 0) mbar_wait(&bars[kBEmpty + x], (uint32_t)(j / kCsBBufs) & 1u, ctl.spin_limit_ns);
+      }
     }
   } else if (warp < 10) {
     // ---------------- scale X by w, split into bf16 hi + lo parts, into TMEM ----------------
