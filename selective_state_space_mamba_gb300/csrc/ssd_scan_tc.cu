@@ -390,6 +390,14 @@ __global__ void __launch_bounds__(kScThreads, 1)
       if (mt == 0) fail();
       ok = false;
     }
+    if (ok) {
+      // The blocks above the diagonal are zero for every head: write them once into both P
+      // buffers (every P warp has read its CB columns: build_table's barrier came after).
+      tc::fence_after_sync();
+      const uint32_t z[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+      for (int b = 0; b < 2; ++b)
+        for (int Jp = quad + 1; Jp < 4; ++Jp) tc::tmem_st8(tmem + lane_base + col_p(b) + 16 * Jp + 8 * half, z);
+    }
     for (int k = 0; k < nh_run && ok; ++k) {
       const int st = k & 1, bf = k & 1;
       // this head's table is complete, and P[bf] has been read by the MMAs of head k - 2
@@ -405,15 +413,16 @@ __global__ void __launch_bounds__(kScThreads, 1)
       const float gi = g_s[i];
       const float ui = quad > 0 ? tc::ex2_approx(gi - g_s[i0 + 32 * quad]) : 0.f;  // triangle row factor
 
-      // ---- rectangle: X rows j < i0 scaled by f_j in place (two threads per row) ----
-      if (i0 > 0) {
-        const int j = mt >> 1;
+      // ---- rectangle: X rows j < i0 scaled by f_j in place, one row per thread of the warps
+      // of row quads 0 and 1, whose triangle rows hold the fewest blocks ----
+      if (i0 > 0 && quad < 2) {
+        const int j = half * 64 + quad * 32 + lane;
         const float f = v_s[kVRect + j];
         const uint32_t f2 = pack_bf16(f, f);
         unsigned char* xrow = stage + j * kRowB;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint4* q = reinterpret_cast<uint4*>(xrow + ((((mt & 1) * 4 + cc) ^ (j & 7)) << 4));
+        for (int cc = 0; cc < 8; ++cc) {
+          uint4* q = reinterpret_cast<uint4*>(xrow + (((cc + lane) & 7) << 4));  // rotated: spread over banks
           uint4 w = *q;
           w.x = mul_bf16x2(w.x, f2);
           w.y = mul_bf16x2(w.y, f2);
@@ -424,44 +433,43 @@ __global__ void __launch_bounds__(kScThreads, 1)
         fence_proxy_async_smem();
       }
 
-      // ---- triangle P for my row: bf16 pairs into P[bf] ----
+      // ---- triangle P for my row: bf16 pairs into P[bf].  Blocks Jp <= quad are nonzero; the
+      // two warps of a row quad take one 16-column half of each, so that both carry the same
+      // work (one half of the diagonal block and quad halves of off-diagonal blocks each) ----
 #pragma unroll
-      for (int Jp = half; Jp < 4; Jp += 2) {
-        const int cb = i0 + 32 * Jp;  // first column of the block
-        uint32_t pk[16];
-        if (Jp > quad) {  // entirely above the diagonal
+      for (int Jp = 0; Jp < 4; ++Jp) {
+        if (Jp > quad) break;  // the same for the whole warp
+        const int cb = i0 + 32 * Jp + 16 * half;  // first column of my half block
+        uint32_t cw[8];  // CB row segment as bf16 pairs
 #pragma unroll
-          for (int q = 0; q < 16; ++q) pk[q] = 0u;
-        } else {
-          uint32_t cw[16];  // CB row segment as bf16 pairs
+        for (int q = 0; q < 2; ++q) {
+          const uint4 w = *reinterpret_cast<const uint4*>(cb_smem + cb_chunk(r, (cb >> 3) + q));
+          cw[4 * q] = w.x; cw[4 * q + 1] = w.y; cw[4 * q + 2] = w.z; cw[4 * q + 3] = w.w;
+        }
+        uint32_t pk[8];
+        if (Jp < quad) {  // w = 2^(G_i - G_r) * dt_j 2^(G_r - G_j), both factors <= 1
+          const float4* vv = reinterpret_cast<const float4*>(v_s + kVTri + v_off(quad) + 32 * Jp + 16 * half);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const uint4 w = *reinterpret_cast<const uint4*>(cb_smem + cb_chunk(r, (cb >> 3) + q));
-            cw[4 * q] = w.x; cw[4 * q + 1] = w.y; cw[4 * q + 2] = w.z; cw[4 * q + 3] = w.w;
+            const float4 f = vv[q];
+            pk[2 * q] = mul_bf16x2(cw[2 * q], pack_bf16(ui * f.x, ui * f.y));
+            pk[2 * q + 1] = mul_bf16x2(cw[2 * q + 1], pack_bf16(ui * f.z, ui * f.w));
           }
-          if (Jp < quad) {  // w = 2^(G_i - G_r) * dt_j 2^(G_r - G_j), both factors <= 1
-            const float4* vv = reinterpret_cast<const float4*>(v_s + kVTri + v_off(quad) + 32 * Jp);
+        } else {  // diagonal 32 x 32 block: 2^(G_i + c_j), exponent -inf above the diagonal
+          const float4* cc4 = reinterpret_cast<const float4*>(v_s + kVDiag + 32 * Jp + 16 * half);
+          const int c0 = 16 * half;  // my columns are cb .. cb + 15; my row is column 32 Jp + lane
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const float4 f = vv[q];
-              pk[2 * q] = mul_bf16x2(cw[2 * q], pack_bf16(ui * f.x, ui * f.y));
-              pk[2 * q + 1] = mul_bf16x2(cw[2 * q + 1], pack_bf16(ui * f.z, ui * f.w));
-            }
-          } else {  // diagonal 32 x 32 block: 2^(G_i + c_j), exponent -inf above the diagonal
-            const float4* cc4 = reinterpret_cast<const float4*>(v_s + kVDiag + 32 * Jp);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const float4 cq = cc4[q];  // columns cb + 4q .. +3; my row is column cb + lane
-              const float w0 = tc::ex2_approx(4 * q <= lane ? gi + cq.x : -INFINITY);
-              const float w1 = tc::ex2_approx(4 * q + 1 <= lane ? gi + cq.y : -INFINITY);
-              const float w2 = tc::ex2_approx(4 * q + 2 <= lane ? gi + cq.z : -INFINITY);
-              const float w3 = tc::ex2_approx(4 * q + 3 <= lane ? gi + cq.w : -INFINITY);
-              pk[2 * q] = mul_bf16x2(cw[2 * q], pack_bf16(w0, w1));
-              pk[2 * q + 1] = mul_bf16x2(cw[2 * q + 1], pack_bf16(w2, w3));
-            }
+          for (int q = 0; q < 4; ++q) {
+            const float4 cq = cc4[q];
+            const float w0 = tc::ex2_approx(c0 + 4 * q <= lane ? gi + cq.x : -INFINITY);
+            const float w1 = tc::ex2_approx(c0 + 4 * q + 1 <= lane ? gi + cq.y : -INFINITY);
+            const float w2 = tc::ex2_approx(c0 + 4 * q + 2 <= lane ? gi + cq.z : -INFINITY);
+            const float w3 = tc::ex2_approx(c0 + 4 * q + 3 <= lane ? gi + cq.w : -INFINITY);
+            pk[2 * q] = mul_bf16x2(cw[2 * q], pack_bf16(w0, w1));
+            pk[2 * q + 1] = mul_bf16x2(cw[2 * q + 1], pack_bf16(w2, w3));
           }
         }
-        tc::tmem_st16(tmem + lane_base + col_p(bf) + 16 * Jp, pk);
+        tc::tmem_st8(tmem + lane_base + col_p(bf) + 16 * Jp + 8 * half, pk);
       }
       tc::tmem_st_wait();
       tc::fence_before_sync();

@@ -22,15 +22,17 @@
 // The per-chunk increments S_c never go to memory: against the chunk-state + state-passing
 // pair this saves writing and re-reading them (f32) entirely.
 //
-// Warps (448 threads):
-//   warp 0     TMA producer: per 64-token step, X of the pair's two heads, the step's rows of
-//              the group's B, and the step's G and dt with the chunk's last G, into a ring
+// Warps (480 threads):
+//   warp 0     TMA producer of X: per 64-token step, X of the pair's two heads with the step's
+//              G and dt and the chunk's last G into the X ring
 //   warp 1     TMEM owner and MMA issuer (one thread): per chunk, once S[q & 1] is free,
-//              2 x 4 MMAs (hi, lo) per step accumulating into it
-//   warps 2-9  scalers, two groups of four warps on alternate steps (one group's chain of wait,
-//              split and barrier overlaps the other's): a token row per thread, x w -> hi (in
-//              place) + lo
-//   warps 10-13 state warps, one state row per thread: h0 or the published state in, h_in out
+//              2 x 4 MMAs (hi, lo) per step accumulating into it, A from the operand ring
+//   warp 2     TMA producer of B: the step's rows of the group's B into the B ring
+//   warps 3-6  scalers, a token row per thread: the row to registers, the X slot handed back at
+//              once, x w -> hi + lo into the operand ring.  X is thus held only from its load
+//              to the scalers' read, and B and the operand from their fill to the MMAs'
+//              completion, instead of one stage holding all three from the load to the MMAs
+//   warps 7-14 state warps, two threads per state row: h0 or the published state in, h_in out
 //              per chunk, the decay and S folded in, h_final at a chain's end, the state
 //              published where a head ends
 // Every wait is bounded; on expiry the CTA records SSM_ERR_TIMEOUT, drains, frees its TMEM and
@@ -40,11 +42,16 @@
 namespace ssm {
 namespace {
 
-constexpr int kSfThreads = 448;  // warps 0 producer, 1 MMA, 2-9 scalers, 10-13 state
+constexpr int kSfScalers = 128;      // warps 3-6: one token row of one head per thread
+constexpr int kSfStateThreads = 256; // warps 7-14: two threads per state row
+constexpr int kSfScaler0 = 96;       // first scaler thread (warps 0-2: X producer, MMA, B producer)
+constexpr int kSfThreads = kSfScaler0 + kSfScalers + kSfStateThreads;
 constexpr int kSfKH = 64;         // tokens per step
-constexpr int kSfStages = 4;      // one chunk of 256 tokens in flight
+constexpr int kSfXS = 4;          // X slots (one chunk of 256 tokens in flight)
+constexpr int kSfBS = 3;          // B slots (B comes from L2: shared by every head of a group)
+constexpr int kSfOS = 2;          // operand (hi + lo) slots
 constexpr int kSfRowBytes = 128;  // 64 bf16 per swizzled row
-constexpr uint32_t kSfScaleBar = 1, kSfStateBar = 2;  // scaler group g: named barrier 1 + 2 g
+constexpr uint32_t kSfScaleBar = 1, kSfStateBar = 2;
 constexpr uint32_t kSfTmemCols = 512;  // h at 0, S[0] at 128, S[1] at 256
 constexpr uint32_t kSfGdHead = (2 * kSfKH + 4) * 4;  // G[64], dt[64], G[T-4 .. T-1] of one head
 
@@ -116,26 +123,38 @@ __host__ __device__ __forceinline__ SfSeg sf_seg(const SfRange& r, int s, int64_
   return g;
 }
 
-// Shared memory (offsets from a 1024-byte aligned base):
-//   stage[2] = { hi[2 heads][64 rows][128 B], lo[2 heads][64 rows][128 B],
-//                B[2 s blocks][64 rows][128 B] }                       all swizzled
-//   gd[2 stages][2 heads]
+// Shared memory (offsets from a 1024-byte aligned base), three rings:
+//   X[kSfXS]   X of the pair's two heads for one step: [2 heads][64 rows][128 B], swizzled;
+//              released as soon as the scalers hold it in registers
+//   B[kSfBS]   the step's rows of the group's B: [2 s blocks][64 rows][128 B], swizzled;
+//              released when the step's MMAs complete
+//   Op[kSfOS]  the weighted X of one step as bf16 hi and lo halves, each laid out like X;
+//              written by the scalers, released when the step's MMAs complete
+//   Hs         h_in of one chunk as bf16, [2 s blocks][128 rows][128 B], swizzled: the state
+//              warps write it here and one TMA store per s block takes it to memory, so
+//              that their 256-byte rows do not reach the load/store unit as scattered
+//              16-byte stores (these held up the scalers' shared-memory accesses)
+//   gd[kSfXS][2 heads]  G, dt and the chunk's last G of the step (travels with X)
 //   barriers, TMEM base, abort flag
 struct SfLayout {
-  uint32_t half_bytes, b_off, stage_bytes, gd0, bars, total;
+  uint32_t x_bytes, b0, op0, op_bytes, hs0, gd0, bars, total;
   __host__ __device__ SfLayout() {
-    half_bytes = 2u * kSfKH * kSfRowBytes;  // 16 KB
-    b_off = 2u * half_bytes;
-    stage_bytes = b_off + 2u * kSfKH * kSfRowBytes;  // 48 KB
-    gd0 = kSfStages * stage_bytes;
-    bars = gd0 + kSfStages * 2u * kSfGdHead;
-    total = bars + 24 * 8 + 16;
+    x_bytes = 2u * kSfKH * kSfRowBytes;  // 16 KB
+    b0 = kSfXS * x_bytes;
+    op0 = b0 + kSfBS * x_bytes;
+    op_bytes = 2u * x_bytes;
+    hs0 = op0 + kSfOS * op_bytes;
+    gd0 = hs0 + 2u * 128 * kSfRowBytes;
+    bars = gd0 + kSfXS * 2u * kSfGdHead;
+    total = bars + 32 * 8 + 16;
   }
 };
 enum SfBar {
-  kXFull = 0, kXScaled = kXFull + kSfStages, kXEmpty = kXScaled + kSfStages, kSReady = kXEmpty + kSfStages,
-  kSFree = kSReady + 2, kDone = kSFree + 2, kSfNumBars = kDone + 1
+  kXFull = 0, kXEmpty = kXFull + kSfXS, kBFull = kXEmpty + kSfXS, kBEmpty = kBFull + kSfBS,
+  kOpFull = kBEmpty + kSfBS, kOpEmpty = kOpFull + kSfOS, kSReady = kOpEmpty + kSfOS, kSFree = kSReady + 2,
+  kDone = kSFree + 2, kSfNumBars = kDone + 1
 };
+static_assert(kSfNumBars <= 32, "barrier area");
 
 // d = a * b + c on bf16 pairs, one rounding
 __device__ __forceinline__ uint32_t sf_fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
@@ -154,7 +173,7 @@ __device__ __forceinline__ uint32_t sf_pack(float lo, float hi) {
 
 __global__ void __launch_bounds__(kSfThreads, 1)
     ssd_state_fused_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_b,
-                              SfParams p, LookbackCtl ctl_call) {
+                              const __grid_constant__ CUtensorMap map_hin, SfParams p, LookbackCtl ctl_call) {
   extern __shared__ unsigned char sf_raw[];
   griddep_launch_dependents();
   const uint32_t raw = smem_addr(sf_raw);
@@ -163,8 +182,8 @@ __global__ void __launch_bounds__(kSfThreads, 1)
   const SfLayout L;
   const int nk = T / kSfKH;  // steps per chunk
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bars);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.bars + 24 * 8);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.bars + 24 * 8 + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.bars + 32 * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.bars + 32 * 8 + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hpg = p.nheads / p.ngroups, ppg = hpg / 2;
@@ -178,7 +197,10 @@ __global__ void __launch_bounds__(kSfThreads, 1)
   auto chain_h = [&](int64_t z) { return chain_g(z) * hpg + 2 * (int)(z % ppg); };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kSfNumBars; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < kSfNumBars; ++i)
+      mbar_init(&bars[i], (i >= kXEmpty && i < kXEmpty + kSfXS) || (i >= kOpFull && i < kOpFull + kSfOS)
+                              ? (uint32_t)kSfScalers
+                              : 1u);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -201,7 +223,7 @@ __global__ void __launch_bounds__(kSfThreads, 1)
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------------------
     if (lane == 0) {
-      int64_t i = 0;
+      int64_t i = 0, nx = 0;  // steps and X copies issued
       bool ok = true;
       for (int s = 0; s < rg.nseg && ok; ++s) {
         const SfSeg sg = sf_seg(rg, s, nc);
@@ -209,34 +231,64 @@ __global__ void __launch_bounds__(kSfThreads, 1)
         const int g = chain_g(sg.chain), h = chain_h(sg.chain);
         for (int64_t c = sg.c0; c < sg.c1 && ok && !*abort_flag; ++c) {
           for (int kh = 0; kh < nk; ++kh, ++i) {
-            const int st = (int)(i % kSfStages);
-            if (i >= kSfStages &&
-                !mbar_wait(&bars[kXEmpty + st], (uint32_t)((i / kSfStages) - 1) & 1u, ctl.spin_limit_ns)) {
+            const int xs = (int)(i % kSfXS);
+            const int tok = (int)(c * T + kh * kSfKH);
+            // X and the step's G / dt: the slot is free once the scalers hold step i - kSfXS
+            if (i >= kSfXS && !mbar_wait(&bars[kXEmpty + xs], (uint32_t)((i / kSfXS) - 1) & 1u, ctl.spin_limit_ns)) {
               ok = false;
               break;
             }
-            const int tok = (int)(c * T + kh * kSfKH);
-            unsigned char* stage = base + st * L.stage_bytes;
-            unsigned char* gd = base + L.gd0 + st * 2 * kSfGdHead;
-            mbar_arrive_expect_tx(&bars[kXFull + st], L.half_bytes + 2u * kSfKH * kSfRowBytes + 2u * kSfGdHead);
+            unsigned char* xst = base + xs * L.x_bytes;
+            unsigned char* gd = base + L.gd0 + xs * 2 * kSfGdHead;
+            mbar_arrive_expect_tx(&bars[kXFull + xs], L.x_bytes + 2u * kSfGdHead);
             for (int hh = 0; hh < 2; ++hh)
-              tc::tma_load_3d(stage + hh * kSfKH * kSfRowBytes, &map_x, (h + hh) * 64, tok, (int)bi, &bars[kXFull + st]);
-            for (int sb = 0; sb < 2; ++sb)
-              tc::tma_load_3d(stage + L.b_off + sb * kSfKH * kSfRowBytes, &map_b, g * 128 + sb * 64, tok, (int)bi,
-                              &bars[kXFull + st]);
+              tc::tma_load_3d(xst + hh * kSfKH * kSfRowBytes, &map_x, (h + hh) * 64, tok, (int)bi, &bars[kXFull + xs]);
             for (int hh = 0; hh < 2; ++hh) {
               const int64_t row = (bi * p.nheads + h + hh) * p.lpad + c * T;
-              bulk_g2s(gd + hh * kSfGdHead, p.G + row + kh * kSfKH, 4u * kSfKH, &bars[kXFull + st]);
-              bulk_g2s(gd + hh * kSfGdHead + 4u * kSfKH, p.dtT + row + kh * kSfKH, 4u * kSfKH, &bars[kXFull + st]);
-              bulk_g2s(gd + hh * kSfGdHead + 8u * kSfKH, p.G + row + T - 4, 16u, &bars[kXFull + st]);
+              bulk_g2s(gd + hh * kSfGdHead, p.G + row + kh * kSfKH, 4u * kSfKH, &bars[kXFull + xs]);
+              bulk_g2s(gd + hh * kSfGdHead + 4u * kSfKH, p.dtT + row + kh * kSfKH, 4u * kSfKH, &bars[kXFull + xs]);
+              bulk_g2s(gd + hh * kSfGdHead + 8u * kSfKH, p.G + row + T - 4, 16u, &bars[kXFull + xs]);
             }
+            ++nx;
           }
         }
       }
       if (!ok) fail();
-      // leave no copy in flight (bounded)
-      for (int64_t j = (i > kSfStages ? i - kSfStages : 0); j < i; ++j)
-        mbar_wait(&bars[kXFull + (int)(j % kSfStages)], (uint32_t)(j / kSfStages) & 1u, ctl.spin_limit_ns);
+      // leave no copy in flight (bounded): the last copies into every slot of both rings
+      for (int64_t j = (nx > kSfXS ? nx - kSfXS : 0); j < nx; ++j)
+        mbar_wait(&bars[kXFull + (int)(j % kSfXS)], (uint32_t)(j / kSfXS) & 1u, ctl.spin_limit_ns);
+    }
+  } else if (warp == 2) {
+    // ------------------------------ TMA producer of B --------------------------------------
+    // Its own thread, so that a B slot, held until the MMAs of its step complete, never holds
+    // back the X loads, which come from DRAM and need the longer lead.
+    if (lane == 0) {
+      int64_t i = 0, nb = 0;  // steps and B copies issued
+      bool ok = true;
+      for (int s = 0; s < rg.nseg && ok; ++s) {
+        const SfSeg sg = sf_seg(rg, s, nc);
+        const int64_t bi = chain_bi(sg.chain);
+        const int g = chain_g(sg.chain);
+        for (int64_t c = sg.c0; c < sg.c1 && ok && !*abort_flag; ++c) {
+          for (int kh = 0; kh < nk; ++kh, ++i) {
+            const int bs = (int)(i % kSfBS);
+            // the slot is free once the MMAs of step i - kSfBS have completed
+            if (i >= kSfBS && !mbar_wait(&bars[kBEmpty + bs], (uint32_t)((i / kSfBS) - 1) & 1u, ctl.spin_limit_ns)) {
+              ok = false;
+              break;
+            }
+            unsigned char* bst = base + L.b0 + bs * L.x_bytes;
+            mbar_arrive_expect_tx(&bars[kBFull + bs], L.x_bytes);
+            for (int sb = 0; sb < 2; ++sb)
+              tc::tma_load_3d(bst + sb * kSfKH * kSfRowBytes, &map_b, g * 128 + sb * 64, (int)(c * T + kh * kSfKH),
+                              (int)bi, &bars[kBFull + bs]);
+            ++nb;
+          }
+        }
+      }
+      if (!ok) fail();
+      for (int64_t j = (nb > kSfBS ? nb - kSfBS : 0); j < nb; ++j)
+        mbar_wait(&bars[kBFull + (int)(j % kSfBS)], (uint32_t)(j / kSfBS) & 1u, ctl.spin_limit_ns);
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer ---------------------------------------------
@@ -256,15 +308,16 @@ __global__ void __launch_bounds__(kSfThreads, 1)
           break;
         }
         for (int kh = 0; kh < nk; ++kh, ++i) {
-          const int st = (int)(i % kSfStages);
-          if (!mbar_wait(&bars[kXScaled + st], (uint32_t)(i / kSfStages) & 1u, ctl.spin_limit_ns)) {
+          const int os = (int)(i % kSfOS), bs = (int)(i % kSfBS);
+          if (!mbar_wait(&bars[kOpFull + os], (uint32_t)(i / kSfOS) & 1u, ctl.spin_limit_ns) ||
+              !mbar_wait(&bars[kBFull + bs], (uint32_t)(i / kSfBS) & 1u, ctl.spin_limit_ns)) {
             ok = false;
             break;
           }
           tc::fence_after_sync();
-          const uint32_t hi0 = smem_addr(base + st * L.stage_bytes);
-          const uint32_t lo0 = hi0 + L.half_bytes;
-          const uint32_t b0 = hi0 + L.b_off;
+          const uint32_t hi0 = smem_addr(base + L.op0 + os * L.op_bytes);
+          const uint32_t lo0 = hi0 + L.x_bytes;
+          const uint32_t b0 = smem_addr(base + L.b0 + bs * L.x_bytes);
 #pragma unroll
           for (int ks = 0; ks < kSfKH / 16; ++ks) {
             const uint32_t koff = ks * 16 * kSfRowBytes;  // 16 tokens = two 8-row groups
@@ -272,7 +325,8 @@ __global__ void __launch_bounds__(kSfThreads, 1)
             tc::mma_bf16(acc, tc::sdesc_sw128(hi0 + koff, ab_lbo, sbo), bdesc, idesc, kh > 0 || ks > 0);
             tc::mma_bf16(acc, tc::sdesc_sw128(lo0 + koff, ab_lbo, sbo), bdesc, idesc, true);
           }
-          tc::mma_commit(&bars[kXEmpty + st]);  // the stage may be refilled
+          tc::mma_commit(&bars[kOpEmpty + os]);  // the operand slot may take a later step
+          tc::mma_commit(&bars[kBEmpty + bs]);   // the B slot may be refilled
         }
         if (ok) {
           tc::mma_commit(&bars[kSReady + sb]);  // S[sb] holds chunk q
@@ -285,61 +339,78 @@ __global__ void __launch_bounds__(kSfThreads, 1)
       // A commit's arrive lands when its MMAs complete, in no fixed order with the others: wait
       // for the last phase of every committed barrier, so that no arrive is still due to this
       // CTA's shared memory when it exits.
-      for (int x = 0; x < kSfStages; ++x)
-        if (i > x) mbar_wait(&bars[kXEmpty + x], (uint32_t)(((i - 1 - x) / kSfStages) & 1), ctl.spin_limit_ns);
+      for (int x = 0; x < kSfOS; ++x)
+        if (i > x) mbar_wait(&bars[kOpEmpty + x], (uint32_t)(((i - 1 - x) / kSfOS) & 1), ctl.spin_limit_ns);
+      for (int x = 0; x < kSfBS; ++x)
+        if (i > x) mbar_wait(&bars[kBEmpty + x], (uint32_t)(((i - 1 - x) / kSfBS) & 1), ctl.spin_limit_ns);
       for (int x = 0; x < 2; ++x)
         if (nready > x) mbar_wait(&bars[kSReady + x], (uint32_t)(((nready - 1 - x) / 2) & 1), ctl.spin_limit_ns);
     }
-  } else if (warp < 10) {
+  } else if (warp < (kSfScaler0 + kSfScalers) / 32) {
     // ---------------- scale X by w, split into bf16 hi + lo parts --------------------------
-    const int grp = (warp - 2) >> 2;          // this group takes the steps i with i % 2 == grp
-    const int t = threadIdx.x - 64 - 128 * grp;  // token row of the step: head t / 64, token t % 64
-    const uint32_t gbar = kSfScaleBar + 2 * grp;
+    // One token row of one head per thread: the row's eight 16-byte pieces go to registers,
+    // the X slot is handed back, then hi and lo are written to the operand slot.
+    const int t = threadIdx.x - kSfScaler0;  // token row of the step: head t / 64, token t % 64
     const int hh = t / kSfKH, tok = t % kSfKH;
     const int64_t nsteps = (u1 - u0) * nk;
-    for (int64_t i = grp; i < nsteps; i += 2) {
-      const int st = (int)(i % kSfStages);
-      const bool bad = !mbar_wait(&bars[kXFull + st], (uint32_t)(i / kSfStages) & 1u, ctl.spin_limit_ns);
-      if (named_bar_any(gbar, 128, bad)) {  // leave together, or not at all
+    for (int64_t i = 0; i < nsteps; ++i) {
+      const int xs = (int)(i % kSfXS), os = (int)(i % kSfOS);
+      const bool bad = !mbar_wait(&bars[kXFull + xs], (uint32_t)(i / kSfXS) & 1u, ctl.spin_limit_ns) ||
+                       (i >= kSfOS && !mbar_wait(&bars[kOpEmpty + os], (uint32_t)((i / kSfOS) - 1) & 1u,
+                                                 ctl.spin_limit_ns));
+      if (named_bar_any(kSfScaleBar, kSfScalers, bad)) {  // leave together, or not at all
         if (t == 0) fail();
         break;
       }
-      const float* gd = reinterpret_cast<const float*>(base + L.gd0 + (st * 2 + hh) * kSfGdHead);
+      const float* gd = reinterpret_cast<const float*>(base + L.gd0 + (xs * 2 + hh) * kSfGdHead);
       const float wv = gd[kSfKH + tok] * tc::ex2_approx(gd[2 * kSfKH + 3] - gd[tok]);
+      const unsigned char* xrow = base + xs * L.x_bytes + t * kSfRowBytes;
+      // the row's pieces in an order rotated by the row, so that a warp's accesses spread over
+      // the banks; each piece keeps its swizzled position in the operand slot
+      uint4 xv[8];
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) xv[cc] = *reinterpret_cast<const uint4*>(xrow + ((cc ^ (t & 7)) << 4));
+      // these reads are performed before the TMA (async proxy) refills the slot
+      fence_proxy_async_smem();
+      mbar_arrive(&bars[kXEmpty + xs]);
       const __nv_bfloat16 w_hi = __float2bfloat16_rn(wv);
       const float w_lo = wv - __bfloat162float(w_hi);
       const uint32_t whi2 = sf_bf16_pair(__bfloat162float(w_hi));
       const uint32_t nwhi2 = whi2 ^ 0x80008000u;
       const uint32_t nwlo2 = sf_bf16_pair(-w_lo);
-      unsigned char* hrow = base + st * L.stage_bytes + t * kSfRowBytes;
-      unsigned char* lrow = hrow + L.half_bytes;
+      unsigned char* hrow = base + L.op0 + os * L.op_bytes + t * kSfRowBytes;
+      unsigned char* lrow = hrow + L.x_bytes;
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) {
-        const int off = (cc ^ (t & 7)) << 4;  // the row's chunks, spread over the banks
-        uint4 v = *reinterpret_cast<const uint4*>(hrow + off);
-        uint32_t* e = reinterpret_cast<uint32_t*>(&v);
-        uint4 r;
-        uint32_t* f = reinterpret_cast<uint32_t*>(&r);
+        const int pc = cc ^ (t & 7);  // the piece's position in the row (X's swizzled layout)
+        uint32_t* e = reinterpret_cast<uint32_t*>(&xv[cc]);
+        uint4 hv, lv;
+        uint32_t* fh = reinterpret_cast<uint32_t*>(&hv);
+        uint32_t* fl = reinterpret_cast<uint32_t*>(&lv);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint32_t x2 = e[k];
           const uint32_t h2 = sf_fma_bf16x2(x2, whi2, 0x80008000u);  // x w_hi, rounded
           const uint32_t d2 = sf_fma_bf16x2(x2, nwhi2, h2);           // hi - x w_hi, exact
-          f[k] = sf_fma_bf16x2(x2, nwlo2, d2) ^ 0x80008000u;          // x w - hi, rounded
-          e[k] = h2;
+          fl[k] = sf_fma_bf16x2(x2, nwlo2, d2) ^ 0x80008000u;          // x w - hi, rounded
+          fh[k] = h2;
         }
-        *reinterpret_cast<uint4*>(hrow + off) = v;
-        *reinterpret_cast<uint4*>(lrow + off) = r;
+        *reinterpret_cast<uint4*>(hrow + (pc << 4)) = hv;
+        *reinterpret_cast<uint4*>(lrow + (pc << 4)) = lv;
       }
-      fence_proxy_async_smem();
-      named_bar_sync(gbar, 128);
-      if (t == 0) mbar_arrive(&bars[kXScaled + st]);
+      fence_proxy_async_smem();  // the MMAs read the operand through the async proxy
+      mbar_arrive(&bars[kOpFull + os]);
     }
   } else {
     // ------------------------------ state warps --------------------------------------------
-    const int quad = warp & 3;       // TMEM lanes 32*quad .. +31
-    const int m = quad * 32 + lane;  // state row: head h + m / 64, p = m % 64
+    // Two threads per state row (TMEM lane), 64 of its 128 columns each.
+    const int sw = warp - (kSfScaler0 + kSfScalers) / 32;  // 0 .. 7
+    const int quad = warp & 3;                  // TMEM lanes 32*quad .. +31
+    const int half = sw >> 2;                   // columns 64*half .. +63
+    const int m = quad * 32 + lane;             // state row: head h + m / 64, p = m % 64
     const int hh = m >> 6, pp = m & 63;
+    const int col0 = 64 * half;
+    const bool leader = half == 0 && m == 0;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     int64_t q = 0;  // chunks run so far (the accumulators alternate)
     bool ok = true;
@@ -348,15 +419,15 @@ __global__ void __launch_bounds__(kSfThreads, 1)
       const int64_t bi = chain_bi(sg.chain);
       const int h = chain_h(sg.chain);
       const int64_t bh = bi * p.nheads + h + hh;
-      const float* h0r = p.h0 ? p.h0 + (bh * 64 + pp) * 128 : nullptr;
-      float* cr = p.carry + (sg.chain * 128 + m) * 128;  // this row of the chain's published state
+      const float* h0r = p.h0 ? p.h0 + (bh * 64 + pp) * 128 + col0 : nullptr;
+      float* cr = p.carry + (sg.chain * 128 + m) * 128 + col0;  // this row of the chain's published state
       const float* Glast = p.G + bh * p.lpad + (T - 1);  // G_last of chunk c at Glast[c * T]
       if (sg.from_carry) {
         // the previous CTA ran this chain's head first and published where it stopped
         bool bad = false;
-        if (m == 0) bad = wait_flag(&p.flags[sg.chain], p.hdr, ctl) != kFlagPrefix;
-        if (named_bar_any(kSfStateBar, 128, bad)) {
-          if (m == 0) fail();
+        if (leader) bad = wait_flag(&p.flags[sg.chain], p.hdr, ctl) != kFlagPrefix;
+        if (named_bar_any(kSfStateBar, kSfStateThreads, bad)) {
+          if (leader) fail();
           ok = false;
           break;
         }
@@ -364,87 +435,91 @@ __global__ void __launch_bounds__(kSfThreads, 1)
       for (int64_t c = sg.c0; c < sg.c1; ++c, ++q) {
         const int sb = (int)(q & 1);
         const bool bad = !mbar_wait(&bars[kSReady + sb], (uint32_t)((q >> 1) & 1), ctl.spin_limit_ns);
-        if (named_bar_any(kSfStateBar, 128, bad)) {  // S[sb] holds chunk c
-          if (m == 0) fail();
+        if (leader) bulk_wait_read<0>();  // the previous chunk's h_in store has read the staging buffer
+        if (named_bar_any(kSfStateBar, kSfStateThreads, bad)) {  // S[sb] holds chunk c
+          if (leader) fail();
           ok = false;
           break;
         }
         tc::fence_after_sync();
         const float dec = exp2f(Glast[c * T]);  // decay over chunk c
-        __nv_bfloat16* hr = p.hin + (((bi * nc + c) * p.nheads + h + hh) * 64 + pp) * 128;
+        unsigned char* hsrow = base + L.hs0 + half * (128 * kSfRowBytes) + m * kSfRowBytes;
         const bool chain_end = c == nc - 1, publish = sg.to_carry && c == sg.c1 - 1;
         const bool first = c == sg.c0;
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {  // 32 columns (s) at a time
-          float v[32];
-          uint32_t sv[32];
-          tc::tmem_ld32(tmem + lane_base + 128u + 128u * sb + 32 * qq, sv);
+        for (int qq = 0; qq < 4; ++qq) {  // 16 columns (s) at a time
+          const uint32_t col = (uint32_t)(col0 + 16 * qq);
+          float v[16];
+          uint32_t sv[16];
+          tc::tmem_ld16(tmem + lane_base + 128u + 128u * sb + col, sv);
           if (first && !sg.from_carry) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float4 f = h0r ? reinterpret_cast<const float4*>(h0r + 32 * qq)[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j = 0; j < 4; ++j) {
+              const float4 f = h0r ? reinterpret_cast<const float4*>(h0r + 16 * qq)[j] : make_float4(0.f, 0.f, 0.f, 0.f);
               v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
             }
           } else if (first) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float4 f = ld_relaxed_f4(reinterpret_cast<const float4*>(cr + 32 * qq) + j);
+            for (int j = 0; j < 4; ++j) {
+              const float4 f = ld_relaxed_f4(reinterpret_cast<const float4*>(cr + 16 * qq) + j);
               v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
             }
           } else {
-            uint32_t r[32];
-            tc::tmem_ld32(tmem + lane_base + 32 * qq, r);
+            uint32_t r[16];
+            tc::tmem_ld16(tmem + lane_base + col, r);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+            for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
           }
           tc::tmem_ld_wait();
-          // h_in[c] (bf16): the state entering chunk c
-          uint4* o = reinterpret_cast<uint4*>(hr + 32 * qq);
+          // h_in[c] (bf16): the state entering chunk c, to the staging buffer (16-byte piece
+          // 2 qq + j of the row's s block, swizzled)
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            o[j] = make_uint4(sf_pack(v[8 * j], v[8 * j + 1]), sf_pack(v[8 * j + 2], v[8 * j + 3]),
-                              sf_pack(v[8 * j + 4], v[8 * j + 5]), sf_pack(v[8 * j + 6], v[8 * j + 7]));
+          for (int j = 0; j < 2; ++j)
+            *reinterpret_cast<uint4*>(hsrow + (((2 * qq + j) ^ (m & 7)) << 4)) =
+                make_uint4(sf_pack(v[8 * j], v[8 * j + 1]), sf_pack(v[8 * j + 2], v[8 * j + 3]),
+                           sf_pack(v[8 * j + 4], v[8 * j + 5]), sf_pack(v[8 * j + 6], v[8 * j + 7]));
           // the state after chunk c
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = fmaf(dec, v[j], __uint_as_float(sv[j]));
+          for (int j = 0; j < 16; ++j) v[j] = fmaf(dec, v[j], __uint_as_float(sv[j]));
           if (chain_end) {
             if (p.h_final) {
-              float4* f = reinterpret_cast<float4*>(p.h_final + (bh * 64 + pp) * 128 + 32 * qq);
+              float4* f = reinterpret_cast<float4*>(p.h_final + (bh * 64 + pp) * 128 + col0 + 16 * qq);
 #pragma unroll
-              for (int j = 0; j < 8; ++j) f[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+              for (int j = 0; j < 4; ++j) f[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
             }
           } else if (publish) {  // h_in[c + 1] for the CTA that runs the rest of this chain
-            float4* f = reinterpret_cast<float4*>(cr + 32 * qq);
+            float4* f = reinterpret_cast<float4*>(cr + 16 * qq);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) f[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            for (int j = 0; j < 4; ++j) f[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
           } else {
-            uint32_t s0[16], s1[16];
+            uint32_t s0[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              s0[j] = __float_as_uint(v[j]);
-              s1[j] = __float_as_uint(v[16 + j]);
-            }
-            tc::tmem_st16(tmem + lane_base + 32 * qq, s0);
-            tc::tmem_st16(tmem + lane_base + 32 * qq + 16, s1);
+            for (int j = 0; j < 16; ++j) s0[j] = __float_as_uint(v[j]);
+            tc::tmem_st16(tmem + lane_base + col, s0);
           }
         }
         tc::tmem_st_wait();
-        if (publish) __threadfence();  // this row of the published state, before the flag
+        if (publish) __threadfence();  // this thread's part of the published state, before the flag
+        fence_proxy_async_smem();      // the staged h_in, before the TMA store reads it
         tc::fence_before_sync();
-        named_bar_sync(kSfStateBar, 128);
-        if (m == 0) {
+        named_bar_sync(kSfStateBar, kSfStateThreads);
+        if (leader) {
+          const int row0 = (int)(((bi * nc + c) * p.nheads + h) * 64);  // the pair's 128 rows of h_in[c]
+          for (int s2 = 0; s2 < 2; ++s2) tma_store_2d(&map_hin, base + L.hs0 + s2 * (128 * kSfRowBytes), 64 * s2, row0);
+          bulk_commit();
           mbar_arrive(&bars[kSFree + sb]);  // S[sb] may take the chunk run two later
           if (publish) st_release_u64(&p.flags[sg.chain], make_flag(ctl.epoch, kFlagPrefix));
         }
       }
     }
+    if (leader) bulk_wait<0>();  // every h_in store has completed
     if (nc == 0 && p.h_final) {  // no chunks: the final state is the initial one (one chain per CTA)
       const int64_t bh = chain_bi(blockIdx.x) * p.nheads + chain_h(blockIdx.x) + hh;
-      const float* h0r = p.h0 ? p.h0 + (bh * 64 + pp) * 128 : nullptr;
-      float4* f = reinterpret_cast<float4*>(p.h_final + (bh * 64 + pp) * 128);
+      const float* h0r = p.h0 ? p.h0 + (bh * 64 + pp) * 128 + col0 : nullptr;
+      float4* f = reinterpret_cast<float4*>(p.h_final + (bh * 64 + pp) * 128 + col0);
 #pragma unroll 4
-      for (int j = 0; j < 32; ++j) f[j] = h0r ? reinterpret_cast<const float4*>(h0r)[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < 16; ++j) f[j] = h0r ? reinterpret_cast<const float4*>(h0r)[j] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 
@@ -531,6 +606,12 @@ cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float*
   if ((e = encode_tensor_map_3d(&map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, bd, bs, box, CU_TENSOR_MAP_SWIZZLE_128B)) !=
       cudaSuccess)
     return e;
+  // h_in as [batch x chunks x heads x 64 rows][128 s] bf16; boxes of 64 s x one pair's 128 rows
+  CUtensorMap map_hin = {};
+  const uint64_t hin_rows = (uint64_t)d.batch * d.nchunks * d.nheads * 64;
+  if (hin_rows > 0 && (e = encode_tensor_map_2d(&map_hin, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws.hin, 128, hin_rows, 256,
+                                                64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+    return e;
   SfParams p;
   p.G = ws.G;
   p.dtT = ws.dtT;
@@ -559,7 +640,8 @@ cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float*
   // a CTA can wait for the state its predecessor publishes
   const int64_t grid = sf_grid(chains, d.nchunks, sms);
   if (grid > chains || ws.sp_tiles < chains) return cudaErrorInvalidValue;
-  return launch_pdl(ssd_state_fused_tc_kernel, dim3((unsigned)grid), dim3(kSfThreads), smem, s, map_x, map_b, p, ctl);
+  return launch_pdl(ssd_state_fused_tc_kernel, dim3((unsigned)grid), dim3(kSfThreads), smem, s, map_x, map_b, map_hin,
+                    p, ctl);
 }
 
 }  // namespace ssm
