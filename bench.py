@@ -41,6 +41,11 @@ SSD = synth.SSD_B4_L8192
 SCAN = synth.SCAN_384x65536
 STEP = synth.STEP_B128
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# GB300 HBM3e bandwidth from NVIDIA's public GB300 NVL72 specification: 576 TB/s for the rack's 72
+# Blackwell Ultra GPUs, i.e. 8 TB/s per GPU.  The gates are also reported against this figure;
+# the measured copy bandwidth (MEASURED_PEAKS.json) stays the roofline denominator.
+DATASHEET_HBM_GBS = 8000.0
+DATASHEET_SOURCE = "NVIDIA GB300 NVL72 specification: 576 TB/s HBM3e over 72 GPUs = 8 TB/s per GPU"
 KERNELS = ("linscan_lookback", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
            "ssd_state_fused")  # the headline step's kernels; the decode step is timed on its own
 
@@ -119,7 +124,7 @@ def kernel_traffic(kernel):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling (every 20 ms); summary() keeps the samples taken
+    """nvidia-smi clock / throttle sampling (every 10 ms); summary() keeps the samples taken
     inside [t0, t1] (host wall-clock bounds of the timed region)."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -134,7 +139,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                          "--format=csv,noheader,nounits", "-lms", "10"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -280,28 +285,32 @@ def run_ours(args, world, rank, local):
             ev[i][2].record(stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
+        barrier(world)
+        # Per-kernel breakdown: the same steps again, with the library's events around every
+        # launch.  Those events keep consecutive launches from overlapping (programmatic
+        # dependent launch), so this second timed pass gives the per-kernel times and the
+        # roofline, not the headline.  The clock record covers both passes.
+        torch.cuda.synchronize()
+        with ssm.KernelTimer(max_launches=8 * args.steps + 8) as kt:
+            for i in range(args.steps):
+                flush.fill_(i & 0xff)
+                ssd_call()
+                scan_call()
+            torch.cuda.synchronize()
         t_wall1 = time.time()
         time.sleep(0.05)
-    barrier(world)
-    # Per-kernel breakdown: the same steps again, with the library's events around every launch.
-    # Those events keep consecutive launches from overlapping (programmatic dependent launch), so
-    # this second timed pass gives the per-kernel times and the roofline, not the headline.
-    torch.cuda.synchronize()
-    with ssm.KernelTimer(max_launches=8 * args.steps + 8) as kt:
-        for i in range(args.steps):
-            flush.fill_(i & 0xff)
-            ssd_call()
-            scan_call()
-        torch.cuda.synchronize()
     barrier(world)
     if ssm.check_device_status(kind="ssd") or ssm.check_device_status(kind="linscan"):
         raise RuntimeError("device status error during the timed region")
     decode = run_decode(args, peaks)
     scan_baselines = run_scan_baselines(args, peaks)
 
-    ssd_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
-    scan_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
-    step_ms = sum(e[0].elapsed_time(e[2]) for e in ev) / args.steps
+    # the median of the per-step samples (the scan page reports the median of interleaved
+    # samples); min and max beside it
+    ssd_s = [e[0].elapsed_time(e[1]) for e in ev]
+    scan_s = [e[1].elapsed_time(e[2]) for e in ev]
+    step_s = [e[0].elapsed_time(e[2]) for e in ev]
+    ssd_ms, scan_ms, step_ms = (statistics.median(v) for v in (ssd_s, scan_s, step_s))
     ssd_ms_max = max_over_ranks(world, ssd_ms)
     scan_ms_max = max_over_ranks(world, scan_ms)
     step_ms_max = max_over_ranks(world, step_ms)
@@ -367,11 +376,18 @@ def run_ours(args, world, rank, local):
             "plan": {"id": plan, "fused_state_path": (plan & 3) - 1, "sequential_state_passing": ((plan >> 2) & 3) - 1,
                      "scan_heads_per_cta": plan >> 4, "tuning_median_ms": round(plan_ms, 4), "how": plan_how},
         },
-        "ssd": {"tokens_per_s": round(value, 1), "ms": round(ssd_ms_max, 4), "model_B_bytes": model_b,
-                "roofline_ms": round(ssd_roof_ms, 4), "roofline_frac": round(ssd_roof_ms / ssd_ms_max, 4),
+        "timing": f"median of {args.steps} per-step CUDA-event samples (min / median / max below)",
+        "ssd": {"tokens_per_s": round(value, 1), "ms": round(ssd_ms_max, 4), "ms_min_median_max": spread(ssd_s),
+                "model_B_bytes": model_b, "roofline_ms": round(ssd_roof_ms, 4),
+                "roofline_frac": round(ssd_roof_ms / ssd_ms_max, 4),
+                "roofline_frac_datasheet": round(model_b / (DATASHEET_HBM_GBS * 1e9) * 1e3 / ssd_ms_max, 4),
                 "io_only_bytes": model_b - 2 * ssd_sizes(SSD)["chunk_states_f32"]},
         "linscan": {"value": round(scan_gbs, 1), "unit": "GB/s", "ms": round(scan_ms_max, 4),
-                    "alg_bytes": sbytes, "frac": round(scan_gbs / world / peaks["hbm_gbs"], 4)},
+                    "ms_min_median_max": spread(scan_s), "alg_bytes": sbytes,
+                    "frac": round(scan_gbs / world / peaks["hbm_gbs"], 4),
+                    "frac_datasheet": round(scan_gbs / world / DATASHEET_HBM_GBS, 4)},
+        "step_ms_min_median_max": spread(step_s),
+        "datasheet_hbm": {"GB/s": DATASHEET_HBM_GBS, "source": DATASHEET_SOURCE},
         "kernels": kernels,
         "decode": decode,
         "scan_baselines": scan_baselines,
@@ -381,6 +397,10 @@ def run_ours(args, world, rank, local):
         "wall_s_timed": round(t_wall, 3),
     }
     return out, ssd_np, scan_np
+
+
+def spread(samples):
+    return [round(min(samples), 4), round(statistics.median(samples), 4), round(max(samples), 4)]
 
 
 def run_decode(args, peaks):
@@ -412,9 +432,11 @@ def run_decode(args, peaks):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"workload": f"ssd_step b{STEP.batch} nh{STEP.nheads} H{STEP.headdim} S{STEP.dstate} G{STEP.ngroups} "
                         f"bf16, f32 state in place",
-            "launches": args.steps, "ms_per_launch": round(ms, 5), "ms_mean": round(sum(per) / len(per), 5),
+            "launches": args.steps, "ms_per_launch": round(ms, 5), "ms_min_median_max": spread(per),
+            "ms_mean": round(sum(per) / len(per), 5),
             "tokens_per_s": round(STEP.batch / (ms * 1e-3), 1), "alg_bytes": nbytes, "GB/s": round(gbs, 1),
-            "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": kernel_traffic("ssd_step"),
+            "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "hbm_frac_datasheet": round(gbs / DATASHEET_HBM_GBS, 4),
+            "traffic": kernel_traffic("ssd_step"),
             "timing": "median of per-launch CUDA events"}
 
 
@@ -562,10 +584,19 @@ def oracle_sample(ssd_np, scan_np, budget_s, unit_batch):
         t_ssd += time.perf_counter() - t0
         done += len(units)
     ssd_tokens_equiv = done / SSD.nheads * SSD.seqlen  # tokens whose every head was computed
-    rows = min(SCAN.rows, max(threads, 16))
+    # the same oracle on one host core: a few whole units
+    one_units = order[:2]
     t0 = time.perf_counter()
-    native.linscan(scan_np["a"], scan_np["b"], rows=np.arange(rows))
-    t_scan = time.perf_counter() - t0
+    native.ssd_fwd(ssd_np["x"], ssd_np["dt"], ssd_np["A"], ssd_np["B"], ssd_np["C"], ssd_np["D"], ssd_np["h0"],
+                   units=one_units, threads=1)
+    t_one = time.perf_counter() - t0
+    # the scan oracle on every row of the workload, repeated until at least 0.5 s have passed
+    reps, t_scan = 0, 0.0
+    while t_scan < 0.5:
+        t0 = time.perf_counter()
+        native.linscan(scan_np["a"], scan_np["b"])
+        t_scan += time.perf_counter() - t0
+        reps += 1
     # decode step: the one-token forward from the carried state, on every unit of the workload
     st = synth.step_inputs(STEP)
     t0 = time.perf_counter()
@@ -575,7 +606,9 @@ def oracle_sample(ssd_np, scan_np, budget_s, unit_batch):
     return {
         "step_tokens_per_s": STEP.batch / t_step, "step_s": t_step,
         "ssd_tokens_per_s": ssd_tokens_equiv / t_ssd, "ssd_units": done, "ssd_s": t_ssd,
-        "scan_gbs": scan_bytes(rows, SCAN.length) / t_scan / 1e9, "scan_rows": rows, "scan_s": t_scan,
+        "ssd_1core_tokens_per_s": len(one_units) / SSD.nheads * SSD.seqlen / t_one, "ssd_1core_units": len(one_units),
+        "ssd_1core_s": t_one,
+        "scan_gbs": reps * scan_bytes(SCAN.rows, SCAN.length) / t_scan / 1e9, "scan_reps": reps, "scan_s": t_scan,
         "cores": threads,
     }
 
@@ -619,15 +652,17 @@ def run_reference(args):
             "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
-def run_ssd_configs(args):
-    """Context beside the headline: every bf16 SSD workload (b8 L2048 nh24, b4 L8192 nh80,
-    b1 L131072 nh32 G8) timed alone with its tuned plan (or --plan rules / --plan-id), L2
-    flushed before each forward, one JSON line each.  Median of `steps` forwards; per-kernel
-    times from the library's events."""
+def run_ssd_configs(args, steps=None):
+    """Every bf16 SSD workload (b8 L2048 nh24, b4 L8192 nh80, b1 L131072 nh32 G8) timed alone
+    with its tuned plan (or --plan rules / --plan-id), L2 flushed before each forward.  Median of
+    `steps` forwards (min and max beside it); per-kernel times from the library's events.
+    Returns one entry per workload."""
     import torch
     import selective_state_space_mamba_gb300 as ssm
     peaks, _ = load_peaks()
+    steps = steps or args.steps
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    entries = []
     for shape in (synth.SSD_B8_L2048, synth.SSD_B4_L8192, synth.SSD_B1_L131072):
         if args.ssd_workload and shape.name != args.ssd_workload:
             continue
@@ -651,7 +686,7 @@ def run_ssd_configs(args):
             flush.fill_(1)
             call()
         ms = []
-        for i in range(args.steps):
+        for i in range(steps):
             flush.fill_(i & 0xff)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
@@ -659,8 +694,8 @@ def run_ssd_configs(args):
             e1.record()
             torch.cuda.synchronize()
             ms.append(e0.elapsed_time(e1))
-        with ssm.KernelTimer(max_launches=8 * args.steps + 8) as kt:
-            for i in range(args.steps):
+        with ssm.KernelTimer(max_launches=8 * steps + 8) as kt:
+            for i in range(steps):
                 flush.fill_(i & 0xff)
                 call()
             torch.cuda.synchronize()
@@ -668,13 +703,15 @@ def run_ssd_configs(args):
             raise RuntimeError(f"device status error in {shape.name}")
         med = float(np.median(ms))
         roof_ms = ssd_model_b_bytes(shape) / (peaks["hbm_gbs"] * 1e9) * 1e3
-        print(json.dumps({"workload": shape.name, "plan": plan, "ms": round(med, 4),
-                          "tokens_per_s": round(shape.batch * shape.seqlen / (med * 1e-3), 1),
-                          "model_B_roofline_ms": round(roof_ms, 4), "roofline_frac": round(roof_ms / med, 4),
-                          "per_kernel_us": {k: round(kt.ms[k] / kt.launches[k] * 1e3, 1)
-                                            for k in kt.ms if kt.launches.get(k)}}), flush=True)
+        entries.append({"workload": shape.name, "plan": plan, "ms": round(med, 4), "ms_min_median_max": spread(ms),
+                        "tokens_per_s": round(shape.batch * shape.seqlen / (med * 1e-3), 1),
+                        "model_B_roofline_ms": round(roof_ms, 4), "roofline_frac": round(roof_ms / med, 4),
+                        "roofline_frac_datasheet": round(roof_ms * peaks["hbm_gbs"] / DATASHEET_HBM_GBS / med, 4),
+                        "per_kernel_us": {k: round(kt.ms[k] / kt.launches[k] * 1e3, 1)
+                                          for k in kt.ms if kt.launches.get(k)}})
         del d, y, hf
         torch.cuda.empty_cache()
+    return entries
 
 
 def main():
@@ -686,6 +723,7 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=15.0, help="time budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-ssd-configs", action="store_true", help="leave out the per-workload SSD block")
     ap.add_argument("--ssd-configs", action="store_true",
                     help="instead of the bench line: time every bf16 SSD workload alone, one JSON line each")
     ap.add_argument("--ssd-workload", default=None, help="with --ssd-configs: only the workload of this name")
@@ -704,10 +742,14 @@ def main():
         return
 
     if args.ssd_configs:
-        run_ssd_configs(args)
+        for e in run_ssd_configs(args):
+            print(json.dumps(e), flush=True)
         return
     world, rank, local = dist_setup(args)
     out, ssd_np, scan_np = run_ours(args, world, rank, local)
+    if not args.no_ssd_configs:
+        # every bf16 SSD workload alone (tuned plan each), for the per-workload rooflines
+        out["ssd_configs"] = run_ssd_configs(args, steps=max(15, min(args.steps, 30)))
     if not args.no_e2e:
         e2e = run_e2e(args)
         e2e["value"] = round(max_over_ranks(world, -e2e["value"]) * -1 * world, 1) if world > 1 else e2e["value"]
@@ -718,8 +760,11 @@ def main():
             "value": round(cb["ssd_tokens_per_s"], 1), "unit": "tokens/s", "cores": cb["cores"], "kind": "oracle",
             "sample": (f"{cb['ssd_units']} of {SSD.batch * SSD.nheads} whole (batch, head) units of the SSD workload "
                        f"in {cb['ssd_s']:.1f} s; tokens/s counts a token once all its heads are done"),
-            "linscan": {"value": round(cb["scan_gbs"], 2), "unit": "GB/s",
-                        "sample": f"{cb['scan_rows']} of {SCAN.rows} rows in {cb['scan_s']:.2f} s"},
+            "one_core": {"value": round(cb["ssd_1core_tokens_per_s"], 1), "unit": "tokens/s", "cores": 1,
+                         "sample": f"{cb['ssd_1core_units']} whole (batch, head) units on one thread in "
+                                   f"{cb['ssd_1core_s']:.2f} s"},
+            "linscan": {"value": round(cb["scan_gbs"], 2), "unit": "GB/s", "cores": cb["cores"],
+                        "sample": f"all {SCAN.rows} rows, {cb['scan_reps']} times, in {cb['scan_s']:.2f} s"},
             "decode": {"value": round(cb["step_tokens_per_s"], 1), "unit": "tokens/s",
                        "sample": f"one whole decode step ({STEP.batch} tokens) in {cb['step_s']:.2f} s"},
         }

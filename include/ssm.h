@@ -76,7 +76,8 @@ typedef enum {
     SSM_ERR_ALIGNMENT = 3,   /* a tensor or workspace base is not aligned as required */
     SSM_ERR_WORKSPACE = 4,   /* workspace NULL or smaller than *_workspace_bytes() */
     SSM_ERR_CUDA = 5,        /* a CUDA runtime call failed (launch, attribute, sync) */
-    SSM_ERR_TIMEOUT = 6      /* a bounded look-back wait gave up (device status word) */
+    SSM_ERR_TIMEOUT = 6,     /* a bounded look-back wait gave up (device status word) */
+    SSM_ERR_BOUNDS = 7       /* a device index check of a debug build (SSM_DEBUG) failed (device status word) */
 } ssm_status;
 
 typedef enum {
@@ -227,13 +228,17 @@ SSM_API ssm_status ssm_linscan_fwd(const float *a, const float *b, float *h, int
  *     ssm_linscan_fwd with a workspace for them.
  *   - It allocates nothing: no cudaMalloc, cudaFree or allocating library routine.  It
  *     enqueues a 16-byte cudaMemsetAsync that clears the scratch header, then the kernel.
- *   - The first call on each device looks up the device address of the scratch array (with
- *     that device current); make that first call before any stream capture.
+ *   - Every call looks up the device address of the scratch array on the current device (the
+ *     first call on a device may load the library's device code there); make the first call on
+ *     each device before any stream capture.
  *   - All calls share the one scratch array, which keeps the previous call's contents.  Calls
  *     that may overlap on the GPU (different streams without ordering) race and must not be
  *     issued.
- *   - Device-side look-back timeouts are not reported by this entry point (there is no
- *     workspace to pass to ssm_check_device_status); the output of such a call is invalid.
+ *   - Device-side look-back timeouts (a wait beyond 1 s, which needs a GPU that stopped making
+ *     progress) are not reported by this entry point: there is no workspace to pass to
+ *     ssm_check_device_status, and the next call clears the scratch's status word.  The
+ *     output of such a call is invalid: tiles whose wait ran out hold NaN, and tiles no thread
+ *     reached keep whatever h held before the call.
  * Errors: SSM_ERR_INVALID_ARG, SSM_ERR_ALIGNMENT, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA.
  */
 SSM_API ssm_status ssm_linscan_fwd_noalloc(const float *a, const float *b, float *h, int64_t rows, int64_t len,
@@ -289,6 +294,22 @@ SSM_API ssm_status ssm_check_device_status(void *workspace, ssm_stream_t stream)
  * SSM_ERR_TIMEOUT in the status word and return; no kernel waits without a limit.
  */
 SSM_API void ssm_debug_set_lookback_fault(int64_t stall_tile, uint64_t spin_limit_ns);
+
+/*
+ * Debug builds.  The library compiled with -DSSM_DEBUG (libssm_gb300_debug.so, built beside the
+ * release library) checks the indexes of its kernels' raw global-memory accesses and of the
+ * shared-memory slots they compute: a failed check records SSM_ERR_BOUNDS in the call's
+ * status word, which ssm_check_device_status reports, and the access is skipped; nothing traps.
+ * This stands in for a memory sanitizer.  ssm_debug_build returns 1 in such a build, else 0.
+ *
+ * ssm_debug_set_bounds_fault is a test hook of debug builds: from the next ssm_ssd_fwd call on,
+ * the chunk-cumsum kernel checks its G and dt^T stores against a bound `shrink` elements short
+ * of the real one, so that the stores of the last `shrink` elements fail the check, are skipped
+ * and SSM_ERR_BOUNDS is reported (the forward's output is then not valid).  0 turns it off.
+ * Release builds: returns SSM_ERR_UNSUPPORTED and changes nothing.
+ */
+SSM_API int ssm_debug_build(void);
+SSM_API ssm_status ssm_debug_set_bounds_fault(int64_t shrink);
 
 /*
  * Test hook for the fused state pass's work split (host only; no GPU call).  For `chains`

@@ -31,7 +31,8 @@
  * computed.  y_out is [n_units, L, H] and hfinal_out is [n_units, H, S]
  * (either may be NULL).  h0 is float64 [batch, nheads, H, S] so a final
  * state can be fed back unrounded; it may be NULL (zeros).  Returns 0, or -1 on a bad
- * argument, -2 on allocation failure.  threads <= 0 keeps the OpenMP default.
+ * argument, -2 on allocation failure.  threads <= 0 takes the OpenMP default; the count
+ * applies to this call only.
  */
 int ssm_oracle_ssd(const float *x, const float *dt, const float *A, const float *B,
                    const float *C, const float *D, const double *h0,
@@ -48,12 +49,11 @@ int ssm_oracle_ssd(const float *x, const float *dt, const float *A, const float 
     const int64_t heads_per_group = nheads / ngroups;
     int failed = 0;
 #ifdef _OPENMP
-    if (threads > 0)
-        omp_set_num_threads(threads);
+    const int nt = threads > 0 ? threads : omp_get_max_threads();  /* this call only */
 #else
     (void)threads;
 #endif
-#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed)
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : failed) num_threads(nt)
     for (int64_t u = 0; u < n_units; ++u) {
         const int64_t bi = units[u] / nheads;
         const int64_t hi = units[u] % nheads;
@@ -110,12 +110,11 @@ int ssm_oracle_linscan(const float *a, const float *b, double *h_out,
         if (rows_sel[r] < 0 || rows_sel[r] >= rows)
             return -1;
 #ifdef _OPENMP
-    if (threads > 0)
-        omp_set_num_threads(threads);
+    const int nt = threads > 0 ? threads : omp_get_max_threads();  /* this call only */
 #else
     (void)threads;
 #endif
-#pragma omp parallel for schedule(dynamic, 1)
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
     for (int64_t r = 0; r < n_sel; ++r) {
         const float *ar = a + rows_sel[r] * L;
         const float *br = b + rows_sel[r] * L;

@@ -12,7 +12,7 @@ import threading
 from . import _build
 
 SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_ALIGNMENT, SSM_ERR_WORKSPACE, SSM_ERR_CUDA, \
-    SSM_ERR_TIMEOUT = range(7)
+    SSM_ERR_TIMEOUT, SSM_ERR_BOUNDS = range(8)
 SSM_F32, SSM_BF16 = 0, 1
 SSM_SCAN_BLELLOCH, SSM_SCAN_THREE_PASS, SSM_SCAN_LOOKBACK_SERIAL, SSM_SCAN_LOOKBACK_WARP, SSM_SCAN_HILLIS_STEELE = \
     1, 2, 3, 4, 5
@@ -22,7 +22,8 @@ EXPORTS = ("ssm_status_string", "ssm_version", "ssm_ssd_fwd_workspace_bytes", "s
            "ssm_linscan_workspace_bytes", "ssm_linscan_fwd", "ssm_check_device_status",
            "ssm_debug_set_lookback_fault", "ssm_profile_begin", "ssm_profile_end", "ssm_linscan_fwd_noalloc",
            "ssm_ssd_step", "ssm_linscan_baseline_workspace_bytes", "ssm_linscan_baseline", "ssm_ssd_fwd_tune",
-           "ssm_ssd_fwd_set_plan", "ssm_ssd_fwd_get_plan", "ssm_ssd_fwd_clear_plans", "ssm_debug_fused_schedule")
+           "ssm_ssd_fwd_set_plan", "ssm_ssd_fwd_get_plan", "ssm_ssd_fwd_clear_plans", "ssm_debug_fused_schedule",
+           "ssm_debug_build", "ssm_debug_set_bounds_fault")
 PROFILE_KERNELS = ("linscan_lookback", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
                    "ssd_state_fused", "ssd_step", "linscan_baseline")
 
@@ -70,6 +71,10 @@ def _declare(lib):
     lib.ssm_check_device_status.restype = i32
     lib.ssm_debug_set_lookback_fault.argtypes = [i64, u64]
     lib.ssm_debug_set_lookback_fault.restype = None
+    lib.ssm_debug_build.argtypes = []
+    lib.ssm_debug_build.restype = i32
+    lib.ssm_debug_set_bounds_fault.argtypes = [i64]
+    lib.ssm_debug_set_bounds_fault.restype = i32
     lib.ssm_linscan_fwd_noalloc.argtypes = [vp, vp, vp, i64, i64, vp]
     lib.ssm_linscan_fwd_noalloc.restype = i32
     lib.ssm_profile_begin.argtypes = [i32]
@@ -100,6 +105,23 @@ def load(build_if_missing: bool = True):
             _declare(lib)
             _lib = lib
     return _lib
+
+
+_lib_debug = None
+
+
+def load_debug():
+    """Load the debug library (libssm_gb300_debug.so: the same kernels with device index checks,
+    built by __graft_entry__.build()), building it first if it is missing or stale.  It is a
+    separate library with its own state; only the tests use it."""
+    global _lib_debug
+    with _lock:
+        if _lib_debug is None:
+            path = _build.build(debug=True)
+            lib = ctypes.CDLL(path)
+            _declare(lib)
+            _lib_debug = lib
+    return _lib_debug
 
 
 def status_string(status: int) -> str:

@@ -34,6 +34,7 @@ namespace {
 
 std::atomic<uint32_t> g_epoch{0};
 std::atomic<int64_t> g_stall_tile{-1};
+std::atomic<int64_t> g_bounds_shrink{0};  // debug builds: see ssm_debug_set_bounds_fault
 std::atomic<uint64_t> g_spin_limit_ns{0};
 constexpr uint64_t kDefaultSpinLimitNs = 1000000000ull;  // 1 s per wait
 
@@ -111,6 +112,7 @@ SsdDims make_dims(int64_t batch, int64_t seqlen, int nheads, int headdim, int ds
   d.plan_fused = -1;
   d.plan_seq = -1;
   d.plan_scan_heads = 0;
+  d.debug_shrink = g_bounds_shrink.load(std::memory_order_relaxed);
   return d;
 }
 
@@ -338,6 +340,7 @@ const char* ssm_status_string(ssm_status status) {
     case SSM_ERR_WORKSPACE: return "SSM_ERR_WORKSPACE: workspace missing or too small";
     case SSM_ERR_CUDA: return "SSM_ERR_CUDA: CUDA runtime error";
     case SSM_ERR_TIMEOUT: return "SSM_ERR_TIMEOUT: a look-back wait exceeded its limit";
+    case SSM_ERR_BOUNDS: return "SSM_ERR_BOUNDS: a device index check of the debug build failed";
   }
   return "unknown ssm_status";
 }
@@ -641,6 +644,25 @@ ssm_status ssm_profile_end(double* ms_out, int64_t* launches_out) {
 void ssm_debug_set_lookback_fault(int64_t stall_tile, uint64_t spin_limit_ns) {
   g_stall_tile.store(stall_tile < 0 ? -1 : stall_tile, std::memory_order_relaxed);
   g_spin_limit_ns.store(spin_limit_ns, std::memory_order_relaxed);
+}
+
+int ssm_debug_build(void) {
+#ifdef SSM_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+ssm_status ssm_debug_set_bounds_fault(int64_t shrink) {
+#ifdef SSM_DEBUG
+  if (shrink < 0) return SSM_ERR_INVALID_ARG;
+  g_bounds_shrink.store(shrink, std::memory_order_relaxed);
+  return SSM_OK;
+#else
+  (void)shrink;
+  return SSM_ERR_UNSUPPORTED;
+#endif
 }
 
 int64_t ssm_debug_fused_schedule(int64_t chains, int64_t nchunks, int sms, int64_t* rows, int64_t cap) {

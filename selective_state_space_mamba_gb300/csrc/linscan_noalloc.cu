@@ -3,8 +3,6 @@
 // look-back descriptor per 4096-element tile) lives in a fixed array in device memory that
 // is part of this library, so the call needs neither a caller-supplied workspace nor any
 // allocation.  It launches exactly the kernel ssm_linscan_fwd launches.
-#include <mutex>
-
 #include <cstddef>
 
 #include "ssm_internal.cuh"
@@ -20,25 +18,15 @@ constexpr size_t kNoAllocScratchBytes = 256 + (size_t)(kNoAllocMaxElems / kLsTil
 // it; it keeps the previous call's contents.
 static __device__ __align__(256) unsigned char g_linscan_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {nullptr};
-
-// Device address of the scratch array on the current device, looked up once per device (in
-// host code the array's name is only a host-side stand-in, not a device address).
+// Device address of the scratch array on the current device.  In host code the array's name is
+// only a host-side stand-in, not a device address, so the address is looked up with the device
+// current; it is looked up on every call (cheap once the library's module is loaded), so that it
+// stays right after a cudaDeviceReset, which loads the module again, possibly elsewhere.
 cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_linscan_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_linscan_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return cudaSuccess;
 }
 

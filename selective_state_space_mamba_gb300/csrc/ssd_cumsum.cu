@@ -73,24 +73,27 @@ __global__ void __launch_bounds__(kCsThreads) ssd_chunk_cumsum_kernel(const DtT*
   const int lh = threadIdx.x % kCsHeads, lt = threadIdx.x / kCsHeads;
   const int tmax = d.seqlen - t0 < T ? (int)(d.seqlen - t0) : T;  // real tokens in this chunk
   const bool head_ok = lh < nhb;
-  const DtT* src = dt + (bi * d.seqlen + t0 + lt) * nh + h0 + (head_ok ? lh : 0);
+  const int64_t src0 = (bi * d.seqlen + t0 + lt) * nh + h0 + (head_ok ? lh : 0);
+  const DtT* src = dt + src0;
   uint32_t raw[kCsLoads];
 #pragma unroll
   for (int k = 0; k < kCsLoads; ++k) {
     const int t = lt + kTokStride * k;
     raw[k] = 0u;
-    if (head_ok && t < tmax) raw[k] = ld_bits(src + (int64_t)kTokStride * k * nh);
+    if (head_ok && t < tmax &&
+        SSM_CHECK(hdr, src0 + (int64_t)kTokStride * k * nh < d.batch * d.seqlen * nh))  // dt [b, L, nh]
+      raw[k] = ld_bits(src + (int64_t)kTokStride * k * nh);
   }
   float Ah[kCsHeadsPerWarp];
 #pragma unroll
   for (int q = 0; q < kCsHeadsPerWarp; ++q) {
     const int hh = warp + q * kCsWarps;
-    Ah[q] = hh < nhb ? A[h0 + hh] : 0.f;
+    Ah[q] = hh < nhb && SSM_CHECK(hdr, h0 + hh < nh) ? A[h0 + hh] : 0.f;
   }
 #pragma unroll
   for (int k = 0; k < kCsLoads; ++k) {
     const int t = lt + kTokStride * k;
-    if (t < T) s_dt[sidx(t, lh, srow)] = __uint_as_float(raw[k]);
+    if (t < T && SSM_CHECK(hdr, sidx(t, lh, srow) < kCsHeads * srow)) s_dt[sidx(t, lh, srow)] = __uint_as_float(raw[k]);
   }
   __syncthreads();
 
@@ -122,7 +125,10 @@ __global__ void __launch_bounds__(kCsThreads) ssd_chunk_cumsum_kernel(const DtT*
     const float excl = incl - run;
 #pragma unroll
     for (int k = 0; k < 8; ++k) gv[k] = (excl + gv[k]) * kLog2e;
-    if (hh < nhb) {
+    // G and dt^T are [b, nh, lpad]; debug builds check each lane's run against that size (less
+    // the test hook's shortfall)
+    if (hh < nhb && SSM_CHECK(hdr, (bi * nh + h0 + hh) * d.lpad + t0 + (lane + 1) * per_lane <=
+                                       d.batch * nh * d.lpad - d.debug_shrink)) {
       const int64_t off = (bi * nh + h0 + hh) * d.lpad + t0 + lane * per_lane;
       if (per_lane == 2) {
         *reinterpret_cast<float2*>(dtT + off) = make_float2(dv[0], dv[1]);

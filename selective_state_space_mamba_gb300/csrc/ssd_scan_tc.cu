@@ -72,7 +72,7 @@ struct ScParams {
   const float* dtT;
   const float* D;
   WsHeader* hdr;
-  int64_t lpad, nchunks;
+  int64_t batch, lpad, nchunks;
   int nheads, ngroups, chunk, row_tiles;
   int heads_per_item, items_per_tile;
 };
@@ -227,12 +227,16 @@ __global__ void __launch_bounds__(kScThreads, 1)
         mbar_arrive_expect_tx(&bars[kStFull + st], (uint32_t)Nj * kRowB + 2u * 64 * kRowB + 8u * T);
         for (int rb = 0; rb < Nj / 128; ++rb)
           tc::tma_load_3d(stage + rb * 128 * kRowB, &map_x, h * 64, tok0 + rb * 128, (int)bi, &bars[kStFull + st]);
-        const int hin_row = (int)(((bi * p.nchunks + c) * p.nheads + h) * 64);
-        for (int sb = 0; sb < 2; ++sb)
-          tma_load_2d(stage + L.hin_off + sb * 64 * kRowB, &map_hin, sb * 64, hin_row, &bars[kStFull + st]);
+        const int64_t hin_row = ((bi * p.nchunks + c) * p.nheads + h) * 64;
+        // h_in rows [b x nc x nh x 64] and the [b, nh, lpad] G / dt^T rows of this head and chunk
+        if (SSM_CHECK(p.hdr, h < p.nheads && hin_row + 64 <= p.batch * p.nchunks * p.nheads * 64))
+          for (int sb = 0; sb < 2; ++sb)
+            tma_load_2d(stage + L.hin_off + sb * 64 * kRowB, &map_hin, sb * 64, (int)hin_row, &bars[kStFull + st]);
         const int64_t grow = (bi * p.nheads + h) * p.lpad + tok0;
-        bulk_g2s(stage + L.g_off, p.G + grow, 4u * T, &bars[kStFull + st]);
-        bulk_g2s(stage + L.dt_off, p.dtT + grow, 4u * T, &bars[kStFull + st]);
+        if (SSM_CHECK(p.hdr, grow + T <= p.batch * p.nheads * p.lpad)) {
+          bulk_g2s(stage + L.g_off, p.G + grow, 4u * T, &bars[kStFull + st]);
+          bulk_g2s(stage + L.dt_off, p.dtT + grow, 4u * T, &bars[kStFull + st]);
+        }
         issued = k + 1;
       }
       for (int k = max(0, issued - 2); k < issued; ++k)
@@ -506,7 +510,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
       const float gi = g_s[i];
       const float e_i = tc::ex2_approx(gi);
       const float u_i = i0 > 0 ? tc::ex2_approx(gi - g_s[i0]) : 0.f;
-      const float Dh = p.D[h];
+      const float Dh = SSM_CHECK(p.hdr, h < p.nheads) ? p.D[h] : 0.f;
       uint32_t xr[32];  // x(i, 0 .. 63) as bf16 pairs
 #pragma unroll
       for (int cc = 0; cc < 8; ++cc) {
@@ -615,6 +619,7 @@ cudaError_t launch_ssd_chunk_scan_tc(const void* x, const void* B, const void* C
   p.dtT = ws.dtT;
   p.D = D;
   p.hdr = ws.hdr;
+  p.batch = d.batch;
   p.lpad = d.lpad;
   p.nchunks = d.nchunks;
   p.nheads = d.nheads;

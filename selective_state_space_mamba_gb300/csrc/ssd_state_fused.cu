@@ -64,7 +64,7 @@ struct SfParams {
   float* carry;      // [chains][128 rows][128] f32: the state where a chain's head ends
   unsigned long long* flags;  // [chains]: carry published (epoch-tagged)
   WsHeader* hdr;
-  int64_t lpad, nchunks, units;  // units = chains x nchunks
+  int64_t batch, lpad, nchunks, units;  // units = chains x nchunks
   int nheads, ngroups, chunk;
 };
 
@@ -245,6 +245,8 @@ __global__ void __launch_bounds__(kSfThreads, 1)
               tc::tma_load_3d(xst + hh * kSfKH * kSfRowBytes, &map_x, (h + hh) * 64, tok, (int)bi, &bars[kXFull + xs]);
             for (int hh = 0; hh < 2; ++hh) {
               const int64_t row = (bi * p.nheads + h + hh) * p.lpad + c * T;
+              // G and dt^T are [b, nh, lpad]: the chunk's T entries of this head
+              if (!SSM_CHECK(p.hdr, h + hh < p.nheads && row + T <= p.batch * p.nheads * p.lpad)) continue;
               bulk_g2s(gd + hh * kSfGdHead, p.G + row + kh * kSfKH, 4u * kSfKH, &bars[kXFull + xs]);
               bulk_g2s(gd + hh * kSfGdHead + 4u * kSfKH, p.dtT + row + kh * kSfKH, 4u * kSfKH, &bars[kXFull + xs]);
               bulk_g2s(gd + hh * kSfGdHead + 8u * kSfKH, p.G + row + T - 4, 16u, &bars[kXFull + xs]);
@@ -419,6 +421,12 @@ __global__ void __launch_bounds__(kSfThreads, 1)
       const int64_t bi = chain_bi(sg.chain);
       const int h = chain_h(sg.chain);
       const int64_t bh = bi * p.nheads + h + hh;
+      // the state rows of both heads (h0, h_final, G) and the chain's published state and flag;
+      // the same answer in every state thread, so that they leave together
+      if (!SSM_CHECK(p.hdr, bi * p.nheads + h + 1 < p.batch * p.nheads && sg.chain < p.units / nc)) {
+        ok = false;
+        break;
+      }
       const float* h0r = p.h0 ? p.h0 + (bh * 64 + pp) * 128 + col0 : nullptr;
       float* cr = p.carry + (sg.chain * 128 + m) * 128 + col0;  // this row of the chain's published state
       const float* Glast = p.G + bh * p.lpad + (T - 1);  // G_last of chunk c at Glast[c * T]
@@ -505,8 +513,10 @@ __global__ void __launch_bounds__(kSfThreads, 1)
         tc::fence_before_sync();
         named_bar_sync(kSfStateBar, kSfStateThreads);
         if (leader) {
-          const int row0 = (int)(((bi * nc + c) * p.nheads + h) * 64);  // the pair's 128 rows of h_in[c]
-          for (int s2 = 0; s2 < 2; ++s2) tma_store_2d(&map_hin, base + L.hs0 + s2 * (128 * kSfRowBytes), 64 * s2, row0);
+          const int64_t row0 = ((bi * nc + c) * p.nheads + h) * 64;  // the pair's 128 rows of h_in[c]
+          if (SSM_CHECK(p.hdr, c < nc && row0 + 128 <= p.batch * nc * p.nheads * 64))
+            for (int s2 = 0; s2 < 2; ++s2)
+              tma_store_2d(&map_hin, base + L.hs0 + s2 * (128 * kSfRowBytes), 64 * s2, (int)row0);
           bulk_commit();
           mbar_arrive(&bars[kSFree + sb]);  // S[sb] may take the chunk run two later
           if (publish) st_release_u64(&p.flags[sg.chain], make_flag(ctl.epoch, kFlagPrefix));
@@ -621,6 +631,7 @@ cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float*
   p.carry = ws.Sc;  // the chunk-state buffer is free on this path: one state per split chain
   p.flags = ws.flags;
   p.hdr = ws.hdr;
+  p.batch = d.batch;
   p.lpad = d.lpad;
   p.nchunks = d.nchunks;
   p.nheads = d.nheads;

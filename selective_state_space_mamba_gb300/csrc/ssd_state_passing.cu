@@ -242,6 +242,12 @@ __global__ void __launch_bounds__(kSeqThreads) ssd_state_passing_seq_kernel(cons
   const int64_t nc = d.nchunks;
   const float* Grow = ws.G + bh * d.lpad + (d.chunk - 1);  // G_last of chunk c at Grow[c * chunk]
   const int64_t step = (int64_t)d.nheads * HS;              // chunk c -> c + 1 in S_c and h_in
+  // S_c and h_in are [b, nc, nh, H, S]: this thread's four entries over every chunk; G is
+  // [b, nh, lpad]: this head's last G of every chunk
+  if (!SSM_CHECK(ws.hdr, (bi * nc * d.nheads + h) * (int64_t)HS + e + (nc > 0 ? nc - 1 : 0) * (int64_t)d.nheads * HS + 4 <=
+                             d.batch * nc * d.nheads * (int64_t)HS &&
+                             bh * d.lpad + nc * d.chunk <= d.batch * d.nheads * d.lpad))
+    return;
   const float* src = ws.Sc + (bi * nc * d.nheads + h) * (int64_t)HS + e;
   HinT* hin = static_cast<HinT*>(ws.hin) + (bi * nc * d.nheads + h) * (int64_t)HS + e;
   float4* slot = &ring[0][threadIdx.x];

@@ -68,7 +68,7 @@ struct CsParams {
   const float* dtT;
   float* Sc;
   WsHeader* hdr;
-  int64_t lpad, nchunks, units;
+  int64_t batch, lpad, nchunks, units;
   int nheads, ngroups, chunk;
 };
 
@@ -199,6 +199,8 @@ __global__ void __launch_bounds__(kCsThreads, 1)
             tc::tma_load_3d(base + st * L.stage_bytes + hh * kCsKH * kCsRowBytes, &map_x, (w.h + hh) * 64,
                             (int)(w.c * T + kh * kCsKH), (int)w.bi, &bars[kXFull + st]);
             const int64_t row = (w.bi * p.nheads + w.h + hh) * p.lpad + w.c * T;
+            // G and dt^T are [b, nh, lpad]: the chunk's T entries of this head
+            if (!SSM_CHECK(p.hdr, w.h + hh < p.nheads && row + T <= p.batch * p.nheads * p.lpad)) continue;
             bulk_g2s(gd + hh * kCsGdHead, p.G + row + kh * kCsKH, 4u * kCsKH, &bars[kXFull + st]);
             bulk_g2s(gd + hh * kCsGdHead + 4u * kCsKH, p.dtT + row + kh * kCsKH, 4u * kCsKH, &bars[kXFull + st]);
             bulk_g2s(gd + hh * kCsGdHead + 8u * kCsKH, p.G + row + T - 4, 16u, &bars[kXFull + st]);
@@ -433,6 +435,7 @@ cudaError_t launch_ssd_chunk_state_tc(const void* x, const void* B, const SsdDim
   p.dtT = ws.dtT;
   p.Sc = ws.Sc;
   p.hdr = ws.hdr;
+  p.batch = d.batch;
   p.lpad = d.lpad;
   p.nchunks = d.nchunks;
   p.nheads = d.nheads;

@@ -97,6 +97,20 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 __device__ __forceinline__ void record_error(WsHeader* hdr, uint32_t epoch, uint32_t code) {
   atomicCAS(&hdr->status, 0ull, ((unsigned long long)epoch << 32) | code);
 }
+
+// Device index checks of debug builds (-DSSM_DEBUG).  SSM_CHECK(hdr, cond) is true when cond
+// holds; otherwise it records SSM_ERR_BOUNDS in the workspace status word (reported by
+// ssm_check_device_status; epoch 0, so that no wait of the call takes it for an abort) and
+// the caller skips the access.  Release builds compile it to the constant true.
+__device__ __forceinline__ bool debug_check(bool ok, WsHeader* hdr) {
+  if (!ok) record_error(hdr, 0u, SSM_ERR_BOUNDS);
+  return ok;
+}
+#ifdef SSM_DEBUG
+#define SSM_CHECK(hdr, cond) ::ssm::debug_check((cond), (hdr))
+#else
+#define SSM_CHECK(hdr, cond) true
+#endif
 __device__ __forceinline__ bool call_aborted(const WsHeader* hdr, uint32_t epoch) {
   unsigned long long s = ld_relaxed_u64(&hdr->status);
   return s != 0ull && (uint32_t)(s >> 32) == epoch;
@@ -323,6 +337,7 @@ struct SsdDims {
   int plan_fused;        // 1: chunk states and state passing in one kernel, 0: two kernels
   int plan_seq;          // 1: sequential state passing, 0: look-back state passing
   int plan_scan_heads;   // chunk scan: heads per CTA (0: cost model)
+  int64_t debug_shrink;  // debug builds: bound shortfall of the cumsum store check (test hook)
 };
 
 // State passing tiling: a tile covers kSpElems state entries of one (batch, head) for up

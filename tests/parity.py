@@ -42,9 +42,17 @@ def assert_f32_close(got, ref, what):
 
 
 def assert_rows_close(got, ref, what):
-    """Per-row normwise float32 rule for the scan."""
-    for r in range(ref.shape[0]):
-        assert_f32_close(got[r], ref[r], f"{what} row {r}")
+    """Per-row normwise float32 rule for the scan: max_t |got - ref| <= 1e-4 max_t |ref| per row."""
+    ref = np.asarray(ref, np.float64)
+    if ref.size == 0:
+        return
+    d = np.abs(np.asarray(got, np.float64) - ref).reshape(ref.shape[0], -1)
+    scale = np.max(np.abs(ref), axis=1) if ref.ndim > 1 else np.abs(ref)
+    dmax = d.max(axis=1)
+    bad = ~((dmax <= F32_RTOL * scale) | (dmax == 0.0))
+    if bad.any():
+        r = int(np.argmax(bad))
+        assert_f32_close(np.asarray(got)[r], ref[r], f"{what} row {r}")
 
 
 def assert_bf16_close(got, ref, what, rms_tol):

@@ -34,14 +34,25 @@ def test_library_exports_every_declared_symbol(lib):
     assert all(s.startswith("ssm_") for s in exported), "only the C ABI is exported"
 
 
+def test_debug_library_exports_every_declared_symbol():
+    # the debug variant (device index checks) is the same ABI; building it is host-only work
+    import ctypes
+    from selective_state_space_mamba_gb300 import _build as b
+    path = b.build(debug=True)
+    dl = ctypes.CDLL(path)
+    for name in _lib.EXPORTS:
+        assert hasattr(dl, name), name
+
+
 def test_library_targets_sm103a():
     assert "arch=compute_103a,code=sm_103a" in " ".join(_build.ARCH)
 
 
 def test_status_strings(lib):
-    for code in range(7):
+    for code in range(8):
         s = _lib.status_string(code)
         assert s.startswith("SSM_")
+    assert _lib.status_string(_lib.SSM_ERR_BOUNDS).startswith("SSM_ERR_BOUNDS")
     assert _lib.status_string(99) == "unknown ssm_status"
     assert lib.ssm_version().decode().count(".") == 2
 
