@@ -4,8 +4,12 @@ Tolerances (fixed for this method, written here once):
   float32 workloads: max |GPU - oracle| <= 1e-4 * max |oracle|, per output tensor (the scan:
     per row).  Relative error is undefined at zero crossings, so "max relative error 1e-4"
     is read normwise.
-  bf16-input workloads (float32 accumulation): max |dy| <= 2e-2 * RMS(y_oracle) and
-    max |dh_final| <= 1e-2 * RMS(h_final_oracle).
+  bf16-input workloads (float32 accumulation): |dy| <= 2e-2 * RMS(y_oracle) + 2^-8 |y_oracle|
+    per element, and max |dh_final| <= 1e-2 * RMS(h_final_oracle).  y is returned in bf16 (the
+    inputs' dtype), whose own rounding alone moves an element by up to 2^-8 of its size: more
+    than 2e-2 * RMS wherever |y| exceeds about 5 RMS (an element of -8.03 at RMS 1.02 rounds to
+    -8.0), so the stated 2e-2 * RMS bounds the computation and the output's rounding is added.
+    h_final is float32 and has no such term.
 """
 from __future__ import annotations
 
@@ -14,6 +18,7 @@ import numpy as np
 F32_RTOL = 1e-4
 BF16_Y_RMS = 2e-2
 BF16_H_RMS = 1e-2
+BF16_OUT_U = 2.0 ** -8  # unit roundoff of a bf16 output (8 significand bits, round to nearest)
 
 
 def to_dev(arr, dtype="f32", device="cuda"):
@@ -55,13 +60,18 @@ def assert_rows_close(got, ref, what):
         assert_f32_close(np.asarray(got)[r], ref[r], f"{what} row {r}")
 
 
-def assert_bf16_close(got, ref, what, rms_tol):
+def assert_bf16_close(got, ref, what, rms_tol, out_u=0.0):
+    """max |got - ref| - out_u |ref| <= rms_tol * RMS(ref): out_u is the output format's unit
+    roundoff (BF16_OUT_U for a bf16 output, 0 for a float32 one)."""
     if ref.size == 0:
         return
-    d, i = err_report(got, ref)
+    ref = np.asarray(ref, np.float64)
+    d = np.abs(np.asarray(got, np.float64) - ref) - out_u * np.abs(ref)
+    i = np.unravel_index(int(np.argmax(d)), d.shape)
     rms = float(np.sqrt(np.mean(ref * ref)))
     assert d[i] <= rms_tol * rms, (
-        f"{what}: max|d|={d[i]:.3e} at {i} (gpu {np.asarray(got)[i]!r}, oracle {ref[i]!r}) > {rms_tol}*RMS {rms:.3e}")
+        f"{what}: |d| - {out_u:.3g}|ref| = {d[i]:.3e} at {i} (gpu {np.asarray(got)[i]!r}, oracle {ref[i]!r}) > "
+        f"{rms_tol}*RMS {rms:.3e}")
 
 
 def assert_ssd_close(dtype, y, y_ref, hf, hf_ref, what):
@@ -70,7 +80,7 @@ def assert_ssd_close(dtype, y, y_ref, hf, hf_ref, what):
         if hf_ref is not None:
             assert_f32_close(hf, hf_ref, f"{what} h_final")
     else:
-        assert_bf16_close(y, y_ref, f"{what} y", BF16_Y_RMS)
+        assert_bf16_close(y, y_ref, f"{what} y", BF16_Y_RMS, BF16_OUT_U)
         if hf_ref is not None:
             assert_bf16_close(hf, hf_ref, f"{what} h_final", BF16_H_RMS)
 
