@@ -261,6 +261,13 @@ def run_ours(args, world, rank, local):
     def scan_call():
         ssm.linscan_fwd(a, bsc, h=h)
 
+    # the scan's CTA shape, chosen the same way (ssm_linscan_fwd_tune)
+    if args.plan == "tune":
+        scan_shape, scan_shape_ms = ssm.tune_linscan_fwd(a, bsc, h=h, reps=5)
+    else:
+        ssm.set_linscan_shape(SCAN.rows, SCAN.length, -1)
+        scan_shape, scan_shape_ms = -1, 0.0
+
     for _ in range(args.warmup):
         flush.fill_(1)
         ssd_call()
@@ -374,7 +381,10 @@ def run_ours(args, world, rank, local):
             "l2": "inputs larger than L2, and L2 flushed by a 256 MiB write before each timed step",
             "parallelism": f"replicas x{world} (independent problems, no collective)",
             "plan": {"id": plan, "fused_state_path": (plan & 3) - 1, "sequential_state_passing": ((plan >> 2) & 3) - 1,
-                     "scan_heads_per_cta": plan >> 4, "tuning_median_ms": round(plan_ms, 4), "how": plan_how},
+                     "scan_heads_per_cta": (plan >> 4) & 0xffff, "fused_ring_split": ("rule", "4+3", "3+4", "5+2")[
+                         (plan >> 20) & 3], "tuning_median_ms": round(plan_ms, 4), "how": plan_how},
+            "scan_shape": {"id": scan_shape, "tuning_median_ms": round(scan_shape_ms, 4),
+                           "how": "ssm_linscan_fwd_tune before the warm-up (-1: the rule of thumb)"},
         },
         "timing": f"median of {args.steps} per-step CUDA-event samples (min / median / max below)",
         "ssd": {"tokens_per_s": round(value, 1), "ms": round(ssd_ms_max, 4), "ms_min_median_max": spread(ssd_s),

@@ -140,10 +140,13 @@ SSM_API ssm_status ssm_ssd_fwd(const void *x, const void *dt, const float *A, co
  *     ranges of chunks, and a CTA that starts inside a chain waits (bounded) for the state its
  *     predecessor publishes; it relies on all of its CTAs being resident at once, so where
  *     other work holds SMs for longer than the wait limit the call reports SSM_ERR_TIMEOUT;
+ *   - the one-kernel pass's shared-memory ring split: X slots (loaded from DRAM) and B slots
+ *     (loaded from L2) share a fixed budget: 4 + 3, 3 + 4 or 5 + 2;
  *   - the chunk scan's run of heads per CTA (the tensor-core path).
  * Without a plan, ssm_ssd_fwd picks by fixed rules of thumb.  A plan id packs
- * (fused + 1) | (sequential + 1) << 2 | heads_per_cta << 4, where fused and sequential are 1
- * (yes), 0 (no) or -1 (rule of thumb) and heads_per_cta 0 means the rule of thumb.
+ * (fused + 1) | (sequential + 1) << 2 | heads_per_cta << 4 | ring << 20, where fused and
+ * sequential are 1 (yes), 0 (no) or -1 (rule of thumb), heads_per_cta (0 .. 65535) 0 means the
+ * rule of thumb, and ring is 1 (4 + 3), 2 (3 + 4), 3 (5 + 2) or 0 (the rule: 4 + 3).
  *
  * ssm_ssd_fwd_tune takes exactly ssm_ssd_fwd's arguments and runs every candidate plan for
  * these sizes on the caller's buffers (y and h_final are overwritten; each candidate computes
@@ -213,6 +216,34 @@ SSM_API size_t ssm_linscan_workspace_bytes(int64_t rows, int64_t len);
  */
 SSM_API ssm_status ssm_linscan_fwd(const float *a, const float *b, float *h, int64_t rows, int64_t len,
                            void *workspace, size_t workspace_bytes, ssm_stream_t stream);
+
+/*
+ * Per-size CTA shapes of ssm_linscan_fwd (the scan counterpart of the SSD plans above, after the
+ * block-size and occupancy search of "Accelerating Mamba-2 with High-Performance Forward Pass
+ * Kernels in NVIDIA CUDA Tile", section "Mamba-2 performance optimization").  A shape fixes the
+ * look-back scan's CTA: its consumer groups (which take the CTA's tiles in turn), the depth of
+ * its shared-memory ring and the CTAs resident per SM:
+ *   1  two groups, 7 stages, one CTA per SM (the rule for rows of at least 4 tiles)
+ *   2  one group, 3 stages, two CTAs per SM (the rule for shorter rows)
+ *   3  two groups, 6 stages, one CTA per SM
+ *   4  one group, 6 stages, one CTA per SM
+ * ssm_linscan_fwd_tune takes ssm_linscan_fwd's arguments, runs every shape on the caller's
+ * buffers (h is overwritten with the scan; a warm-up and `reps` timed runs each, CUDA events on
+ * `stream`, synchronizing it) and stores the shape with the smallest median time for the current
+ * device and these (rows, len) in a process-wide table that later ssm_linscan_fwd calls use;
+ * *shape_out and *ms_out (either may be NULL) receive it and its time.  A device error recorded
+ * by a candidate (SSM_ERR_TIMEOUT) is returned and nothing is stored.  ssm_linscan_set_shape
+ * stores a shape (-1 or 0 removes the entry), ssm_linscan_get_shape reads it (-1: none, the
+ * rule applies), ssm_linscan_clear_shapes empties the table.  ssm_linscan_fwd_noalloc always
+ * takes the rule.  Errors: as ssm_linscan_fwd, plus SSM_ERR_INVALID_ARG for reps < 1 or a shape
+ * outside -1 .. 4.
+ */
+SSM_API ssm_status ssm_linscan_fwd_tune(const float *a, const float *b, float *h, int64_t rows, int64_t len,
+                                        void *workspace, size_t workspace_bytes, ssm_stream_t stream, int reps,
+                                        int *shape_out, float *ms_out);
+SSM_API ssm_status ssm_linscan_set_shape(int64_t rows, int64_t len, int shape);
+SSM_API ssm_status ssm_linscan_get_shape(int64_t rows, int64_t len, int *shape);
+SSM_API void ssm_linscan_clear_shapes(void);
 
 /*
  * Scalar selective scan for callers that cannot allocate device memory (the pages have no

@@ -17,7 +17,8 @@ from . import _lib
 from ._lib import SSM_BF16, SSM_F32, SsmError
 
 __all__ = ["ssd_fwd", "ssd_step", "linscan_fwd", "linscan_baseline", "tune_ssd_fwd", "set_ssd_fwd_plan",
-           "get_ssd_fwd_plan", "clear_ssd_fwd_plans", "plan_id", "Workspace", "check_device_status", "ssd_fwd_workspace_bytes",
+           "get_ssd_fwd_plan", "clear_ssd_fwd_plans", "plan_id", "tune_linscan_fwd",
+           "set_linscan_shape", "get_linscan_shape", "clear_linscan_shapes", "Workspace", "check_device_status", "ssd_fwd_workspace_bytes",
            "linscan_workspace_bytes", "SsmError", "version"]
 
 
@@ -157,9 +158,10 @@ def _ssd_sizes(x, B, chunk):
     return b, L, nh, H, S, G, chunk, _dtype_code(x)
 
 
-def plan_id(fused: int = -1, sequential: int = -1, heads_per_cta: int = 0) -> int:
-    """Pack a plan for ssd_fwd (see include/ssm.h): each flag 1, 0 or -1 (rule of thumb)."""
-    return (fused + 1) | ((sequential + 1) << 2) | (heads_per_cta << 4)
+def plan_id(fused: int = -1, sequential: int = -1, heads_per_cta: int = 0, fused_ring: int = 0) -> int:
+    """Pack a plan for ssd_fwd (see include/ssm.h): each flag 1, 0 or -1 (rule of thumb); fused_ring
+    1, 2 or 3 picks the fused pass's X + B slot split (4 + 3, 3 + 4, 5 + 2), 0 its rule."""
+    return (fused + 1) | ((sequential + 1) << 2) | (heads_per_cta << 4) | (fused_ring << 20)
 
 
 def tune_ssd_fwd(x, dt, A, B, C, D, h0=None, chunk: int = 256, reps: int = 5, *, y=None, h_final=None,
@@ -259,6 +261,45 @@ def linscan_fwd(a, b, *, h=None, workspace: Workspace | None = None):
     st = lib.ssm_linscan_fwd(_ptr(a), _ptr(b), _ptr(h), rows, L, ws.ptr(), ws.nbytes, _stream_ptr(a.device))
     _lib.check(st, "ssm_linscan_fwd")
     return h
+
+
+def tune_linscan_fwd(a, b, *, h=None, reps: int = 5, workspace: Workspace | None = None):
+    """Time every CTA shape of linscan_fwd for these sizes on these tensors and keep the fastest
+    for later calls of the same sizes (ssm_linscan_fwd_tune).  Returns (shape, median ms)."""
+    import ctypes
+    torch = _torch()
+    lib = _lib.load()
+    _require(a.shape == b.shape and a.dim() == 2, "a, b must be [rows, L] and equal")
+    _require(a.dtype == torch.float32 and b.dtype == torch.float32, "a, b must be float32")
+    _require(a.is_cuda and b.is_cuda and a.is_contiguous() and b.is_contiguous(), "contiguous CUDA tensors")
+    rows, L = a.shape
+    if h is None:
+        h = torch.empty_like(a)
+    need = lib.ssm_linscan_workspace_bytes(rows, L)
+    ws = workspace if workspace is not None else _workspace("linscan", a.device, max(need, 1))
+    if workspace is not None:
+        ws.ensure(need)
+    shape, ms = ctypes.c_int(-1), ctypes.c_float(0.0)
+    _lib.check(lib.ssm_linscan_fwd_tune(_ptr(a), _ptr(b), _ptr(h), rows, L, ws.ptr(), ws.nbytes, _stream_ptr(a.device),
+                                        int(reps), ctypes.byref(shape), ctypes.byref(ms)), "ssm_linscan_fwd_tune")
+    return shape.value, ms.value
+
+
+def set_linscan_shape(rows: int, length: int, shape: int) -> None:
+    """Store a CTA shape (1 .. 4; -1 removes) for linscan_fwd calls of these sizes."""
+    _lib.check(_lib.load().ssm_linscan_set_shape(int(rows), int(length), int(shape)), "ssm_linscan_set_shape")
+
+
+def get_linscan_shape(rows: int, length: int) -> int:
+    """The stored CTA shape for these sizes, or -1 (the rule applies)."""
+    import ctypes
+    v = ctypes.c_int(-1)
+    _lib.check(_lib.load().ssm_linscan_get_shape(int(rows), int(length), ctypes.byref(v)), "ssm_linscan_get_shape")
+    return v.value
+
+
+def clear_linscan_shapes() -> None:
+    _lib.load().ssm_linscan_clear_shapes()
 
 
 SCAN_BASELINES = {"blelloch": _lib.SSM_SCAN_BLELLOCH, "three_pass": _lib.SSM_SCAN_THREE_PASS,

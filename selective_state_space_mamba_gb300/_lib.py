@@ -23,7 +23,8 @@ EXPORTS = ("ssm_status_string", "ssm_version", "ssm_ssd_fwd_workspace_bytes", "s
            "ssm_debug_set_lookback_fault", "ssm_profile_begin", "ssm_profile_end", "ssm_linscan_fwd_noalloc",
            "ssm_ssd_step", "ssm_linscan_baseline_workspace_bytes", "ssm_linscan_baseline", "ssm_ssd_fwd_tune",
            "ssm_ssd_fwd_set_plan", "ssm_ssd_fwd_get_plan", "ssm_ssd_fwd_clear_plans", "ssm_debug_fused_schedule",
-           "ssm_debug_build", "ssm_debug_set_bounds_fault")
+           "ssm_debug_build", "ssm_debug_set_bounds_fault", "ssm_linscan_fwd_tune", "ssm_linscan_set_shape",
+           "ssm_linscan_get_shape", "ssm_linscan_clear_shapes")
 PROFILE_KERNELS = ("linscan_lookback", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
                    "ssd_state_fused", "ssd_step", "linscan_baseline")
 
@@ -67,6 +68,14 @@ def _declare(lib):
     lib.ssm_linscan_workspace_bytes.restype = sz
     lib.ssm_linscan_fwd.argtypes = [vp, vp, vp, i64, i64, vp, sz, vp]
     lib.ssm_linscan_fwd.restype = i32
+    lib.ssm_linscan_fwd_tune.argtypes = [vp, vp, vp, i64, i64, vp, sz, vp, i32, vp, vp]
+    lib.ssm_linscan_fwd_tune.restype = i32
+    lib.ssm_linscan_set_shape.argtypes = [i64, i64, i32]
+    lib.ssm_linscan_set_shape.restype = i32
+    lib.ssm_linscan_get_shape.argtypes = [i64, i64, vp]
+    lib.ssm_linscan_get_shape.restype = i32
+    lib.ssm_linscan_clear_shapes.argtypes = []
+    lib.ssm_linscan_clear_shapes.restype = None
     lib.ssm_check_device_status.argtypes = [vp, vp]
     lib.ssm_check_device_status.restype = i32
     lib.ssm_debug_set_lookback_fault.argtypes = [i64, u64]

@@ -112,12 +112,14 @@ SsdDims make_dims(int64_t batch, int64_t seqlen, int nheads, int headdim, int ds
   d.plan_fused = -1;
   d.plan_seq = -1;
   d.plan_scan_heads = 0;
+  d.plan_ring = 0;
   d.debug_shrink = g_bounds_shrink.load(std::memory_order_relaxed);
   return d;
 }
 
 // ---- per-shape plans (ssm_ssd_fwd_tune / ssm_ssd_fwd_set_plan) ----
-// A plan id packs (fused + 1) | (seq + 1) << 2 | scan_heads << 4, with -1 meaning "the heuristic".
+// A plan id packs (fused + 1) | (seq + 1) << 2 | scan_heads << 4 | ring << 20, with -1 (0 for
+// scan_heads and ring) meaning "the heuristic".
 struct PlanKey {
   int dev;
   int64_t batch, seqlen;
@@ -136,13 +138,27 @@ bool plan_key(const SsdDims& d, PlanKey* k) {
   *k = PlanKey{dev, d.batch, d.seqlen, d.nheads, d.headdim, d.dstate, d.ngroups, d.chunk, (int)d.dtype};
   return true;
 }
-int plan_id(int fused, int seq, int heads) { return (fused + 1) | ((seq + 1) << 2) | (heads << 4); }
-bool plan_valid(int id) { return id >= 0 && (id & 3) != 3 && ((id >> 2) & 3) != 3 && (id >> 4) <= 65535; }
+int plan_id(int fused, int seq, int heads, int ring = 0) {
+  return (fused + 1) | ((seq + 1) << 2) | (heads << 4) | (ring << 20);
+}
+bool plan_valid(int id) { return id >= 0 && (id & 3) != 3 && ((id >> 2) & 3) != 3 && (id >> 20) <= 3; }
 void apply_plan(SsdDims& d, int id) {
   d.plan_fused = (id & 3) - 1;
   d.plan_seq = ((id >> 2) & 3) - 1;
-  d.plan_scan_heads = id >> 4;
+  d.plan_scan_heads = (id >> 4) & 0xffff;
+  d.plan_ring = (id >> 20) & 3;
 }
+// ---- per-size CTA shapes of the scalar scan (ssm_linscan_fwd_tune / ssm_linscan_set_shape) ----
+std::mutex g_ls_mu;
+std::map<std::tuple<int, int64_t, int64_t>, int> g_ls_shapes;
+int cached_ls_shape(int64_t rows, int64_t len) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lk(g_ls_mu);
+  const auto it = g_ls_shapes.find(std::make_tuple(dev, rows, len));
+  return it == g_ls_shapes.end() ? 0 : it->second;
+}
+
 void apply_cached_plan(SsdDims& d) {
   PlanKey k;
   if (!plan_key(d, &k)) return;
@@ -405,7 +421,8 @@ ssm_status ssm_ssd_fwd_tune(const void* x, const void* dt, const float* A, const
     heads.erase(std::unique(heads.begin() + 1, heads.end()), heads.end());
   }
   for (int hd : heads) {
-    if (ssd_tc_supported(d) && ssd_state_fused_possible(d)) cands.push_back(plan_id(1, -1, hd));
+    if (ssd_tc_supported(d) && ssd_state_fused_possible(d))
+      for (int ring = 1; ring <= 3; ++ring) cands.push_back(plan_id(1, -1, hd, ring));  // ring splits
     cands.push_back(plan_id(0, 1, hd));
     cands.push_back(plan_id(0, 0, hd));
   }
@@ -549,9 +566,98 @@ ssm_status ssm_linscan_fwd(const float* a, const float* b, float* h, int64_t row
   const LinscanWorkspace ws = linscan_workspace_layout(n, workspace);
   const LookbackCtl ctl = next_lookback_ctl();
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (timed_launch(0, s, [&] { return launch_linscan(a, b, h, rows, len, ws, ctl, s); }) != cudaSuccess)
+  const int shape = cached_ls_shape(rows, len);
+  if (timed_launch(0, s, [&] { return launch_linscan(a, b, h, rows, len, ws, ctl, s, shape); }) != cudaSuccess)
     return SSM_ERR_CUDA;
   return SSM_OK;
+}
+
+ssm_status ssm_linscan_fwd_tune(const float* a, const float* b, float* h, int64_t rows, int64_t len, void* workspace,
+                                size_t workspace_bytes, ssm_stream_t stream, int reps, int* shape_out, float* ms_out) {
+  if (reps < 1) return SSM_ERR_INVALID_ARG;
+  if (shape_out) *shape_out = -1;
+  if (ms_out) *ms_out = 0.f;
+  // the same argument checks as a call, by a call with the rule's shape
+  ssm_status st = ssm_linscan_fwd(a, b, h, rows, len, workspace, workspace_bytes, stream);
+  if (st != SSM_OK || rows == 0 || len == 0) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const LinscanWorkspace ws = linscan_workspace_layout(rows * len, workspace);
+  cudaEvent_t e0, e1;
+  if (cudaEventCreate(&e0) != cudaSuccess) return SSM_ERR_CUDA;
+  if (cudaEventCreate(&e1) != cudaSuccess) {
+    cudaEventDestroy(e0);
+    return SSM_ERR_CUDA;
+  }
+  int best = -1;
+  float best_ms = 0.f;
+  for (int shape = 1; shape <= kLsShapes && st == SSM_OK; ++shape) {
+    std::vector<float> t;
+    for (int r = 0; r <= reps && st == SSM_OK; ++r) {  // one warm-up, then `reps` timed runs
+      if (cudaEventRecord(e0, s) != cudaSuccess ||
+          launch_linscan(a, b, h, rows, len, ws, next_lookback_ctl(), s, shape) != cudaSuccess ||
+          cudaEventRecord(e1, s) != cudaSuccess) {
+        st = SSM_ERR_CUDA;
+        break;
+      }
+      float ms = 0.f;
+      if (cudaEventSynchronize(e1) != cudaSuccess || cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess) {
+        st = SSM_ERR_CUDA;
+        break;
+      }
+      if (r > 0) t.push_back(ms);
+    }
+    if (st != SSM_OK) break;
+    unsigned long long word = 0;  // a device-side timeout in a candidate is reported, not skipped
+    if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) {
+      st = SSM_ERR_CUDA;
+      break;
+    }
+    if (word != 0) {
+      st = static_cast<ssm_status>(word & 0xffffffffu);
+      break;
+    }
+    std::sort(t.begin(), t.end());
+    if (best < 0 || t[t.size() / 2] < best_ms) {
+      best = shape;
+      best_ms = t[t.size() / 2];
+    }
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (st != SSM_OK) return st;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_ls_mu);
+    g_ls_shapes[std::make_tuple(dev, rows, len)] = best;
+  }
+  if (shape_out) *shape_out = best;
+  if (ms_out) *ms_out = best_ms;
+  return SSM_OK;
+}
+
+ssm_status ssm_linscan_set_shape(int64_t rows, int64_t len, int shape) {
+  if (rows < 0 || len < 0 || shape < -1 || shape > kLsShapes) return SSM_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SSM_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_ls_mu);
+  if (shape <= 0)
+    g_ls_shapes.erase(std::make_tuple(dev, rows, len));
+  else
+    g_ls_shapes[std::make_tuple(dev, rows, len)] = shape;
+  return SSM_OK;
+}
+
+ssm_status ssm_linscan_get_shape(int64_t rows, int64_t len, int* shape) {
+  if (!shape || rows < 0 || len < 0) return SSM_ERR_INVALID_ARG;
+  *shape = cached_ls_shape(rows, len);
+  if (*shape == 0) *shape = -1;
+  return SSM_OK;
+}
+
+void ssm_linscan_clear_shapes(void) {
+  std::lock_guard<std::mutex> lk(g_ls_mu);
+  g_ls_shapes.clear();
 }
 
 size_t ssm_linscan_baseline_workspace_bytes(ssm_scan_algo algo, int64_t rows, int64_t len) {

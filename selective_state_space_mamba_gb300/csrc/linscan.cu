@@ -92,6 +92,9 @@ struct LsCfg {
 #endif
 using LsLongRows = LsCfg<2, SSM_LS_LONG_STAGES, 1>;  // one CTA per SM (224 KB of stages)
 using LsShortRows = LsCfg<1, 3, 2>;  // two CTAs per SM (96 KB of stages each)
+// further CTA shapes the per-size tuner (ssm_linscan_fwd_tune) chooses among
+using LsTwoGroups6 = LsCfg<2, 6, 1>;  // two groups, 6 stages, one CTA per SM
+using LsOneGroup6 = LsCfg<1, 6, 1>;   // one group, 6 stages, one CTA per SM
 
 template <class Cfg>
 struct LsShared {
@@ -504,7 +507,7 @@ __global__ void __launch_bounds__(Cfg::kBlock, Cfg::kMinBlocks)
 }
 
 // Grid (resident CTAs: every CTA of a launch runs at once) per device and CTA shape.
-int g_ls_grid[2][64] = {};
+int g_ls_grid[4][64] = {};
 
 template <class Cfg>
 cudaError_t launch_cfg(int slot, int dev, const CUtensorMap& map_a, const CUtensorMap& map_b, const CUtensorMap& map_h,
@@ -538,7 +541,7 @@ cudaError_t launch_cfg(int slot, int dev, const CUtensorMap& map_a, const CUtens
 #endif
 
 cudaError_t launch_linscan(const float* a, const float* b, float* h, int64_t rows, int64_t len,
-                           const LinscanWorkspace& ws, const LookbackCtl& ctl, cudaStream_t s) {
+                           const LinscanWorkspace& ws, const LookbackCtl& ctl, cudaStream_t s, int shape) {
   LsArgs p{a, b, h, rows * len, len, (rows * len) / kLsRow};
   if (p.lines > 0x7fffffffLL) return cudaErrorInvalidValue;  // TMA coordinates are 32-bit
   CUtensorMap map_a{}, map_b{}, map_h{};
@@ -559,9 +562,14 @@ cudaError_t launch_linscan(const float* a, const float* b, float* h, int64_t row
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64) return cudaErrorInvalidDevice;
-  if (len >= (int64_t)SSM_LS_LONG_ROW_TILES * kLsTile)
-    return launch_cfg<LsLongRows>(0, dev, map_a, map_b, map_h, p, ws, ctl, s);
-  return launch_cfg<LsShortRows>(1, dev, map_a, map_b, map_h, p, ws, ctl, s);
+  if (shape == 0) shape = len >= (int64_t)SSM_LS_LONG_ROW_TILES * kLsTile ? 1 : 2;  // the rule
+  switch (shape) {
+    case 1: return launch_cfg<LsLongRows>(0, dev, map_a, map_b, map_h, p, ws, ctl, s);
+    case 2: return launch_cfg<LsShortRows>(1, dev, map_a, map_b, map_h, p, ws, ctl, s);
+    case 3: return launch_cfg<LsTwoGroups6>(2, dev, map_a, map_b, map_h, p, ws, ctl, s);
+    case 4: return launch_cfg<LsOneGroup6>(3, dev, map_a, map_b, map_h, p, ws, ctl, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace ssm

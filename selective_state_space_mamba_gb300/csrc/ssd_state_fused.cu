@@ -47,9 +47,9 @@ constexpr int kSfStateThreads = 256; // warps 7-14: two threads per state row
 constexpr int kSfScaler0 = 96;       // first scaler thread (warps 0-2: X producer, MMA, B producer)
 constexpr int kSfThreads = kSfScaler0 + kSfScalers + kSfStateThreads;
 constexpr int kSfKH = 64;         // tokens per step
-constexpr int kSfXS = 4;          // X slots (one chunk of 256 tokens in flight)
-constexpr int kSfBS = 3;          // B slots (B comes from L2: shared by every head of a group)
-constexpr int kSfOS = 2;          // operand (hi + lo) slots
+// Ring depths: X slots and B slots are template parameters (the plan picks the split: 4 + 3,
+// 3 + 4 or 5 + 2; B comes from L2, shared by every head of a group); operand (hi + lo) slots:
+constexpr int kSfOS = 2;
 constexpr int kSfRowBytes = 128;  // 64 bf16 per swizzled row
 constexpr uint32_t kSfScaleBar = 1, kSfStateBar = 2;
 constexpr uint32_t kSfTmemCols = 512;  // h at 0, S[0] at 128, S[1] at 256
@@ -124,9 +124,9 @@ __host__ __device__ __forceinline__ SfSeg sf_seg(const SfRange& r, int s, int64_
 }
 
 // Shared memory (offsets from a 1024-byte aligned base), three rings:
-//   X[kSfXS]   X of the pair's two heads for one step: [2 heads][64 rows][128 B], swizzled;
+//   X[XS]      X of the pair's two heads for one step: [2 heads][64 rows][128 B], swizzled;
 //              released as soon as the scalers hold it in registers
-//   B[kSfBS]   the step's rows of the group's B: [2 s blocks][64 rows][128 B], swizzled;
+//   B[BS]      the step's rows of the group's B: [2 s blocks][64 rows][128 B], swizzled;
 //              released when the step's MMAs complete
 //   Op[kSfOS]  the weighted X of one step as bf16 hi and lo halves, each laid out like X;
 //              written by the scalers, released when the step's MMAs complete
@@ -134,27 +134,22 @@ __host__ __device__ __forceinline__ SfSeg sf_seg(const SfRange& r, int s, int64_
 //              warps write it here and one TMA store per s block takes it to memory, so
 //              that their 256-byte rows do not reach the load/store unit as scattered
 //              16-byte stores (these held up the scalers' shared-memory accesses)
-//   gd[kSfXS][2 heads]  G, dt and the chunk's last G of the step (travels with X)
+//   gd[XS][2 heads]  G, dt and the chunk's last G of the step (travels with X)
 //   barriers, TMEM base, abort flag
+template <int XS, int BS>
 struct SfLayout {
   uint32_t x_bytes, b0, op0, op_bytes, hs0, gd0, bars, total;
   __host__ __device__ SfLayout() {
     x_bytes = 2u * kSfKH * kSfRowBytes;  // 16 KB
-    b0 = kSfXS * x_bytes;
-    op0 = b0 + kSfBS * x_bytes;
+    b0 = XS * x_bytes;
+    op0 = b0 + BS * x_bytes;
     op_bytes = 2u * x_bytes;
     hs0 = op0 + kSfOS * op_bytes;
     gd0 = hs0 + 2u * 128 * kSfRowBytes;
-    bars = gd0 + kSfXS * 2u * kSfGdHead;
+    bars = gd0 + XS * 2u * kSfGdHead;
     total = bars + 32 * 8 + 16;
   }
 };
-enum SfBar {
-  kXFull = 0, kXEmpty = kXFull + kSfXS, kBFull = kXEmpty + kSfXS, kBEmpty = kBFull + kSfBS,
-  kOpFull = kBEmpty + kSfBS, kOpEmpty = kOpFull + kSfOS, kSReady = kOpEmpty + kSfOS, kSFree = kSReady + 2,
-  kDone = kSFree + 2, kSfNumBars = kDone + 1
-};
-static_assert(kSfNumBars <= 32, "barrier area");
 
 // d = a * b + c on bf16 pairs, one rounding
 __device__ __forceinline__ uint32_t sf_fma_bf16x2(uint32_t a, uint32_t b, uint32_t c) {
@@ -171,15 +166,22 @@ __device__ __forceinline__ uint32_t sf_pack(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+template <int XS, int BS>
 __global__ void __launch_bounds__(kSfThreads, 1)
     ssd_state_fused_tc_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_b,
                               const __grid_constant__ CUtensorMap map_hin, SfParams p, LookbackCtl ctl_call) {
+  constexpr int kSfXS = XS, kSfBS = BS;
+  // mbarriers: X full / empty, B full / empty, operand full / empty, S ready / free, done
+  constexpr int kXFull = 0, kXEmpty = kXFull + kSfXS, kBFull = kXEmpty + kSfXS, kBEmpty = kBFull + kSfBS;
+  constexpr int kOpFull = kBEmpty + kSfBS, kOpEmpty = kOpFull + kSfOS, kSReady = kOpEmpty + kSfOS;
+  constexpr int kSFree = kSReady + 2, kDone = kSFree + 2, kSfNumBars = kDone + 1;
+  static_assert(kSfNumBars <= 32, "barrier area");
   extern __shared__ unsigned char sf_raw[];
   griddep_launch_dependents();
   const uint32_t raw = smem_addr(sf_raw);
   unsigned char* base = sf_raw + ((1024u - (raw & 1023u)) & 1023u);
   const int T = p.chunk;
-  const SfLayout L;
+  const SfLayout<XS, BS> L;
   const int nk = T / kSfKH;  // steps per chunk
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.bars + 32 * 8);
@@ -637,10 +639,6 @@ cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float*
   p.nheads = d.nheads;
   p.ngroups = d.ngroups;
   p.chunk = d.chunk;
-  const SfLayout L;
-  const size_t smem = L.total + 1024;
-  if ((e = ensure_smem_limit(reinterpret_cast<const void*>(ssd_state_fused_tc_kernel), smem)) != cudaSuccess)
-    return e;
   const int64_t chains = d.batch * (int64_t)(d.nheads / 2);
   p.units = chains * d.nchunks;
   int dev = 0, sms = 148;
@@ -651,8 +649,18 @@ cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float*
   // a CTA can wait for the state its predecessor publishes
   const int64_t grid = sf_grid(chains, d.nchunks, sms);
   if (grid > chains || ws.sp_tiles < chains) return cudaErrorInvalidValue;
-  return launch_pdl(ssd_state_fused_tc_kernel, dim3((unsigned)grid), dim3(kSfThreads), smem, s, map_x, map_b, map_hin,
-                    p, ctl);
+  // the plan's ring split (X slots + B slots); the rule is 4 + 3
+  auto go = [&](auto kernel, size_t total) -> cudaError_t {
+    const size_t smem = total + 1024;
+    cudaError_t e2 = ensure_smem_limit(reinterpret_cast<const void*>(kernel), smem);
+    if (e2 != cudaSuccess) return e2;
+    return launch_pdl(kernel, dim3((unsigned)grid), dim3(kSfThreads), smem, s, map_x, map_b, map_hin, p, ctl);
+  };
+  switch (d.plan_ring) {
+    case 2: return go(ssd_state_fused_tc_kernel<3, 4>, SfLayout<3, 4>().total);
+    case 3: return go(ssd_state_fused_tc_kernel<5, 2>, SfLayout<5, 2>().total);
+    default: return go(ssd_state_fused_tc_kernel<4, 3>, SfLayout<4, 3>().total);
+  }
 }
 
 }  // namespace ssm

@@ -337,6 +337,7 @@ struct SsdDims {
   int plan_fused;        // 1: chunk states and state passing in one kernel, 0: two kernels
   int plan_seq;          // 1: sequential state passing, 0: look-back state passing
   int plan_scan_heads;   // chunk scan: heads per CTA (0: cost model)
+  int plan_ring;         // fused state pass: 1 = 4 X + 3 B slots, 2 = 3 + 4, 3 = 5 + 2 (0: rule, 4 + 3)
   int64_t debug_shrink;  // debug builds: bound shortfall of the cumsum store check (test hook)
 };
 
@@ -389,8 +390,10 @@ LinscanWorkspace linscan_workspace_layout(int64_t n, void* base);
 cudaError_t ensure_smem_limit(const void* func, size_t bytes);
 
 // Launchers (return a CUDA error code; 0 = success).
+// shape: the CTA shape (ssm_linscan_fwd_tune in ssm.h: 1 .. 4), 0 for the rule by row length
 cudaError_t launch_linscan(const float* a, const float* b, float* h, int64_t rows, int64_t len,
-                           const LinscanWorkspace& ws, const LookbackCtl& ctl, cudaStream_t s);
+                           const LinscanWorkspace& ws, const LookbackCtl& ctl, cudaStream_t s, int shape = 0);
+constexpr int kLsShapes = 4;
 cudaError_t launch_ssd_chunk_cumsum(const void* dt, const float* A, const SsdDims& d,
                                     const SsdWorkspace& ws, cudaStream_t s);
 cudaError_t launch_ssd_chunk_state(const void* x, const void* B, const SsdDims& d,

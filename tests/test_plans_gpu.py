@@ -36,6 +36,7 @@ def test_every_plan_is_correct(cuda_lib, dtype, hpg):
     plans = [ssm.plan_id(0, 1, 0), ssm.plan_id(0, 0, 0)]
     if dtype == "bf16":
         plans += [ssm.plan_id(1, -1, 0)] + [ssm.plan_id(f, 1 - f, h) for f in (0, 1) for h in (1, 2, hpg)]
+        plans += [ssm.plan_id(1, -1, h, ring) for ring in (1, 2, 3) for h in (0, 1)]  # the fused pass's ring splits
     try:
         for plan in plans:
             ssm.set_ssd_fwd_plan(d["x"], d["B"], shape.chunk, plan)
@@ -78,6 +79,48 @@ def test_invalid_plan_rejected(cuda_lib):
     with pytest.raises(ssm.SsmError) as e:
         ssm.set_ssd_fwd_plan(x, B, 256, 3)   # fused field 3 is not a choice
     assert e.value.status == _lib.SSM_ERR_INVALID_ARG
+    with pytest.raises(ssm.SsmError) as e:
+        ssm.set_ssd_fwd_plan(x, B, 256, 4 << 20)  # ring field 4 is not a choice
+    assert e.value.status == _lib.SSM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("rows,length", [(3, 1), (5, 4095), (4, 4097), (384, 1000), (2, 65537), (384, 65536)])
+def test_every_scan_shape_is_correct(cuda_lib, rows, length):
+    """Each CTA shape of the scan (consumer groups x ring depth x CTAs per SM) against the oracle."""
+    import selective_state_space_mamba_gb300 as ssm
+    from oracle import native
+    inp = synth.scan_inputs(rows, length, seed=rows * 7 + length)
+    a, b = P.to_dev(inp["a"]), P.to_dev(inp["b"])
+    ref = native.linscan(inp["a"], inp["b"])
+    try:
+        for shape in (1, 2, 3, 4):
+            ssm.set_linscan_shape(rows, length, shape)
+            assert ssm.get_linscan_shape(rows, length) == shape
+            h = ssm.linscan_fwd(a, b)
+            assert ssm.check_device_status(kind="linscan") == 0
+            P.assert_rows_close(P.to_np(h), ref, f"scan shape {shape} {rows}x{length}")
+    finally:
+        ssm.clear_linscan_shapes()
+    assert ssm.get_linscan_shape(rows, length) == -1
+
+
+def test_scan_tune_stores_the_fastest_shape(cuda_lib):
+    import selective_state_space_mamba_gb300 as ssm
+    from selective_state_space_mamba_gb300 import _lib
+    from oracle import native
+    inp = synth.scan_inputs(96, 65536, seed=77)
+    a, b = P.to_dev(inp["a"]), P.to_dev(inp["b"])
+    try:
+        shape, ms = ssm.tune_linscan_fwd(a, b, reps=3)
+        assert 1 <= shape <= 4 and ms > 0
+        assert ssm.get_linscan_shape(96, 65536) == shape
+        h = ssm.linscan_fwd(a, b)
+        P.assert_rows_close(P.to_np(h), native.linscan(inp["a"], inp["b"]), f"tuned scan shape {shape}")
+        with pytest.raises(ssm.SsmError) as e:
+            ssm.set_linscan_shape(96, 65536, 5)
+        assert e.value.status == _lib.SSM_ERR_INVALID_ARG
+    finally:
+        ssm.clear_linscan_shapes()
 
 
 def _sm_count():
@@ -85,12 +128,14 @@ def _sm_count():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
-@pytest.mark.parametrize("extra_chains,seqlen,chunk,G,h0,final", [(8, 520, 64, 1, True, True), (1, 300, 64, 1, True, True),
-                                                                 (40, 1000, 128, 2, True, True),
-                                                                 (148, 200, 64, 4, True, True),
-                                                                 (8, 700, 128, 1, False, False),
-                                                                 (8, 200, 256, 1, True, True)])
-def test_fused_pass_with_more_chains_than_sms(cuda_lib, extra_chains, seqlen, chunk, G, h0, final):
+@pytest.mark.parametrize("extra_chains,seqlen,chunk,G,h0,final,ring", [(8, 520, 64, 1, True, True, 0),
+                                                                      (1, 300, 64, 1, True, True, 2),
+                                                                      (40, 1000, 128, 2, True, True, 0),
+                                                                      (148, 200, 64, 4, True, True, 3),
+                                                                      (8, 700, 128, 1, False, False, 0),
+                                                                      (8, 200, 256, 1, True, True, 2),
+                                                                      (40, 1000, 256, 1, True, True, 3)])
+def test_fused_pass_with_more_chains_than_sms(cuda_lib, extra_chains, seqlen, chunk, G, h0, final, ring):
     """The fused state pass with more (batch, head pair) chains than SMs: one CTA per SM runs an
     equal range of chunks, so chains are split between CTAs and the CTA that runs a chain's
     tail starts from the state its predecessor publishes (with one chunk per chain the ranges
@@ -110,7 +155,7 @@ def test_fused_pass_with_more_chains_than_sms(cuda_lib, extra_chains, seqlen, ch
     y_ref, hf_ref = native.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
                                    inp["h0"] if h0 else None, units=units)
     try:
-        ssm.set_ssd_fwd_plan(d["x"], d["B"], chunk, ssm.plan_id(1, -1, 0))
+        ssm.set_ssd_fwd_plan(d["x"], d["B"], chunk, ssm.plan_id(1, -1, 0, ring))
         first = None
         for rep in range(2):
             y, hf = ssm.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"] if h0 else None,

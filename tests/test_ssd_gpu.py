@@ -114,8 +114,8 @@ def test_headline_workload_every_plan_every_unit(cuda_lib):
     shape = synth.SSD_B4_L8192
     inp = synth.ssd_inputs(shape)
     x_dev, b_dev = P.to_dev(inp["x"], shape.dtype), P.to_dev(inp["B"], shape.dtype)
-    plans = [ssm.plan_id(1, -1, 0), ssm.plan_id(1, -1, 16), ssm.plan_id(0, 1, 0), ssm.plan_id(0, 0, 0),
-             ssm.plan_id(0, 1, 40)]
+    plans = [ssm.plan_id(1, -1, 0), ssm.plan_id(1, -1, 16, 2), ssm.plan_id(1, -1, 0, 3), ssm.plan_id(0, 1, 0),
+             ssm.plan_id(0, 0, 0), ssm.plan_id(0, 1, 40)]
     outs = {}
     try:
         for plan in plans:
