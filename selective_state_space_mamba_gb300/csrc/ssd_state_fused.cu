@@ -186,13 +186,11 @@ __global__ void __launch_bounds__(kSfThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + L.bars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L.bars + 32 * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L.bars + 32 * 8 + 4);
+  volatile uint32_t* claim_slot = reinterpret_cast<volatile uint32_t*>(base + L.bars + 32 * 8 + 8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hpg = p.nheads / p.ngroups, ppg = hpg / 2;
   const int64_t nc = p.nchunks;
-  const int64_t u0 = (int64_t)blockIdx.x * p.units / gridDim.x;
-  const int64_t u1 = (int64_t)(blockIdx.x + 1) * p.units / gridDim.x;
-  const SfRange rg = nc > 0 && u1 > u0 ? sf_range(u0, u1, nc) : SfRange{0, 0, 0, 0, 0, 0, 0, false, false};
   // chain -> (batch, group, first head of the pair)
   auto chain_bi = [&](int64_t z) { return z / ((int64_t)ppg * p.ngroups); };
   auto chain_g = [&](int64_t z) { return (int)((z / ppg) % p.ngroups); };
@@ -214,7 +212,16 @@ __global__ void __launch_bounds__(kSfThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  griddep_wait();  // G and dt come from the previous kernel
+  griddep_wait();  // G and dt come from the previous kernel (which also zeroed the claim counter)
+  // The CTA's range index is claimed in order from the workspace counter, not taken from
+  // blockIdx: the CTA it may wait for (range index - 1) has then claimed first, so it is
+  // running, and its first segment waits for nobody.  No CTA needs another to be resident.
+  if (threadIdx.x == 0) *claim_slot = atomicAdd(&p.hdr->counter, 1u);
+  __syncthreads();
+  const int64_t vb = *claim_slot;
+  const int64_t u0 = vb * p.units / gridDim.x;
+  const int64_t u1 = (vb + 1) * p.units / gridDim.x;
+  const SfRange rg = nc > 0 && u1 > u0 ? sf_range(u0, u1, nc) : SfRange{0, 0, 0, 0, 0, 0, 0, false, false};
   // published states carry this launch's epoch (the last CTA to finish moves it on)
   const LookbackCtl ctl = device_epoch(ctl_call, p.hdr);
   auto fail = [&](void) {
@@ -527,7 +534,7 @@ __global__ void __launch_bounds__(kSfThreads, 1)
     }
     if (leader) bulk_wait<0>();  // every h_in store has completed
     if (nc == 0 && p.h_final) {  // no chunks: the final state is the initial one (one chain per CTA)
-      const int64_t bh = chain_bi(blockIdx.x) * p.nheads + chain_h(blockIdx.x) + hh;
+      const int64_t bh = chain_bi(vb) * p.nheads + chain_h(vb) + hh;
       const float* h0r = p.h0 ? p.h0 + (bh * 64 + pp) * 128 + col0 : nullptr;
       float4* f = reinterpret_cast<float4*>(p.h_final + (bh * 64 + pp) * 128 + col0);
 #pragma unroll 4

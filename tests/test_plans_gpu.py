@@ -177,3 +177,33 @@ def test_fused_pass_with_more_chains_than_sms(cuda_lib, extra_chains, seqlen, ch
                 assert np.array_equal(first[0], y) and (not final or np.array_equal(first[1], hf))
     finally:
         ssm.clear_ssd_fwd_plans()
+
+
+def test_fused_pass_shares_the_gpu(cuda_lib):
+    """The fused state pass while bf16 matmuls on another stream hold SMs.  Its CTAs take their
+    ranges in claim order, not by block index, so a CTA that waits for the state its
+    predecessor publishes waits for a CTA that is already running, whichever SMs are free when
+    the CTAs start.  The result is bit-identical to the same call on an idle GPU."""
+    import torch
+    import selective_state_space_mamba_gb300 as ssm
+    chains = _sm_count() + 40
+    shape = synth.SSDShape("fused_shared", 1, 1000, 2 * chains, 64, 128, 1, 128, "bf16", h0=True)
+    inp = synth.ssd_inputs(shape, seed=77)
+    d = dev_inputs(inp, "bf16")
+    try:
+        ssm.set_ssd_fwd_plan(d["x"], d["B"], shape.chunk, ssm.plan_id(1, -1, 0))
+        y0, hf0 = run(ssm, d, shape.chunk)
+        a = torch.randn(8192, 8192, device="cuda", dtype=torch.bfloat16) / 64
+        busy, mine = torch.cuda.Stream(), torch.cuda.Stream()
+        torch.cuda.synchronize()
+        for rep in range(3):
+            with torch.cuda.stream(busy):
+                prods = [a @ a for _ in range(4)]
+            with torch.cuda.stream(mine):
+                y, hf = ssm.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], chunk=shape.chunk)
+            torch.cuda.synchronize()
+            del prods
+            assert ssm.check_device_status(kind="ssd") == 0
+            assert np.array_equal(P.to_np(y), y0) and np.array_equal(P.to_np(hf), hf0), f"call {rep}"
+    finally:
+        ssm.clear_ssd_fwd_plans()
