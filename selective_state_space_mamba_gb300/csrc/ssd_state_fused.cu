@@ -66,6 +66,7 @@ struct SfParams {
   WsHeader* hdr;
   int64_t batch, lpad, nchunks, units;  // units = chains x nchunks
   int nheads, ngroups, chunk;
+  int b_keep;  // B is small next to L2: load it with evict-last priority
 };
 
 // This CTA's units [u0, u1) of (chain, chunk), chain-major, as segments in the order they run:
@@ -250,8 +251,10 @@ __global__ void __launch_bounds__(kSfThreads, 1)
             unsigned char* xst = base + xs * L.x_bytes;
             unsigned char* gd = base + L.gd0 + xs * 2 * kSfGdHead;
             mbar_arrive_expect_tx(&bars[kXFull + xs], L.x_bytes + 2u * kSfGdHead);
+            // x is read once: evict-first, so that its stream does not push B out of L2
             for (int hh = 0; hh < 2; ++hh)
-              tc::tma_load_3d(xst + hh * kSfKH * kSfRowBytes, &map_x, (h + hh) * 64, tok, (int)bi, &bars[kXFull + xs]);
+              tc::tma_load_3d_hint(xst + hh * kSfKH * kSfRowBytes, &map_x, (h + hh) * 64, tok, (int)bi, &bars[kXFull + xs],
+                                   l2_evict_first_policy());
             for (int hh = 0; hh < 2; ++hh) {
               const int64_t row = (bi * p.nheads + h + hh) * p.lpad + c * T;
               // G and dt^T are [b, nh, lpad]: the chunk's T entries of this head
@@ -290,9 +293,16 @@ __global__ void __launch_bounds__(kSfThreads, 1)
             }
             unsigned char* bst = base + L.b0 + bs * L.x_bytes;
             mbar_arrive_expect_tx(&bars[kBFull + bs], L.x_bytes);
-            for (int sb = 0; sb < 2; ++sb)
-              tc::tma_load_3d(bst + sb * kSfKH * kSfRowBytes, &map_b, g * 128 + sb * 64, (int)(c * T + kh * kSfKH),
-                              (int)bi, &bars[kBFull + bs]);
+            // B is read by every head pair of its group: where all of it fits well inside L2
+            // (8 MB at b4 L8192), evict-last keeps it there against the x stream
+            for (int sb = 0; sb < 2; ++sb) {
+              if (p.b_keep)
+                tc::tma_load_3d_hint(bst + sb * kSfKH * kSfRowBytes, &map_b, g * 128 + sb * 64, (int)(c * T + kh * kSfKH),
+                                     (int)bi, &bars[kBFull + bs], l2_evict_last_policy());
+              else
+                tc::tma_load_3d(bst + sb * kSfKH * kSfRowBytes, &map_b, g * 128 + sb * 64, (int)(c * T + kh * kSfKH),
+                                (int)bi, &bars[kBFull + bs]);
+            }
             ++nb;
           }
         }
@@ -646,14 +656,17 @@ cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float*
   p.nheads = d.nheads;
   p.ngroups = d.ngroups;
   p.chunk = d.chunk;
+  // B's lines keep evict-last priority after the pass (until read again with another policy),
+  // so the hint is given only where all of B takes at most a quarter of L2
+  p.b_keep = (uint64_t)d.batch * (uint64_t)d.seqlen * (uint64_t)d.ngroups * 128u * 2u <= (32ull << 20);
   const int64_t chains = d.batch * (int64_t)(d.nheads / 2);
   p.units = chains * d.nchunks;
   int dev = 0, sms = 148;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   // one chain per CTA, or one CTA per SM with ranges of at least one chain (chains > SMs), so
-  // that a range never lies inside one chain; every CTA is resident at once (one per SM), so
-  // a CTA can wait for the state its predecessor publishes
+  // that a range never lies inside one chain; the CTAs claim their ranges in order, so the CTA
+  // whose published state a range waits for is already running
   const int64_t grid = sf_grid(chains, d.nchunks, sms);
   if (grid > chains || ws.sp_tiles < chains) return cudaErrorInvalidValue;
   // the plan's ring split (X slots + B slots); the rule is 4 + 3
