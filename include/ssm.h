@@ -138,15 +138,18 @@ SSM_API ssm_status ssm_ssd_fwd(const void *x, const void *dt, const float *A, co
  *     state-passing, the latter sequential over chunks or a decoupled look-back.  With more
  *     (batch, head pair) chains than SMs the one-kernel pass runs one CTA per SM on equal
  *     ranges of chunks, and a CTA that starts inside a chain waits (bounded) for the state its
- *     predecessor publishes; it relies on all of its CTAs being resident at once, so where
- *     other work holds SMs for longer than the wait limit the call reports SSM_ERR_TIMEOUT;
+ *     predecessor publishes; the CTAs claim their ranges in order, so that predecessor is
+ *     always already running and the pass needs no co-residency of its CTAs;
  *   - the one-kernel pass's shared-memory ring split: X slots (loaded from DRAM) and B slots
  *     (loaded from L2) share a fixed budget: 4 + 3, 3 + 4 or 5 + 2;
  *   - the chunk scan's run of heads per CTA (the tensor-core path).
  * Without a plan, ssm_ssd_fwd picks by fixed rules of thumb.  A plan id packs
  * (fused + 1) | (sequential + 1) << 2 | heads_per_cta << 4 | ring << 20, where fused and
- * sequential are 1 (yes), 0 (no) or -1 (rule of thumb), heads_per_cta (0 .. 65535) 0 means the
- * rule of thumb, and ring is 1 (4 + 3), 2 (3 + 4), 3 (5 + 2) or 0 (the rule: 4 + 3).
+ * sequential are 1 (yes), 0 (no) or -1 (rule of thumb), heads_per_cta (0 .. 65535) n > 0 gives
+ * every chunk-scan CTA a run of at most n heads (a tile's heads split evenly) and 0 means the
+ * split a model of the hardware's CTA dispatch finds fastest (large runs first, small runs
+ * last; ssm_debug_scan_schedule shows it), and ring is 1 (4 + 3), 2 (3 + 4), 3 (5 + 2) or 0
+ * (the rule: 4 + 3).
  *
  * ssm_ssd_fwd_tune takes exactly ssm_ssd_fwd's arguments and runs every candidate plan for
  * these sizes on the caller's buffers (y and h_final are overwritten; each candidate computes
@@ -351,6 +354,18 @@ SSM_API ssm_status ssm_debug_set_bounds_fault(int64_t shrink);
  * returns the number of segments, or -1 for a negative size or sms < 1.
  */
 SSM_API int64_t ssm_debug_fused_schedule(int64_t chains, int64_t nchunks, int sms, int64_t *rows, int64_t cap);
+
+/*
+ * Test hook for the chunk scan's work split (host only; no GPU call).  The chunk scan's CTAs
+ * take its `tiles` tiles ((batch, chunk, group, row tile), row tile fastest; `row_tiles` = 1 for
+ * chunk 128, 2 for chunk 256) in order, in three tiers: tier k covers the next out[2k] tiles with
+ * out[2k+1] CTAs per tile, the tile's `heads_per_group` heads split evenly between those CTAs.
+ * `plan_heads` is the plan's heads per CTA (0: the split a model of the hardware's CTA dispatch
+ * on `sms` SMs finds fastest, large runs of heads first and small ones last).  Writes six
+ * int64 to `out` (which may be NULL) and returns the number of CTAs, or -1 for invalid sizes.
+ */
+SSM_API int64_t ssm_debug_scan_schedule(int64_t tiles, int row_tiles, int heads_per_group, int sms, int plan_heads,
+                                        int64_t *out);
 
 /*
  * Kernel timing (measurement aid; not needed in normal use).  Between ssm_profile_begin()

@@ -23,6 +23,7 @@ EXPORTS = ("ssm_status_string", "ssm_version", "ssm_ssd_fwd_workspace_bytes", "s
            "ssm_debug_set_lookback_fault", "ssm_profile_begin", "ssm_profile_end", "ssm_linscan_fwd_noalloc",
            "ssm_ssd_step", "ssm_linscan_baseline_workspace_bytes", "ssm_linscan_baseline", "ssm_ssd_fwd_tune",
            "ssm_ssd_fwd_set_plan", "ssm_ssd_fwd_get_plan", "ssm_ssd_fwd_clear_plans", "ssm_debug_fused_schedule",
+           "ssm_debug_scan_schedule",
            "ssm_debug_build", "ssm_debug_set_bounds_fault", "ssm_linscan_fwd_tune", "ssm_linscan_set_shape",
            "ssm_linscan_get_shape", "ssm_linscan_clear_shapes")
 PROFILE_KERNELS = ("linscan_lookback", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
@@ -52,6 +53,8 @@ def _declare(lib):
     lib.ssm_ssd_fwd_tune.restype = i32
     lib.ssm_debug_fused_schedule.argtypes = [i64, i64, i32, vp, i64]
     lib.ssm_debug_fused_schedule.restype = i64
+    lib.ssm_debug_scan_schedule.argtypes = [i64, i32, i32, i32, i32, vp]
+    lib.ssm_debug_scan_schedule.restype = i64
     lib.ssm_ssd_fwd_set_plan.argtypes = [i64, i64, i32, i32, i32, i32, i32, i32, i32]
     lib.ssm_ssd_fwd_set_plan.restype = i32
     lib.ssm_ssd_fwd_get_plan.argtypes = [i64, i64, i32, i32, i32, i32, i32, i32, vp]

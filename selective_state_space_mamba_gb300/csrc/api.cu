@@ -775,4 +775,21 @@ int64_t ssm_debug_fused_schedule(int64_t chains, int64_t nchunks, int sms, int64
   return ssd_fused_schedule(chains, nchunks, sms, rows, cap < 0 ? 0 : cap);
 }
 
+int64_t ssm_debug_scan_schedule(int64_t tiles, int row_tiles, int heads_per_group, int sms, int plan_heads,
+                                int64_t* out) {
+  if (tiles < 0 || (row_tiles != 1 && row_tiles != 2) || tiles % row_tiles || heads_per_group < 1 || sms < 1 ||
+      plan_heads < 0)
+    return -1;
+  const ScTiers s = sc_schedule(tiles, row_tiles, heads_per_group, sms, plan_heads);
+  int64_t grid = 0;
+  for (int k = 0; k < 3; ++k) {
+    if (out) {
+      out[2 * k] = s.tiles[k];
+      out[2 * k + 1] = s.items[k];
+    }
+    grid += s.tiles[k] * s.items[k];
+  }
+  return grid;
+}
+
 }  // extern "C"

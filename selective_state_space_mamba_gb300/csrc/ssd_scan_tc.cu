@@ -3,7 +3,11 @@
 //     Y = 2^G (C h_in^T) + ((C B^T) . 2^(G_i - G_j) dt_j . [i >= j]) X + D X,
 // on the 5th-generation tensor cores for bf16 inputs (f32 accumulation).
 //
-// CTA = (batch, chunk, 128-row tile of the chunk starting at row i0, group, run of heads).
+// CTA = (batch, chunk, 128-row tile of the chunk starting at row i0, group, run of heads).  The
+// CTAs take the tiles in order (the two row tiles of a chunk adjacent, so that they run at the
+// same time and share their x, h_in, G and dt reads in L2), in up to three tiers with a
+// different number of CTAs per tile each: large runs of heads first, small ones last, so that
+// the last wave of CTAs ends together (see ScTiers).
 // The tile's columns j split into the rectangle j < i0 and the triangle i0 <= j < i0 + 128.
 // In the rectangle every weight factors through the tile's first row:
 //     2^(G_i - G_j) dt_j = u_i f_j,   u_i = 2^(G_i - G_i0) <= 1,   f_j = dt_j 2^(G_i0 - G_j) <= dt_j,
@@ -35,6 +39,14 @@
 // Every wait is bounded.  A math-warp wait that gives up is voted on (bar.red.or) so that all
 // math warps leave together; the CTA then drains, frees its TMEM and returns.
 #include "tc_common.cuh"
+
+#include <algorithm>
+#include <functional>
+#include <map>
+#include <mutex>
+#include <queue>
+#include <tuple>
+#include <vector>
 
 #ifndef SSM_SCAN_Y_EVICT_FIRST  // y is written once: evict-first priority in L2
 #define SSM_SCAN_Y_EVICT_FIRST 1
@@ -74,7 +86,8 @@ struct ScParams {
   WsHeader* hdr;
   int64_t batch, lpad, nchunks;
   int nheads, ngroups, chunk, row_tiles;
-  int heads_per_item, items_per_tile;
+  int64_t tier_tiles[3];  // CTAs in order: tier s covers the next tier_tiles[s] tiles,
+  int tier_items[3];      // with tier_items[s] CTAs per tile (its heads split evenly)
 };
 
 // Shared memory (offsets from a 1024-byte aligned base), chunk size T:
@@ -151,10 +164,23 @@ __global__ void __launch_bounds__(kScThreads, 1)
 
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // work item -> (batch, chunk, group, row tile, run of heads)
-  int64_t item = blockIdx.x;
-  const int k_item = (int)(item % p.items_per_tile);
-  item /= p.items_per_tile;
+  // CTA -> tier -> (tile, run of heads) -> (batch, chunk, group, row tile)
+  int64_t item = 0;
+  int k_item = 0, n_items = 1;
+  {
+    int64_t cta = blockIdx.x, tile0 = 0;
+    for (int s = 0; s < 3; ++s) {
+      const int64_t n = p.tier_tiles[s] * p.tier_items[s];
+      if (cta < n || s == 2) {
+        item = tile0 + cta / p.tier_items[s];
+        k_item = (int)(cta % p.tier_items[s]);
+        n_items = p.tier_items[s];
+        break;
+      }
+      cta -= n;
+      tile0 += p.tier_tiles[s];
+    }
+  }
   const int R = (int)(item % p.row_tiles);
   item /= p.row_tiles;
   const int g = (int)(item % p.ngroups);
@@ -162,8 +188,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
   const int64_t c = item % p.nchunks;
   const int64_t bi = item / p.nchunks;
   const int hpg = p.nheads / p.ngroups;
-  const int h_first = g * hpg + k_item * p.heads_per_item;
-  const int nh_run = min(p.heads_per_item, hpg - k_item * p.heads_per_item);
+  const int h_first = g * hpg + (k_item * hpg) / n_items;
+  const int nh_run = ((k_item + 1) * hpg) / n_items - (k_item * hpg) / n_items;
   const int i0 = R * 128;   // first chunk row of the tile (0 or 128)
   const int Nj = i0 + 128;  // columns 0 .. Nj-1 can be at or below the diagonal
   const int tok0 = (int)(c * T);
@@ -588,6 +614,105 @@ bool ssd_scan_tc_supported(const SsdDims& d) {
   return d.dtype == SSM_BF16 && d.headdim == 64 && d.dstate == 128 && (d.chunk == 128 || d.chunk == 256);
 }
 
+// ---- the chunk scan's work split -------------------------------------------------------
+// The CTAs take the tiles (batch, chunk, group, row tile) in order, a tile's heads split evenly
+// between its CTAs.  With one CTA per SM the hardware hands each CTA, in index order, to the SM
+// that frees first, so the split decides how the last wave ends: tiers of large runs of heads
+// first and small ones last end it more evenly than one split for all tiles, and large runs
+// pay the per-CTA set-up (C and B rows, CB, the first stage, the drain) less often.
+
+// Greedy list scheduling over `sms` SMs, the model of that dispatch.  Costs in units of a head
+// of a first row tile: a head of a later row tile (which adds the rectangle) 1.25, a CTA's
+// set-up and drain 4.7 (per-role timings at b4 L8192 nh80: 1.18 us, 1.47 us and ~5.5 us).
+double sc_model_makespan(const ScTiers& s, int row_tiles, int hpg, int sms) {
+  std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+  for (int i = 0; i < sms; ++i) free_at.push(0.0);
+  double end = 0.0;
+  int64_t tile = 0;
+  for (int k = 0; k < 3; ++k)
+    for (int64_t tt = 0; tt < s.tiles[k]; ++tt, ++tile) {
+      const double per_head = (tile % row_tiles) ? 1.25 : 1.0;
+      for (int j = 0; j < s.items[k]; ++j) {
+        const int nh = ((j + 1) * hpg) / s.items[k] - (j * hpg) / s.items[k];
+        const double t0 = free_at.top();
+        free_at.pop();
+        free_at.push(t0 + nh * per_head + 4.7);
+        end = std::max(end, t0 + nh * per_head + 4.7);
+      }
+    }
+  return end;
+}
+
+ScTiers sc_uniform(int64_t tiles, int items) {
+  ScTiers s{};
+  s.tiles[0] = tiles;
+  s.items[0] = items;
+  s.items[1] = s.items[2] = 1;
+  return s;
+}
+
+// The split for `tiles` tiles of `hpg` heads.  plan_heads > 0 (a plan): runs of at most that
+// many heads, one tier.  0: the split the model finds fastest among one tier of 1..8 CTAs per
+// tile and three tiers around the best of those (the first f chunks with a CTAs per tile, the
+// last m with c, the rest with b; a <= b < c), kept only where the model gains 2 % (its error
+// is larger than that); computed once per shape and SM count.  Searched only up to 16 waves:
+// beyond, the last wave weighs little.
+ScTiers sc_schedule(int64_t tiles, int row_tiles, int hpg, int sms, int plan_heads) {
+  if (plan_heads > 0) {
+    const int run = plan_heads < hpg ? plan_heads : hpg;
+    return sc_uniform(tiles, (hpg + run - 1) / run);
+  }
+  static std::mutex mu;
+  static std::map<std::tuple<int64_t, int, int, int>, ScTiers> cache;
+  const auto key = std::make_tuple(tiles, row_tiles, hpg, sms);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  int b_best = 1;
+  double t_best = -1.0;
+  for (int b = 1; b <= std::min(hpg, 8); ++b) {
+    if (tiles * b > 16LL * sms && b > 1) break;
+    const double tm = sc_model_makespan(sc_uniform(tiles, b), row_tiles, hpg, sms);
+    if (t_best < 0 || tm < t_best) {
+      t_best = tm;
+      b_best = b;
+    }
+  }
+  ScTiers best = sc_uniform(tiles, b_best);
+  const int64_t chunks = tiles / row_tiles;  // tiles of one (batch, chunk, group), adjacent
+  if (tiles * b_best <= 16LL * sms && chunks >= 8) {
+    const double uniform_time = t_best;
+    for (int b = std::max(1, b_best - 1); b <= std::min(hpg, b_best + 1); ++b)
+      for (int a = std::max(1, b - 1); a <= b; ++a)
+        for (int cm : {2, 4}) {
+          const int c = std::min(hpg, cm * b);
+          if (c <= b) continue;
+          for (int fq : {0, 1, 2, 3, 4})      // first chunks: 0 .. 1/2 of them
+            for (int mq : {0, 1, 2, 4}) {     // last chunks: 0 .. 1/8 of them
+              const int64_t f = chunks * fq / 8, m = chunks * mq / 32;
+              if ((fq && !f) || (mq && !m) || f + m > chunks) continue;
+              ScTiers s{};
+              s.tiles[0] = f * row_tiles;
+              s.items[0] = a;
+              s.tiles[1] = (chunks - f - m) * row_tiles;
+              s.items[1] = b;
+              s.tiles[2] = m * row_tiles;
+              s.items[2] = c;
+              const double tm = sc_model_makespan(s, row_tiles, hpg, sms);
+              if (tm < t_best && tm < 0.98 * uniform_time) {
+                t_best = tm;
+                best = s;
+              }
+            }
+        }
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  cache[key] = best;
+  return best;
+}
+
 cudaError_t launch_ssd_chunk_scan_tc(const void* x, const void* B, const void* C, const float* D, void* y,
                                      const SsdDims& d, const SsdWorkspace& ws, const LookbackCtl& ctl,
                                      cudaStream_t s) {
@@ -630,32 +755,19 @@ cudaError_t launch_ssd_chunk_scan_tc(const void* x, const void* B, const void* C
   int dev = 0, sms = 148;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  // Split each (batch, chunk, group, row tile)'s heads into runs, one CTA per run and one CTA
-  // per SM at a time: choose the run length that minimises waves x (heads per run + the
-  // per-CTA set-up, about three heads' worth).
   const int64_t tiles = d.batch * d.nchunks * d.ngroups * p.row_tiles;
-  int64_t best_cost = -1;
-  if (d.plan_scan_heads > 0) {  // the plan fixes the run length
-    p.heads_per_item = d.plan_scan_heads < hpg ? d.plan_scan_heads : hpg;
-    p.items_per_tile = (hpg + p.heads_per_item - 1) / p.heads_per_item;
-    best_cost = 0;
+  const ScTiers tiers = sc_schedule(tiles, p.row_tiles, hpg, sms, d.plan_scan_heads);
+  int64_t grid = 0;
+  for (int k = 0; k < 3; ++k) {
+    p.tier_tiles[k] = tiers.tiles[k];
+    p.tier_items[k] = tiers.items[k];
+    grid += tiers.tiles[k] * tiers.items[k];
   }
-  for (int hpi = 1; hpi <= hpg && best_cost != 0; ++hpi) {
-    const int items = (hpg + hpi - 1) / hpi;
-    if (hpi > 1 && (hpg + hpi - 2) / (hpi - 1) == items) continue;  // same split, shorter runs
-    const int64_t waves = (tiles * items + sms - 1) / sms;
-    const int64_t cost = waves * (hpi + 3);
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      p.heads_per_item = hpi;
-      p.items_per_tile = items;
-    }
-  }
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const ScLayout L(d.chunk);
   const size_t smem = L.total + 1024;
   if ((e = ensure_smem_limit(reinterpret_cast<const void*>(ssd_chunk_scan_tc_kernel), smem)) != cudaSuccess)
     return e;
-  const int64_t grid = tiles * p.items_per_tile;
   return launch_pdl(ssd_chunk_scan_tc_kernel, dim3((unsigned)grid), dim3(kScThreads), smem, s, map_c, map_b, map_x,
                     map_hin, map_y, p, ctl);
 }

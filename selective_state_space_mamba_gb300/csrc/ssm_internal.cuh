@@ -401,6 +401,15 @@ cudaError_t ensure_smem_limit(const void* func, size_t bytes);
 cudaError_t launch_linscan(const float* a, const float* b, float* h, int64_t rows, int64_t len,
                            const LinscanWorkspace& ws, const LookbackCtl& ctl, cudaStream_t s, int shape = 0);
 constexpr int kLsShapes = 4;
+// The chunk scan's CTA split: tier s covers the next tiles[s] tiles (batch, chunk, group, row
+// tile; in that order, row tile fastest) with items[s] CTAs per tile, a tile's heads split
+// evenly between them.  plan_heads > 0 fixes runs of at most that many heads (one tier).
+struct ScTiers {
+  int64_t tiles[3];
+  int items[3];
+};
+ScTiers sc_schedule(int64_t tiles, int row_tiles, int hpg, int sms, int plan_heads);
+
 cudaError_t launch_ssd_chunk_cumsum(const void* dt, const float* A, const SsdDims& d,
                                     const SsdWorkspace& ws, cudaStream_t s);
 cudaError_t launch_ssd_chunk_state(const void* x, const void* B, const SsdDims& d,
