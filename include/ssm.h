@@ -357,8 +357,8 @@ SSM_API int64_t ssm_debug_fused_schedule(int64_t chains, int64_t nchunks, int sm
 
 /*
  * Test hook for the chunk scan's work split (host only; no GPU call).  The chunk scan's CTAs
- * take its `tiles` tiles ((batch, chunk, group, row tile), row tile fastest; `row_tiles` = 1 for
- * chunk 128, 2 for chunk 256) in order, in three tiers: tier k covers the next out[2k] tiles with
+ * take its `tiles` tiles ((batch, chunk, group, row tile), row tile fastest and the later row tile
+ * first; `row_tiles` = 1 for chunk 128, 2 for chunk 256) in order, in three tiers: tier k covers the next out[2k] tiles with
  * out[2k+1] CTAs per tile, the tile's `heads_per_group` heads split evenly between those CTAs.
  * `plan_heads` is the plan's heads per CTA (0: the split a model of the hardware's CTA dispatch
  * on `sms` SMs finds fastest, large runs of heads first and small ones last).  Writes six

@@ -4,10 +4,10 @@
 // on the 5th-generation tensor cores for bf16 inputs (f32 accumulation).
 //
 // CTA = (batch, chunk, 128-row tile of the chunk starting at row i0, group, run of heads).  The
-// CTAs take the tiles in order (the two row tiles of a chunk adjacent, so that they run at the
-// same time and share their x, h_in, G and dt reads in L2), in up to three tiers with a
-// different number of CTAs per tile each: large runs of heads first, small ones last, so that
-// the last wave of CTAs ends together (see ScTiers).
+// CTAs take the tiles in order (the two row tiles of a chunk adjacent, the later one first, so
+// that they run at the same time and share their x, h_in, G and dt reads in L2), in up to three
+// tiers with a different number of CTAs per tile each: large runs of heads first, small ones
+// last, so that the last wave of CTAs ends together (see ScTiers).
 // The tile's columns j split into the rectangle j < i0 and the triangle i0 <= j < i0 + 128.
 // In the rectangle every weight factors through the tile's first row:
 //     2^(G_i - G_j) dt_j = u_i f_j,   u_i = 2^(G_i - G_i0) <= 1,   f_j = dt_j 2^(G_i0 - G_j) <= dt_j,
@@ -181,7 +181,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
       tile0 += p.tier_tiles[s];
     }
   }
-  const int R = (int)(item % p.row_tiles);
+  // of a chunk's two row tiles the later one (with the rectangle, the longer CTA) comes first
+  const int R = p.row_tiles - 1 - (int)(item % p.row_tiles);
   item /= p.row_tiles;
   const int g = (int)(item % p.ngroups);
   item /= p.ngroups;
@@ -631,7 +632,7 @@ double sc_model_makespan(const ScTiers& s, int row_tiles, int hpg, int sms) {
   int64_t tile = 0;
   for (int k = 0; k < 3; ++k)
     for (int64_t tt = 0; tt < s.tiles[k]; ++tt, ++tile) {
-      const double per_head = (tile % row_tiles) ? 1.25 : 1.0;
+      const double per_head = (row_tiles == 2 && tile % 2 == 0) ? 1.25 : 1.0;  // the later row tile first
       for (int j = 0; j < s.items[k]; ++j) {
         const int nh = ((j + 1) * hpg) / s.items[k] - (j * hpg) / s.items[k];
         const double t0 = free_at.top();
@@ -670,10 +671,14 @@ ScTiers sc_schedule(int64_t tiles, int row_tiles, int hpg, int sms, int plan_hea
     const auto it = cache.find(key);
     if (it != cache.end()) return it->second;
   }
-  int b_best = 1;
+  // Runs of at most 40 heads: the later row tile takes ~25 % longer per head, so over a longer
+  // run the two row tiles of a chunk drift apart by more than their shared lines stay in L2
+  // (measured at b4 L8192 nh80: runs of 80 heads first cost 1-15 us against runs of 40).
+  const int min_items = (hpg + 39) / 40;
+  int b_best = min_items;
   double t_best = -1.0;
-  for (int b = 1; b <= std::min(hpg, 8); ++b) {
-    if (tiles * b > 16LL * sms && b > 1) break;
+  for (int b = min_items; b <= std::max(min_items, std::min(hpg, 8)); ++b) {
+    if (tiles * b > 16LL * sms && b > min_items) break;
     const double tm = sc_model_makespan(sc_uniform(tiles, b), row_tiles, hpg, sms);
     if (t_best < 0 || tm < t_best) {
       t_best = tm;
@@ -684,8 +689,8 @@ ScTiers sc_schedule(int64_t tiles, int row_tiles, int hpg, int sms, int plan_hea
   const int64_t chunks = tiles / row_tiles;  // tiles of one (batch, chunk, group), adjacent
   if (tiles * b_best <= 16LL * sms && chunks >= 8) {
     const double uniform_time = t_best;
-    for (int b = std::max(1, b_best - 1); b <= std::min(hpg, b_best + 1); ++b)
-      for (int a = std::max(1, b - 1); a <= b; ++a)
+    for (int b = std::max(min_items, b_best - 1); b <= std::min(hpg, b_best + 1); ++b)
+      for (int a = std::max(min_items, b - 1); a <= b; ++a)
         for (int cm : {2, 4}) {
           const int c = std::min(hpg, cm * b);
           if (c <= b) continue;

@@ -402,8 +402,9 @@ cudaError_t launch_linscan(const float* a, const float* b, float* h, int64_t row
                            const LinscanWorkspace& ws, const LookbackCtl& ctl, cudaStream_t s, int shape = 0);
 constexpr int kLsShapes = 4;
 // The chunk scan's CTA split: tier s covers the next tiles[s] tiles (batch, chunk, group, row
-// tile; in that order, row tile fastest) with items[s] CTAs per tile, a tile's heads split
-// evenly between them.  plan_heads > 0 fixes runs of at most that many heads (one tier).
+// tile; in that order, row tile fastest, the later row tile first) with items[s] CTAs per tile,
+// a tile's heads split evenly between them.  plan_heads > 0 fixes runs of at most that many
+// heads (one tier).
 struct ScTiers {
   int64_t tiles[3];
   int items[3];
