@@ -644,6 +644,8 @@ double sc_model_makespan(const ScTiers& s, int row_tiles, int hpg, int sms) {
   return end;
 }
 
+int64_t sc_ctas(const ScTiers& s) { return s.tiles[0] * s.items[0] + s.tiles[1] * s.items[1] + s.tiles[2] * s.items[2]; }
+
 ScTiers sc_uniform(int64_t tiles, int items) {
   ScTiers s{};
   s.tiles[0] = tiles;
@@ -653,11 +655,12 @@ ScTiers sc_uniform(int64_t tiles, int items) {
 }
 
 // The split for `tiles` tiles of `hpg` heads.  plan_heads > 0 (a plan): runs of at most that
-// many heads, one tier.  0: the split the model finds fastest among one tier of 1..8 CTAs per
+// many heads, one tier.  0: the split the model finds fastest among one tier of up to 8 CTAs per
 // tile and three tiers around the best of those (the first f chunks with a CTAs per tile, the
-// last m with c, the rest with b; a <= b < c), kept only where the model gains 2 % (its error
-// is larger than that); computed once per shape and SM count.  Searched only up to 16 waves:
-// beyond, the last wave weighs little.
+// last m with c, the rest with b; a <= b < c), all with runs of at most 40 heads, kept only
+// where the model gains 2 % (its error is larger than that), fewer CTAs deciding between equal
+// model times; computed once per shape and SM count.  Searched only up to 8 waves: beyond, the
+// last wave weighs little.
 ScTiers sc_schedule(int64_t tiles, int row_tiles, int hpg, int sms, int plan_heads) {
   if (plan_heads > 0) {
     const int run = plan_heads < hpg ? plan_heads : hpg;
@@ -678,7 +681,7 @@ ScTiers sc_schedule(int64_t tiles, int row_tiles, int hpg, int sms, int plan_hea
   int b_best = min_items;
   double t_best = -1.0;
   for (int b = min_items; b <= std::max(min_items, std::min(hpg, 8)); ++b) {
-    if (tiles * b > 16LL * sms && b > min_items) break;
+    if (tiles * b > 8LL * sms && b > min_items) break;
     const double tm = sc_model_makespan(sc_uniform(tiles, b), row_tiles, hpg, sms);
     if (t_best < 0 || tm < t_best) {
       t_best = tm;
@@ -687,16 +690,16 @@ ScTiers sc_schedule(int64_t tiles, int row_tiles, int hpg, int sms, int plan_hea
   }
   ScTiers best = sc_uniform(tiles, b_best);
   const int64_t chunks = tiles / row_tiles;  // tiles of one (batch, chunk, group), adjacent
-  if (tiles * b_best <= 16LL * sms && chunks >= 8) {
+  if (tiles * b_best <= 8LL * sms && chunks >= 8) {
     const double uniform_time = t_best;
     for (int b = std::max(min_items, b_best - 1); b <= std::min(hpg, b_best + 1); ++b)
       for (int a = std::max(min_items, b - 1); a <= b; ++a)
         for (int cm : {2, 4}) {
           const int c = std::min(hpg, cm * b);
           if (c <= b) continue;
-          for (int fq : {0, 1, 2, 3, 4})      // first chunks: 0 .. 1/2 of them
-            for (int mq : {0, 1, 2, 4}) {     // last chunks: 0 .. 1/8 of them
-              const int64_t f = chunks * fq / 8, m = chunks * mq / 32;
+          for (int fq : {0, 1, 2, 3, 4})       // first chunks: 0 .. 1/2 of them
+            for (int mq = 0; mq <= 8; ++mq) {  // last chunks: 0 .. 1/8 of them, in 64ths
+              const int64_t f = chunks * fq / 8, m = chunks * mq / 64;
               if ((fq && !f) || (mq && !m) || f + m > chunks) continue;
               ScTiers s{};
               s.tiles[0] = f * row_tiles;
@@ -706,7 +709,10 @@ ScTiers sc_schedule(int64_t tiles, int row_tiles, int hpg, int sms, int plan_hea
               s.tiles[2] = m * row_tiles;
               s.items[2] = c;
               const double tm = sc_model_makespan(s, row_tiles, hpg, sms);
-              if (tm < t_best && tm < 0.98 * uniform_time) {
+              // the model's makespan moves in steps: of equal ones, the split with fewer CTAs
+              // (fewer set-ups) measured faster
+              if (tm < 0.98 * uniform_time &&
+                  (tm < t_best - 1e-9 || (tm <= t_best + 1e-9 && sc_ctas(s) < sc_ctas(best)))) {
                 t_best = tm;
                 best = s;
               }
