@@ -179,6 +179,29 @@ def test_fused_pass_with_more_chains_than_sms(cuda_lib, extra_chains, seqlen, ch
         ssm.clear_ssd_fwd_plans()
 
 
+def test_fused_pass_with_large_B(cuda_lib):
+    """The fused state pass where the group's B rows exceed 32 MB (b2 L65600 G1: 33.6 MB): its B
+    loads then carry no evict-last priority (the lines would keep it after the pass).  Every
+    output is compared with the float64 oracle."""
+    import torch
+    import selective_state_space_mamba_gb300 as ssm
+    from oracle import native
+    shape = synth.SSDShape("fused_large_B", 2, 65600, 4, 64, 128, 1, 256, "bf16", h0=True)
+    assert shape.batch * shape.seqlen * shape.ngroups * 128 * 2 > 32 << 20
+    inp = synth.ssd_inputs(shape, seed=79)
+    d = dev_inputs(inp, "bf16")
+    y_ref, hf_ref = native.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"])
+    try:
+        ssm.set_ssd_fwd_plan(d["x"], d["B"], shape.chunk, ssm.plan_id(1, -1, 0))
+        y, hf = run(ssm, d, shape.chunk)
+        nh = shape.nheads
+        yu = np.stack([y[u // nh, :, u % nh] for u in range(shape.batch * nh)])
+        hu = np.stack([hf[u // nh, u % nh] for u in range(shape.batch * nh)])
+        P.assert_ssd_close("bf16", yu, y_ref, hu, hf_ref, shape.name)
+    finally:
+        ssm.clear_ssd_fwd_plans()
+
+
 def test_fused_pass_shares_the_gpu(cuda_lib):
     """The fused state pass while bf16 matmuls on another stream hold SMs.  Its CTAs take their
     ranges in claim order, not by block index, so a CTA that waits for the state its
