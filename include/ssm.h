@@ -148,8 +148,9 @@ SSM_API ssm_status ssm_ssd_fwd(const void *x, const void *dt, const float *A, co
  * sequential are 1 (yes), 0 (no) or -1 (rule of thumb), heads_per_cta (0 .. 65535) n > 0 gives
  * every chunk-scan CTA a run of at most n heads (a tile's heads split evenly) and 0 means the
  * split a model of the hardware's CTA dispatch finds fastest (large runs first, small runs
- * last; ssm_debug_scan_schedule shows it), and ring is 1 (4 + 3), 2 (3 + 4), 3 (5 + 2) or 0
- * (the rule: 4 + 3).
+ * last; ssm_debug_scan_schedule shows it; the first call of a shape on a device spends up to
+ * ~25 ms of host time on that search, which is cached, makes no CUDA call and so may fall
+ * inside a stream capture), and ring is 1 (4 + 3), 2 (3 + 4), 3 (5 + 2) or 0 (the rule: 4 + 3).
  *
  * ssm_ssd_fwd_tune takes exactly ssm_ssd_fwd's arguments and runs every candidate plan for
  * these sizes on the caller's buffers (y and h_final are overwritten; each candidate computes
