@@ -676,7 +676,7 @@ ScTiers sc_schedule(int64_t tiles, int row_tiles, int hpg, int sms, int plan_hea
   }
   // Runs of at most 40 heads: the later row tile takes ~25 % longer per head, so over a longer
   // run the two row tiles of a chunk drift apart by more than their shared lines stay in L2
-  // (measured at b4 L8192 nh80: runs of 80 heads first cost 1-15 us against runs of 40).
+  // (measured at b4 L8192 nh80: runs of 80 heads first cost 1-20 us against runs of 40).
   const int min_items = (hpg + 39) / 40;
   int b_best = min_items;
   double t_best = -1.0;
