@@ -86,8 +86,10 @@ struct ScParams {
   WsHeader* hdr;
   int64_t batch, lpad, nchunks;
   int nheads, ngroups, chunk, row_tiles;
-  int64_t tier_tiles[3];  // CTAs in order: tier s covers the next tier_tiles[s] tiles,
-  int tier_items[3];      // with tier_items[s] CTAs per tile (its heads split evenly)
+  // CTAs in order: tier s covers the next tier_tiles[s] tiles with tier_items[s] CTAs per tile;
+  // a tile's heads split evenly, tier_run[s] heads per CTA and one more for its first
+  // tier_rem[s] CTAs (all below 2^31: the grid is)
+  int tier_tiles[3], tier_items[3], tier_run[3], tier_rem[3];
 };
 
 // Shared memory (offsets from a 1024-byte aligned base), chunk size T:
@@ -164,33 +166,32 @@ __global__ void __launch_bounds__(kScThreads, 1)
 
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // CTA -> tier -> (tile, run of heads) -> (batch, chunk, group, row tile)
-  int64_t item = 0;
-  int k_item = 0, n_items = 1;
+  // CTA -> tier -> (tile, run of heads) -> (batch, chunk, group, row tile), in 32 bits
+  int item, run0, nh_run;
   {
-    int64_t cta = blockIdx.x, tile0 = 0;
-    for (int s = 0; s < 3; ++s) {
-      const int64_t n = p.tier_tiles[s] * p.tier_items[s];
-      if (cta < n || s == 2) {
-        item = tile0 + cta / p.tier_items[s];
-        k_item = (int)(cta % p.tier_items[s]);
-        n_items = p.tier_items[s];
-        break;
-      }
-      cta -= n;
-      tile0 += p.tier_tiles[s];
-    }
+    // constant parameter indices only (a runtime index would copy the parameters to the stack)
+    const int n0 = p.tier_tiles[0] * p.tier_items[0], n1 = p.tier_tiles[1] * p.tier_items[1];
+    const int cta = blockIdx.x;
+    const bool t0 = cta < n0, t1 = !t0 && cta < n0 + n1;
+    const int rel = t0 ? cta : (t1 ? cta - n0 : cta - n0 - n1);
+    const int tile0 = t0 ? 0 : (t1 ? p.tier_tiles[0] : p.tier_tiles[0] + p.tier_tiles[1]);
+    const int items = t0 ? p.tier_items[0] : (t1 ? p.tier_items[1] : p.tier_items[2]);
+    const int run = t0 ? p.tier_run[0] : (t1 ? p.tier_run[1] : p.tier_run[2]);
+    const int rem = t0 ? p.tier_rem[0] : (t1 ? p.tier_rem[1] : p.tier_rem[2]);
+    item = tile0 + rel / items;
+    const int k_item = rel % items;
+    run0 = k_item * run + min(k_item, rem);
+    nh_run = run + (k_item < rem ? 1 : 0);
   }
   // of a chunk's two row tiles the later one (with the rectangle, the longer CTA) comes first
-  const int R = p.row_tiles - 1 - (int)(item % p.row_tiles);
+  const int R = p.row_tiles - 1 - item % p.row_tiles;
   item /= p.row_tiles;
-  const int g = (int)(item % p.ngroups);
+  const int g = item % p.ngroups;
   item /= p.ngroups;
-  const int64_t c = item % p.nchunks;
-  const int64_t bi = item / p.nchunks;
+  const int64_t c = item % (int)p.nchunks;
+  const int64_t bi = item / (int)p.nchunks;
   const int hpg = p.nheads / p.ngroups;
-  const int h_first = g * hpg + (k_item * hpg) / n_items;
-  const int nh_run = ((k_item + 1) * hpg) / n_items - (k_item * hpg) / n_items;
+  const int h_first = g * hpg + run0;
   const int i0 = R * 128;   // first chunk row of the tile (0 or 128)
   const int Nj = i0 + 128;  // columns 0 .. Nj-1 can be at or below the diagonal
   const int tok0 = (int)(c * T);
@@ -634,7 +635,7 @@ double sc_model_makespan(const ScTiers& s, int row_tiles, int hpg, int sms) {
     for (int64_t tt = 0; tt < s.tiles[k]; ++tt, ++tile) {
       const double per_head = (row_tiles == 2 && tile % 2 == 0) ? 1.25 : 1.0;  // the later row tile first
       for (int j = 0; j < s.items[k]; ++j) {
-        const int nh = ((j + 1) * hpg) / s.items[k] - (j * hpg) / s.items[k];
+        const int nh = hpg / s.items[k] + (j < hpg % s.items[k] ? 1 : 0);
         const double t0 = free_at.top();
         free_at.pop();
         free_at.push(t0 + nh * per_head + 4.7);
@@ -769,12 +770,14 @@ cudaError_t launch_ssd_chunk_scan_tc(const void* x, const void* B, const void* C
   const int64_t tiles = d.batch * d.nchunks * d.ngroups * p.row_tiles;
   const ScTiers tiers = sc_schedule(tiles, p.row_tiles, hpg, sms, d.plan_scan_heads);
   int64_t grid = 0;
-  for (int k = 0; k < 3; ++k) {
-    p.tier_tiles[k] = tiers.tiles[k];
-    p.tier_items[k] = tiers.items[k];
-    grid += tiers.tiles[k] * tiers.items[k];
-  }
+  for (int k = 0; k < 3; ++k) grid += tiers.tiles[k] * tiers.items[k];
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  for (int k = 0; k < 3; ++k) {
+    p.tier_tiles[k] = (int)tiers.tiles[k];
+    p.tier_items[k] = tiers.items[k];
+    p.tier_run[k] = hpg / tiers.items[k];
+    p.tier_rem[k] = hpg % tiers.items[k];
+  }
   const ScLayout L(d.chunk);
   const size_t smem = L.total + 1024;
   if ((e = ensure_smem_limit(reinterpret_cast<const void*>(ssd_chunk_scan_tc_kernel), smem)) != cudaSuccess)

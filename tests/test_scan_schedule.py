@@ -30,8 +30,8 @@ def decode(tiers, hpg, cta):
     for s, (nt, ni) in enumerate(tiers):
         if cta < nt * ni or s == 2:
             k = cta % ni
-            first = (k * hpg) // ni
-            return tile0 + cta // ni, first, ((k + 1) * hpg) // ni - first
+            run, rem = divmod(hpg, ni)  # the first `rem` CTAs of a tile take one head more
+            return tile0 + cta // ni, k * run + min(k, rem), run + (1 if k < rem else 0)
         cta -= nt * ni
         tile0 += nt
     raise AssertionError("unreachable")
