@@ -90,6 +90,7 @@ struct ScParams {
   // a tile's heads split evenly, tier_run[s] heads per CTA and one more for its first
   // tier_rem[s] CTAs (all below 2^31: the grid is)
   int tier_tiles[3], tier_items[3], tier_run[3], tier_rem[3];
+  int first_wave;  // CTAs below this index (one per SM) may start while the previous kernel runs
 };
 
 // Shared memory (offsets from a 1024-byte aligned base), chunk size T:
@@ -209,7 +210,12 @@ __global__ void __launch_bounds__(kScThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  griddep_wait();  // set-up above touched no global memory; h_in comes from the previous kernel
+  // Each role waits for the previous kernel (griddep_wait) only before its first use of what
+  // that kernel or the cumsum wrote (h_in, G, dt) or of D, so that the C and B rows, CB and
+  // the first two stages' x rows are loaded and built while the previous kernel ends.  The
+  // forward's inputs are safe to read before the wait: the kernel before this one lets its
+  // dependents launch only after its own wait, so by the time this grid runs every kernel
+  // before that one (which may have written the inputs) has completed.
   auto fail = [&](void) {
     record_error(p.hdr, ctl.epoch, SSM_ERR_TIMEOUT);
     *abort_flag = 1;
@@ -218,6 +224,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
   if (warp == 0) {
     // ------------------------------ TMA producer ------------------------------------------
     if (lane == 0 && nh_run > 0) {
+      const uint32_t x_bytes = (uint32_t)Nj * kRowB, rest_bytes = 2u * 64 * kRowB + 8u * T;  // h_in, G, dt
       mbar_arrive_expect_tx(&bars[kInFull], 2u * 128 * kRowB + 2u * Nj * kRowB);
       for (int sb = 0; sb < 2; ++sb) {
         tc::tma_load_3d(base + L.c0 + sb * 128 * kRowB, &map_c, g * 128 + sb * 64, tok0 + i0, (int)bi, &bars[kInFull]);
@@ -239,6 +246,22 @@ __global__ void __launch_bounds__(kScThreads, 1)
         tc::bulk_prefetch_l2(p.G + grow, 4u * T);
         tc::bulk_prefetch_l2(p.dtT + grow, 4u * T);
       };
+      // A stage's phase completes on the producer's one arrive (issued with the h_in, G and dt
+      // copies) and all of its bytes; the x rows' bytes are declared without an arrive, so that
+      // the first two stages' x can be requested before the wait.
+      auto load_x = [&](int k) {
+        unsigned char* stage = base + L.st0 + (k & 1) * L.st_bytes;
+        mbar_expect_tx(&bars[kStFull + (k & 1)], x_bytes);
+        for (int rb = 0; rb < Nj / 128; ++rb)
+          tc::tma_load_3d(stage + rb * 128 * kRowB, &map_x, (h_first + k) * 64, tok0 + rb * 128, (int)bi,
+                          &bars[kStFull + (k & 1)]);
+      };
+      // x is an input: the first wave requests its first two stages' x before the wait, to
+      // overlap the previous kernel's end.  Later CTAs start after it has ended and keep the
+      // order below (the L2 prefetch two heads ahead first), which measured faster for them.
+      const int x_early = (int)blockIdx.x < p.first_wave ? (nh_run < 2 ? nh_run : 2) : 0;
+      for (int k = 0; k < x_early; ++k) load_x(k);
+      griddep_wait();
       int issued = 0;
       for (int k = 0; k < nh_run && !*abort_flag; ++k) {
         const int st = k & 1;
@@ -252,9 +275,8 @@ __global__ void __launch_bounds__(kScThreads, 1)
         }
         const int h = h_first + k;
         unsigned char* stage = base + L.st0 + st * L.st_bytes;
-        mbar_arrive_expect_tx(&bars[kStFull + st], (uint32_t)Nj * kRowB + 2u * 64 * kRowB + 8u * T);
-        for (int rb = 0; rb < Nj / 128; ++rb)
-          tc::tma_load_3d(stage + rb * 128 * kRowB, &map_x, h * 64, tok0 + rb * 128, (int)bi, &bars[kStFull + st]);
+        if (k >= x_early) load_x(k);
+        mbar_arrive_expect_tx(&bars[kStFull + st], rest_bytes);
         const int64_t hin_row = ((bi * p.nchunks + c) * p.nheads + h) * 64;
         // h_in rows [b x nc x nh x 64] and the [b, nh, lpad] G / dt^T rows of this head and chunk
         if (SSM_CHECK(p.hdr, h < p.nheads && hin_row + 64 <= p.batch * p.nchunks * p.nheads * 64))
@@ -267,7 +289,11 @@ __global__ void __launch_bounds__(kScThreads, 1)
         }
         issued = k + 1;
       }
-      for (int k = max(0, issued - 2); k < issued; ++k)
+      // a stage whose x was requested early but whose other copies were not (an abort) gets
+      // its arrive now, so that its phase completes once the x rows have landed
+      for (int k = issued; k < x_early; ++k) mbar_arrive(&bars[kStFull + k]);
+      const int in_flight = issued > x_early ? issued : x_early;
+      for (int k = max(0, in_flight - 2); k < in_flight; ++k)
         mbar_wait(&bars[kStFull + (k & 1)], (uint32_t)(k >> 1) & 1u, ctl.spin_limit_ns);
       mbar_wait(&bars[kInFull], 0, ctl.spin_limit_ns);
     }
@@ -289,6 +315,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
         }
         tc::mma_commit(&bars[kCbDone]);
       }
+      griddep_wait();
       const uint32_t id_kk = tc::idesc_bf16_f32(128, 64, false, false);  // Y2: C, h_in both K-major
       const uint32_t id_kn = tc::idesc_bf16_f32(128, 64, false, true);   // Ya, Yt: X MN-major
       const uint32_t xlbo = (uint32_t)T * kRowB;
@@ -381,6 +408,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
       fence_proxy_async_smem();  // the rectangle MMA reads CB through the async proxy
       tc::fence_before_sync();
     }
+    griddep_wait();
 
     // Factor table of head k (layout at kVTri / kVRect / kVDiag).  Returns false (all threads
     // alike) when the head's stage never arrived.
@@ -520,6 +548,7 @@ __global__ void __launch_bounds__(kScThreads, 1)
     // y = Yt + 2^(G_i) Y2 + u_i Ya + D x for the tile's 128 rows (one per thread) x 64 p.
     // x and G are read from the stage as soon as it lands (the stage is refilled only after
     // this group has released it through kXRead); the accumulators once the MMAs are done.
+    griddep_wait();  // D, and the stages' h_in, G and dt
     const int et = threadIdx.x - 320;  // 0..127
     const int quad = warp & 3;         // TMEM lanes 32*quad .. +31
     const int r = quad * 32 + lane;    // tile row
@@ -772,6 +801,7 @@ cudaError_t launch_ssd_chunk_scan_tc(const void* x, const void* B, const void* C
   int64_t grid = 0;
   for (int k = 0; k < 3; ++k) grid += tiers.tiles[k] * tiers.items[k];
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  p.first_wave = sms;
   for (int k = 0; k < 3; ++k) {
     p.tier_tiles[k] = (int)tiers.tiles[k];
     p.tier_items[k] = tiers.items[k];

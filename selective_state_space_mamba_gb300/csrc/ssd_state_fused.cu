@@ -178,7 +178,6 @@ __global__ void __launch_bounds__(kSfThreads, 1)
   constexpr int kSFree = kSReady + 2, kDone = kSFree + 2, kSfNumBars = kDone + 1;
   static_assert(kSfNumBars <= 32, "barrier area");
   extern __shared__ unsigned char sf_raw[];
-  griddep_launch_dependents();
   const uint32_t raw = smem_addr(sf_raw);
   unsigned char* base = sf_raw + ((1024u - (raw & 1023u)) & 1023u);
   const int T = p.chunk;
@@ -214,6 +213,10 @@ __global__ void __launch_bounds__(kSfThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   griddep_wait();  // G and dt come from the previous kernel (which also zeroed the claim counter)
+  // Dependents may launch only now: the chunk scan loads the forward's inputs (C, B, x) before
+  // its own wait, which is safe because this point is reached only after the cumsum, and so
+  // every kernel before it, has completed.
+  griddep_launch_dependents();
   // The CTA's range index is claimed in order from the workspace counter, not taken from
   // blockIdx: the CTA it may wait for (range index - 1) has then claimed first, so it is
   // running, and its first segment waits for nobody.  No CTA needs another to be resident.

@@ -56,8 +56,10 @@ __global__ void __launch_bounds__(kSpThreads, kSpMinBlocks)
   __shared__ uint64_t s_bar;
   __shared__ uint32_t s_tile;
   __shared__ int s_last, s_found;
-  griddep_launch_dependents();
   griddep_wait();  // S_c, G and the claim counter come from the previous kernels
+  // after the wait: the chunk scan that follows loads the forward's inputs before its own
+  // wait, which is safe once this grid's start implies that every earlier kernel has ended
+  griddep_launch_dependents();
   const LookbackCtl ctl = device_epoch(ctl_call, ws.hdr);
 
   if (threadIdx.x == 0) {
@@ -229,8 +231,8 @@ __global__ void __launch_bounds__(kSeqThreads) ssd_state_passing_seq_kernel(cons
                                                                             float* __restrict__ h_final, SsdDims d,
                                                                             SsdWorkspace ws) {
   __shared__ float4 ring[kSeqAhead][kSeqThreads];
-  griddep_launch_dependents();
   griddep_wait();  // S_c and G come from the previous kernels
+  griddep_launch_dependents();  // after the wait, as in the look-back kernel above
   const int HS = d.headdim * d.dstate;
   const int64_t q4 = HS / 4;
   const int64_t gidx = (int64_t)blockIdx.x * kSeqThreads + threadIdx.x;
