@@ -155,7 +155,10 @@ SSM_API ssm_status ssm_ssd_fwd(const void *x, const void *dt, const float *A, co
  * ssm_ssd_fwd_tune takes exactly ssm_ssd_fwd's arguments and runs every candidate plan for
  * these sizes on the caller's buffers (y and h_final are overwritten; each candidate computes
  * the same result up to rounding): one warm-up and `reps` timed runs each (CUDA events on
- * `stream`), synchronizing the stream.  The plan with the smallest median time is stored for
+ * `stream`), synchronizing the stream.  Before each run, outside the timed events, it writes a
+ * temporary device buffer of twice the L2 size (allocated for the call and freed at its end;
+ * the runs go back to back if it cannot be allocated), so that every candidate is timed with
+ * its inputs out of L2, as after other work.  The plan with the smallest median time is stored for
  * the current device and these sizes in a process-wide table that later ssm_ssd_fwd calls
  * with the same sizes use; *plan_out and *ms_out (either may be NULL) receive it and its time.
  * A device error recorded by a candidate (SSM_ERR_TIMEOUT) is returned and no plan is stored.
@@ -233,7 +236,7 @@ SSM_API ssm_status ssm_linscan_fwd(const float *a, const float *b, float *h, int
  *   4  one group, 6 stages, one CTA per SM
  * ssm_linscan_fwd_tune takes ssm_linscan_fwd's arguments, runs every shape on the caller's
  * buffers (h is overwritten with the scan; a warm-up and `reps` timed runs each, CUDA events on
- * `stream`, synchronizing it) and stores the shape with the smallest median time for the current
+ * `stream`, synchronizing it; each run preceded by the same L2 flush as ssm_ssd_fwd_tune's) and stores the shape with the smallest median time for the current
  * device and these (rows, len) in a process-wide table that later ssm_linscan_fwd calls use;
  * *shape_out and *ms_out (either may be NULL) receive it and its time.  A device error recorded
  * by a candidate (SSM_ERR_TIMEOUT) is returned and nothing is stored.  ssm_linscan_set_shape

@@ -117,6 +117,34 @@ SsdDims make_dims(int64_t batch, int64_t seqlen, int nheads, int headdim, int ds
   return d;
 }
 
+// Scratch that a tuner writes before each of its runs, outside the timed events: twice the
+// L2 size, so that every candidate starts with its inputs out of L2 and dirty lines of other
+// data in it, as a call does after other work, and not from the previous candidate's warm
+// lines (which would favour, for inputs that fit in L2, plans that are slower from DRAM).
+// Without the memory for it the runs go back to back.
+struct TuneFlush {
+  void* buf = nullptr;
+  size_t bytes = 0;
+  TuneFlush() {
+    int dev = 0, l2 = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess ||
+        l2 <= 0)
+      return;
+    if (cudaMalloc(&buf, 2 * (size_t)l2) != cudaSuccess) {
+      buf = nullptr;
+      (void)cudaGetLastError();  // clear the allocation error: the tuner runs on without it
+      return;
+    }
+    bytes = 2 * (size_t)l2;
+  }
+  ~TuneFlush() {
+    if (buf) cudaFree(buf);
+  }
+  TuneFlush(const TuneFlush&) = delete;
+  TuneFlush& operator=(const TuneFlush&) = delete;
+  cudaError_t run(cudaStream_t s, int r) const { return buf ? cudaMemsetAsync(buf, r & 0xff, bytes, s) : cudaSuccess; }
+};
+
 // ---- per-shape plans (ssm_ssd_fwd_tune / ssm_ssd_fwd_set_plan) ----
 // A plan id packs (fused + 1) | (seq + 1) << 2 | scan_heads << 4 | ring << 20, with -1 (0 for
 // scan_heads and ring) meaning "the heuristic".
@@ -435,12 +463,13 @@ ssm_status ssm_ssd_fwd_tune(const void* x, const void* dt, const float* A, const
   int best = -1;
   float best_ms = 0.f;
   st = SSM_OK;
+  const TuneFlush flush;
   for (int id : cands) {
     SsdDims dc = d;
     apply_plan(dc, id);
     std::vector<float> t;
     for (int r = 0; r <= reps && st == SSM_OK; ++r) {  // one warm-up, then `reps` timed runs
-      if (cudaEventRecord(e0, s) != cudaSuccess) st = SSM_ERR_CUDA;
+      if (flush.run(s, r) != cudaSuccess || cudaEventRecord(e0, s) != cudaSuccess) st = SSM_ERR_CUDA;
       if (st == SSM_OK) st = run_ssd(x, dt, A, B, C, D, h0, y, h_final, dc, workspace, s);
       if (st == SSM_OK && cudaEventRecord(e1, s) != cudaSuccess) st = SSM_ERR_CUDA;
       float ms = 0.f;
@@ -590,10 +619,11 @@ ssm_status ssm_linscan_fwd_tune(const float* a, const float* b, float* h, int64_
   }
   int best = -1;
   float best_ms = 0.f;
+  const TuneFlush flush;
   for (int shape = 1; shape <= kLsShapes && st == SSM_OK; ++shape) {
     std::vector<float> t;
     for (int r = 0; r <= reps && st == SSM_OK; ++r) {  // one warm-up, then `reps` timed runs
-      if (cudaEventRecord(e0, s) != cudaSuccess ||
+      if (flush.run(s, r) != cudaSuccess || cudaEventRecord(e0, s) != cudaSuccess ||
           launch_linscan(a, b, h, rows, len, ws, next_lookback_ctl(), s, shape) != cudaSuccess ||
           cudaEventRecord(e1, s) != cudaSuccess) {
         st = SSM_ERR_CUDA;
