@@ -139,13 +139,20 @@ SSM_API ssm_status ssm_ssd_fwd(const void *x, const void *dt, const float *A, co
  *     (batch, head pair) chains than SMs the one-kernel pass runs one CTA per SM on equal
  *     ranges of chunks, and a CTA that starts inside a chain waits (bounded) for the state its
  *     predecessor publishes; the CTAs claim their ranges in order, so that predecessor is
- *     always already running and the pass needs no co-residency of its CTAs;
+ *     always already running and the pass needs no co-residency of its CTAs.  With few long
+ *     chains the one-kernel pass can instead split them ("split chains"): one CTA per SM runs
+ *     an equal piece of chunks at once, every piece that starts inside a chain from a zero
+ *     state, and a light second kernel then adds to each such piece's chunk-initial states the
+ *     state it enters with (composed in f32 from the pieces' end states; h_in is then rounded
+ *     to bf16 twice);
  *   - the one-kernel pass's shared-memory ring split: X slots (loaded from DRAM) and B slots
  *     (loaded from L2) share a fixed budget: 4 + 3, 3 + 4 or 5 + 2;
  *   - the chunk scan's run of heads per CTA (the tensor-core path).
  * Without a plan, ssm_ssd_fwd picks by fixed rules of thumb.  A plan id packs
  * (fused + 1) | (sequential + 1) << 2 | heads_per_cta << 4 | ring << 20, where fused and
- * sequential are 1 (yes), 0 (no) or -1 (rule of thumb), heads_per_cta (0 .. 65535) n > 0 gives
+ * sequential are 1 (yes), 0 (no) or -1 (rule of thumb), fused may also be 2 (the one-kernel
+ * pass with split chains; the rule takes it for between a sixteenth and a half as many chains
+ * as SMs, with at least 64 chunks each), heads_per_cta (0 .. 65535) n > 0 gives
  * every chunk-scan CTA a run of at most n heads (a tile's heads split evenly) and 0 means the
  * split a model of the hardware's CTA dispatch finds fastest (large runs first, small runs
  * last; ssm_debug_scan_schedule shows it; the first call of a shape on a device spends up to
@@ -354,10 +361,13 @@ SSM_API ssm_status ssm_debug_set_bounds_fault(int64_t shrink);
  * (batch, head pair) chains of `nchunks` chunks on a GPU with `sms` SMs it lists, in the order
  * each CTA runs them, the segments of every CTA: one row of six int64 per segment, (cta, chain,
  * first chunk, end chunk, starts from the state the previous CTA publishes, publishes its final
- * state for the next CTA).  Writes at most `cap` rows to `rows` (which may be NULL) and
- * returns the number of segments, or -1 for a negative size or sms < 1.
+ * state for the next CTA).  With `split` nonzero, the split-chains schedule: a segment that
+ * starts inside its chain starts from zero instead (its state is added afterwards) and one that
+ * ends inside its chain publishes into its CTA's own slot.  Writes at most `cap` rows to `rows`
+ * (which may be NULL) and returns the number of segments, or -1 for a negative size or sms < 1.
  */
-SSM_API int64_t ssm_debug_fused_schedule(int64_t chains, int64_t nchunks, int sms, int64_t *rows, int64_t cap);
+SSM_API int64_t ssm_debug_fused_schedule(int64_t chains, int64_t nchunks, int sms, int split, int64_t *rows,
+                                         int64_t cap);
 
 /*
  * Test hook for the chunk scan's work split (host only; no GPU call).  The chunk scan's CTAs
@@ -381,10 +391,11 @@ SSM_API int64_t ssm_debug_scan_schedule(int64_t tiles, int row_tiles, int heads_
  * Kernel ids: 0 linscan_lookback, 1 ssd_chunk_cumsum, 2 ssd_chunk_state,
  * 3 ssd_state_passing, 4 ssd_chunk_scan, 5 ssd_state_fused (chunk states and state passing in
  * one pass; used instead of 2 and 3 where it applies), 6 ssd_step (ssm_ssd_step),
- * 7 linscan_baseline (ssm_linscan_baseline, all its launches).  Host-side only;
+ * 7 linscan_baseline (ssm_linscan_baseline, all its launches), 8 ssd_state_fixup (the second
+ * kernel of the one-kernel state pass with split chains).  Host-side only;
  * process-global; not thread-safe.
  */
-#define SSM_PROFILE_KERNELS 8
+#define SSM_PROFILE_KERNELS 9
 SSM_API ssm_status ssm_profile_begin(int max_launches);
 SSM_API ssm_status ssm_profile_end(double *ms_out, int64_t *launches_out);
 

@@ -159,8 +159,9 @@ def _ssd_sizes(x, B, chunk):
 
 
 def plan_id(fused: int = -1, sequential: int = -1, heads_per_cta: int = 0, fused_ring: int = 0) -> int:
-    """Pack a plan for ssd_fwd (see include/ssm.h): each flag 1, 0 or -1 (rule of thumb); fused_ring
-    1, 2 or 3 picks the fused pass's X + B slot split (4 + 3, 3 + 4, 5 + 2), 0 its rule."""
+    """Pack a plan for ssd_fwd (see include/ssm.h): each flag 1, 0 or -1 (rule of thumb), fused
+    also 2 (the fused pass with split chains); fused_ring 1, 2 or 3 picks the fused pass's X + B
+    slot split (4 + 3, 3 + 4, 5 + 2), 0 its rule."""
     return (fused + 1) | ((sequential + 1) << 2) | (heads_per_cta << 4) | (fused_ring << 20)
 
 

@@ -27,7 +27,7 @@ EXPORTS = ("ssm_status_string", "ssm_version", "ssm_ssd_fwd_workspace_bytes", "s
            "ssm_debug_build", "ssm_debug_set_bounds_fault", "ssm_linscan_fwd_tune", "ssm_linscan_set_shape",
            "ssm_linscan_get_shape", "ssm_linscan_clear_shapes")
 PROFILE_KERNELS = ("linscan_lookback", "ssd_chunk_cumsum", "ssd_chunk_state", "ssd_state_passing", "ssd_chunk_scan",
-                   "ssd_state_fused", "ssd_step", "linscan_baseline")
+                   "ssd_state_fused", "ssd_step", "linscan_baseline", "ssd_state_fixup")
 
 _lib = None
 _lock = threading.Lock()
@@ -51,7 +51,7 @@ def _declare(lib):
     lib.ssm_ssd_fwd.restype = i32
     lib.ssm_ssd_fwd_tune.argtypes = [vp] * 9 + [i64, i64, i32, i32, i32, i32, i32, i32, vp, sz, vp, i32, vp, vp]
     lib.ssm_ssd_fwd_tune.restype = i32
-    lib.ssm_debug_fused_schedule.argtypes = [i64, i64, i32, vp, i64]
+    lib.ssm_debug_fused_schedule.argtypes = [i64, i64, i32, i32, vp, i64]
     lib.ssm_debug_fused_schedule.restype = i64
     lib.ssm_debug_scan_schedule.argtypes = [i64, i32, i32, i32, i32, vp]
     lib.ssm_debug_scan_schedule.restype = i64

@@ -22,7 +22,9 @@ cudaError_t launch_ssd_chunk_state_tc(const void* x, const void* B, const SsdDim
 bool ssd_scan_tc_supported(const SsdDims& d);
 bool ssd_state_fused_supported(const SsdDims& d);
 bool ssd_state_fused_possible(const SsdDims& d);
-int64_t ssd_fused_schedule(int64_t chains, int64_t nchunks, int sms, int64_t* rows, int64_t cap);
+bool ssd_state_fused_split(const SsdDims& d);
+int64_t ssd_fused_schedule(int64_t chains, int64_t nchunks, int sms, bool split, int64_t* rows, int64_t cap);
+cudaError_t launch_ssd_state_fixup(float* h_final, const SsdDims& d, const SsdWorkspace& ws, cudaStream_t s);
 cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float* h0, float* h_final,
                                       const SsdDims& d, const SsdWorkspace& ws, const LookbackCtl& ctl,
                                       cudaStream_t s);
@@ -147,7 +149,7 @@ struct TuneFlush {
 
 // ---- per-shape plans (ssm_ssd_fwd_tune / ssm_ssd_fwd_set_plan) ----
 // A plan id packs (fused + 1) | (seq + 1) << 2 | scan_heads << 4 | ring << 20, with -1 (0 for
-// scan_heads and ring) meaning "the heuristic".
+// scan_heads and ring) meaning "the heuristic"; fused 2 is the fused pass with split chains.
 struct PlanKey {
   int dev;
   int64_t batch, seqlen;
@@ -169,7 +171,7 @@ bool plan_key(const SsdDims& d, PlanKey* k) {
 int plan_id(int fused, int seq, int heads, int ring = 0) {
   return (fused + 1) | ((seq + 1) << 2) | (heads << 4) | (ring << 20);
 }
-bool plan_valid(int id) { return id >= 0 && (id & 3) != 3 && ((id >> 2) & 3) != 3 && (id >> 20) <= 3; }
+bool plan_valid(int id) { return id >= 0 && ((id >> 2) & 3) != 3 && (id >> 20) <= 3; }
 void apply_plan(SsdDims& d, int id) {
   d.plan_fused = (id & 3) - 1;
   d.plan_seq = ((id >> 2) & 3) - 1;
@@ -351,6 +353,10 @@ ssm_status run_ssd(const void* x, const void* dt, const float* A, const void* B,
     if (timed_launch(5, s, [&] { return launch_ssd_state_fused_tc(x, B, h0, h_final, d, ws, ctl, s); }) !=
         cudaSuccess)
       return SSM_ERR_CUDA;
+    // split chains: add to every piece the state it enters with
+    if (ssd_state_fused_split(d) &&
+        timed_launch(8, s, [&] { return launch_ssd_state_fixup(h_final, d, ws, s); }) != cudaSuccess)
+      return SSM_ERR_CUDA;
   } else {
     if (timed_launch(2, s, [&] {
           return state_tc ? launch_ssd_chunk_state_tc(x, B, d, ws, ctl, s)
@@ -438,8 +444,13 @@ ssm_status ssm_ssd_fwd_tune(const void* x, const void* dt, const float* A, const
   st = check_ssd_buffers(x, dt, A, B, C, D, h0, y, h_final, d, workspace, workspace_bytes);
   if (st != SSM_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // candidates: the fused state path where it is possible, else the two state kernels with
-  // either state-passing kernel; times the chunk scan's runs of heads per CTA
+  // candidates: the fused state path where it is possible (with split chains as well where
+  // there are fewer chains than SMs), else the two state kernels with either state-passing
+  // kernel; times the chunk scan's runs of heads per CTA
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SSM_ERR_CUDA;
+  const bool split_cands = d.nchunks > 1 && batch * (int64_t)(nheads / 2) < sms;
   std::vector<int> cands;
   std::vector<int> heads = {0};
   if (ssd_scan_tc_supported(d)) {
@@ -450,7 +461,10 @@ ssm_status ssm_ssd_fwd_tune(const void* x, const void* dt, const float* A, const
   }
   for (int hd : heads) {
     if (ssd_tc_supported(d) && ssd_state_fused_possible(d))
-      for (int ring = 1; ring <= 3; ++ring) cands.push_back(plan_id(1, -1, hd, ring));  // ring splits
+      for (int ring = 1; ring <= 3; ++ring) {  // ring splits
+        cands.push_back(plan_id(1, -1, hd, ring));
+        if (split_cands) cands.push_back(plan_id(2, -1, hd, ring));  // the same with split chains
+      }
     cands.push_back(plan_id(0, 1, hd));
     cands.push_back(plan_id(0, 0, hd));
   }
@@ -801,8 +815,8 @@ ssm_status ssm_debug_set_bounds_fault(int64_t shrink) {
 #endif
 }
 
-int64_t ssm_debug_fused_schedule(int64_t chains, int64_t nchunks, int sms, int64_t* rows, int64_t cap) {
-  return ssd_fused_schedule(chains, nchunks, sms, rows, cap < 0 ? 0 : cap);
+int64_t ssm_debug_fused_schedule(int64_t chains, int64_t nchunks, int sms, int split, int64_t* rows, int64_t cap) {
+  return ssd_fused_schedule(chains, nchunks, sms, split != 0, rows, cap < 0 ? 0 : cap);
 }
 
 int64_t ssm_debug_scan_schedule(int64_t tiles, int row_tiles, int heads_per_group, int sms, int plan_heads,

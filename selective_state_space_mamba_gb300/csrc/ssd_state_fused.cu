@@ -13,6 +13,13 @@
 // whole chains, then the tail, which starts from the state the previous CTA published for
 // that chain: the previous CTA ran that head first, and its head is shorter than what this
 // CTA runs before its tail by the range length minus the chain length, so the wait is short.
+// With few long chains (fewer than half as many as SMs) one CTA per chain leaves most SMs idle,
+// so the pass can instead split them ("split chains"): one CTA per SM runs an equal range of
+// units at once, every segment that starts inside its chain from a zero state, and each range
+// publishes the state where it stops into its own slot; ssd_state_fixup (below) then adds to
+// every such piece's h_in, and to h_final, the state the piece enters with.  The recurrence is
+// linear in the state, so this gives the chain's states exactly (h_in is rounded to bf16 once
+// more).
 // The pair's rows (2 heads x 64 p = 128 TMEM lanes, x 128 s columns, f32) have three TMEM
 // homes: the running state h and two accumulators S[0], S[1].  The MMAs add the weighted X^T B
 // of the CTA's q-th chunk c into S[q & 1] without waiting for the state; the state warps then
@@ -38,6 +45,10 @@
 // Every wait is bounded; on expiry the CTA records SSM_ERR_TIMEOUT, drains, frees its TMEM and
 // returns.
 #include "tc_common.cuh"
+
+#ifndef SSM_SF_SPLIT_MIN_CHUNKS  // the rule splits chains of at least this many chunks
+#define SSM_SF_SPLIT_MIN_CHUNKS 64
+#endif
 
 namespace ssm {
 namespace {
@@ -67,6 +78,7 @@ struct SfParams {
   int64_t batch, lpad, nchunks, units;  // units = chains x nchunks
   int nheads, ngroups, chunk;
   int b_keep;  // B is small next to L2: load it with evict-last priority
+  int split;   // chains split into independent pieces (see ssd_state_fixup below)
 };
 
 // This CTA's units [u0, u1) of (chain, chunk), chain-major, as segments in the order they run:
@@ -76,7 +88,7 @@ struct SfParams {
 struct SfRange {
   int64_t first_chain, last_chain, full_begin;
   int c_first, c_last_end, nfull, nseg;
-  bool has_tail, has_head;
+  bool has_tail, has_head, single;  // single: the range lies inside one chain (one segment)
 };
 struct SfSeg {
   int64_t chain;
@@ -95,10 +107,20 @@ __host__ __device__ __forceinline__ SfRange sf_range(int64_t u0, int64_t u1, int
   const int64_t full_end = r.last_chain + (r.has_head ? 0 : 1);
   r.nfull = full_end > r.full_begin ? (int)(full_end - r.full_begin) : 0;
   r.nseg = (r.has_head ? 1 : 0) + r.nfull + (r.has_tail ? 1 : 0);
+  r.single = r.first_chain == r.last_chain;
+  if (r.single) r.nseg = 1;  // a whole chain, or (split chains) a piece inside one
   return r;
 }
 __host__ __device__ __forceinline__ SfSeg sf_seg(const SfRange& r, int s, int64_t nc) {
   SfSeg g;
+  if (r.single) {
+    g.chain = r.first_chain;
+    g.c0 = r.c_first;
+    g.c1 = r.c_last_end;
+    g.from_carry = r.c_first > 0;
+    g.to_carry = r.c_last_end < nc;
+    return g;
+  }
   if (r.has_head) {
     if (s == 0) {
       g.chain = r.last_chain;
@@ -225,7 +247,7 @@ __global__ void __launch_bounds__(kSfThreads, 1)
   const int64_t vb = *claim_slot;
   const int64_t u0 = vb * p.units / gridDim.x;
   const int64_t u1 = (vb + 1) * p.units / gridDim.x;
-  const SfRange rg = nc > 0 && u1 > u0 ? sf_range(u0, u1, nc) : SfRange{0, 0, 0, 0, 0, 0, 0, false, false};
+  const SfRange rg = nc > 0 && u1 > u0 ? sf_range(u0, u1, nc) : SfRange{0, 0, 0, 0, 0, 0, 0, false, false, false};
   // published states carry this launch's epoch (the last CTA to finish moves it on)
   const LookbackCtl ctl = device_epoch(ctl_call, p.hdr);
   auto fail = [&](void) {
@@ -450,9 +472,11 @@ __global__ void __launch_bounds__(kSfThreads, 1)
         break;
       }
       const float* h0r = p.h0 ? p.h0 + (bh * 64 + pp) * 128 + col0 : nullptr;
-      float* cr = p.carry + (sg.chain * 128 + m) * 128 + col0;  // this row of the chain's published state
+      // this row of the published state: the chain's slot, or with split chains the range's
+      // (a range ends inside at most one chain)
+      float* cr = p.carry + ((p.split ? vb : sg.chain) * 128 + m) * 128 + col0;
       const float* Glast = p.G + bh * p.lpad + (T - 1);  // G_last of chunk c at Glast[c * T]
-      if (sg.from_carry) {
+      if (sg.from_carry && !p.split) {
         // the previous CTA ran this chain's head first and published where it stopped
         bool bad = false;
         if (leader) bad = wait_flag(&p.flags[sg.chain], p.hdr, ctl) != kFlagPrefix;
@@ -488,6 +512,9 @@ __global__ void __launch_bounds__(kSfThreads, 1)
               const float4 f = h0r ? reinterpret_cast<const float4*>(h0r + 16 * qq)[j] : make_float4(0.f, 0.f, 0.f, 0.f);
               v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
             }
+          } else if (first && p.split) {  // a piece of a split chain: from zero, fixed up later
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = 0.f;
           } else if (first) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -530,7 +557,7 @@ __global__ void __launch_bounds__(kSfThreads, 1)
           }
         }
         tc::tmem_st_wait();
-        if (publish) __threadfence();  // this thread's part of the published state, before the flag
+        if (publish && !p.split) __threadfence();  // this thread's part of the published state, before the flag
         fence_proxy_async_smem();      // the staged h_in, before the TMA store reads it
         tc::fence_before_sync();
         named_bar_sync(kSfStateBar, kSfStateThreads);
@@ -541,7 +568,7 @@ __global__ void __launch_bounds__(kSfThreads, 1)
               tma_store_2d(&map_hin, base + L.hs0 + s2 * (128 * kSfRowBytes), 64 * s2, (int)row0);
           bulk_commit();
           mbar_arrive(&bars[kSFree + sb]);  // S[sb] may take the chunk run two later
-          if (publish) st_release_u64(&p.flags[sg.chain], make_flag(ctl.epoch, kFlagPrefix));
+          if (publish && !p.split) st_release_u64(&p.flags[sg.chain], make_flag(ctl.epoch, kFlagPrefix));
         }
       }
     }
@@ -564,17 +591,158 @@ __global__ void __launch_bounds__(kSfThreads, 1)
   if (threadIdx.x == 0) retire_tile(p.hdr, gridDim.x);  // the last CTA moves the epoch on
 }
 
+// ---------------------------------------------------------------------------------------------
+// ssd_state_fixup: with split chains the fused pass runs all pieces of a chain at once, every
+// piece that starts inside its chain from a zero state, and each range leaves the state where
+// its last segment ends in its own slot E[j] (j = the range index).  The state entering the
+// piece that range k starts at unit u_k (inside chain z, which starts at unit zc) follows the
+// chain's own recurrence taken over pieces:
+//     H(u_k) = E[k-1] + 2^(D(u_(k-1), u_k)) H(u_(k-1))   if u_(k-1) > zc,  else  H(u_k) = E[k-1]
+// with D(a, b) the decay exponent (the sum of G_last) over the chunks a .. b-1.  This kernel
+// forms H(u_k) in f32 and adds 2^(D(u_k, c)) H(u_k) to h_in[c] for every chunk c of the piece,
+// and to h_final where the piece ends its chain; what the fused pass wrote there is the
+// piece's own part, exact by linearity of the recurrence.  One CTA per (piece, block of 16
+// state rows of one head), eight consecutive entries per thread.
+constexpr int kFxThreads = 256;
+constexpr int kFxRows = 16;
+constexpr int kFxPieces = 256;  // earlier pieces whose decay sums are formed together
+constexpr int kFxBatch = 8;     // chunks whose h_in loads are in flight together
+constexpr int kFxFold = 2;      // earlier pieces' end states in flight together
+
+struct FxParams {
+  const float* G;
+  __nv_bfloat16* hin;  // [b, nc, nh, 64, 128]
+  float* h_final;      // [b, nh, 64, 128] or null
+  const float* carry;  // [ranges][128 rows][128]: E
+  int64_t units, ranges, nchunks, lpad;
+  int nheads, chunk;
+};
+
+// eight bf16 (w) += f * acc, rounded back to bf16
+__device__ __forceinline__ void fx_apply(uint4& w, float f, const float* acc) {
+  uint32_t* u = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __uint_as_float(u[i] << 16), hi = __uint_as_float(u[i] & 0xffff0000u);
+    const __nv_bfloat162 r = __floats2bfloat162_rn(fmaf(f, acc[2 * i], lo), fmaf(f, acc[2 * i + 1], hi));
+    u[i] = *reinterpret_cast<const uint32_t*>(&r);
+  }
+}
+
+__global__ void __launch_bounds__(kFxThreads, 3) ssd_state_fixup_kernel(FxParams p) {
+  __shared__ float s_piece[kFxPieces];  // decay exponents of the pieces walked back over
+  griddep_wait();               // h_in, h_final and E come from the fused pass
+  griddep_launch_dependents();  // after the wait: the chunk scan reads the forward's inputs early
+  const int64_t nc = p.nchunks;
+  constexpr int kBlocks = 128 / kFxRows;
+  const int64_t k = 1 + blockIdx.x / kBlocks;  // the range that starts the piece
+  const int rb = (int)(blockIdx.x % kBlocks);
+  auto u = [&](int64_t j) { return j * p.units / p.ranges; };
+  const int64_t uk = u(k);
+  if (k >= p.ranges || uk % nc == 0) return;  // a piece that starts its chain began from h0
+  const int64_t z = uk / nc, zc = z * nc;
+  const int b = (int)(uk - zc);  // the piece's chunks [b, e) of the chain (below 2^31)
+  const int e = (int)((u(k + 1) < zc + nc ? u(k + 1) : zc + nc) - zc);
+  const int pairs = p.nheads / 2;
+  const int64_t bi = z / pairs;
+  const int m = rb * kFxRows + (int)threadIdx.x / 16;  // state row of the pair, 0 .. 127
+  const int h = 2 * (int)(z % pairs) + m / 64, pp = m & 63;
+  const int s0 = ((int)threadIdx.x % 16) * 8;
+  const int warp = (int)threadIdx.x >> 5, lane = (int)threadIdx.x & 31;
+  const int64_t bh = bi * p.nheads + h;
+  const float* Glast = p.G + bh * p.lpad + (p.chunk - 1);  // G_last of chunk c at Glast[c * chunk]
+  const float* slot = p.carry + m * 128 + s0;             // E[j] at slot + j * 16384
+  auto load8 = [&](int64_t j, float* v) {
+    const float4* q = reinterpret_cast<const float4*>(slot + j * 16384);
+    const float4 a0 = q[0], a1 = q[1];
+    v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
+    v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+  };
+  // H(u_k) = E[k-1] + sum over the pieces j < k of this chain that start inside it (u(j) > zc)
+  // of 2^(D(u(j), u_k)) E[j-1], unrolled from the recurrence above
+  float acc[8];
+  load8(k - 1, acc);
+  int64_t j_lo = k;
+  while (j_lo > 1 && u(j_lo - 1) > zc) --j_lo;  // pieces j_lo .. k-1 started inside the chain
+  float lg = 0.f;                               // D(u(j), u_k), accumulated newest first
+  for (int64_t jb = k - 1; jb >= j_lo; jb -= kFxPieces) {
+    const int nb = (int)(jb - j_lo + 1 < kFxPieces ? jb - j_lo + 1 : kFxPieces);  // pieces jb, jb-1, ..
+    __syncthreads();  // s_piece of the previous batch has been read
+    for (int i = warp; i < nb; i += kFxThreads / 32) {  // a warp per piece: its decay exponent
+      const int64_t j = jb - i;
+      float t = 0.f;
+      for (int64_t c = u(j) - zc + lane; c < u(j + 1) - zc; c += 32) t += Glast[c * p.chunk];
+      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      if (lane == 0) s_piece[i] = t;
+    }
+    __syncthreads();
+    for (int i0 = 0; i0 < nb; i0 += kFxFold) {  // kFxFold pieces' end states in flight at a time
+      float v[kFxFold][8];
+#pragma unroll
+      for (int i = 0; i < kFxFold; ++i)
+        if (i0 + i < nb) load8(jb - (i0 + i) - 1, v[i]);
+#pragma unroll
+      for (int i = 0; i < kFxFold; ++i) {
+        if (i0 + i < nb) {
+          lg += s_piece[i0 + i];
+          const float f = exp2f(lg);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) acc[q] = fmaf(f, v[i][q], acc[q]);
+        }
+      }
+    }
+  }
+  // h_in[c] += 2^(D(b, c)) H over the piece, kFxBatch chunks per step so that their loads overlap
+  const int64_t cstride = (int64_t)p.nheads * 8192;
+  __nv_bfloat16* q = p.hin + ((bi * nc + b) * p.nheads + h) * 8192 + pp * 128 + s0;  // chunk b
+  const float* gq = Glast + (int64_t)b * p.chunk;
+  float lgc = 0.f;
+  int c = b;
+  for (; c + kFxBatch <= e; c += kFxBatch, q += kFxBatch * cstride, gq += kFxBatch * p.chunk) {
+    uint4 w[kFxBatch];
+    float g[kFxBatch];
+#pragma unroll
+    for (int i = 0; i < kFxBatch; ++i) {
+      w[i] = *reinterpret_cast<const uint4*>(q + i * cstride);
+      g[i] = gq[i * p.chunk];
+    }
+#pragma unroll
+    for (int i = 0; i < kFxBatch; ++i) {
+      fx_apply(w[i], exp2f(lgc), acc);
+      *reinterpret_cast<uint4*>(q + i * cstride) = w[i];
+      lgc += g[i];
+    }
+  }
+  for (; c < e; ++c, q += cstride, gq += p.chunk) {
+    uint4 w = *reinterpret_cast<const uint4*>(q);
+    fx_apply(w, exp2f(lgc), acc);
+    *reinterpret_cast<uint4*>(q) = w;
+    lgc += *gq;
+  }
+  if ((int64_t)e == nc && p.h_final) {
+    const float f = exp2f(lgc);
+    float4* q = reinterpret_cast<float4*>(p.h_final + (bh * 64 + pp) * 128 + s0);
+    float4 a0 = q[0], a1 = q[1];
+    a0.x = fmaf(f, acc[0], a0.x); a0.y = fmaf(f, acc[1], a0.y); a0.z = fmaf(f, acc[2], a0.z); a0.w = fmaf(f, acc[3], a0.w);
+    a1.x = fmaf(f, acc[4], a1.x); a1.y = fmaf(f, acc[5], a1.y); a1.z = fmaf(f, acc[6], a1.z); a1.w = fmaf(f, acc[7], a1.w);
+    q[0] = a0;
+    q[1] = a1;
+  }
+}
+
 // CTAs of a launch: one per chain, or one per SM (ranges of at least one chain) when there are
-// more chains than SMs
-__host__ __forceinline__ int64_t sf_grid(int64_t chains, int64_t nchunks, int sms) {
-  return (chains <= sms || nchunks == 0) ? chains : sms;
+// more chains than SMs; with split chains one per SM (at most one per unit)
+__host__ __forceinline__ int64_t sf_grid(int64_t chains, int64_t nchunks, int sms, bool split) {
+  if (nchunks == 0) return chains;
+  if (split) return chains * nchunks < sms ? chains * nchunks : sms;
+  return chains <= sms ? chains : sms;
 }
 
 }  // namespace
 
-int64_t ssd_fused_schedule(int64_t chains, int64_t nchunks, int sms, int64_t* rows, int64_t cap) {
+int64_t ssd_fused_schedule(int64_t chains, int64_t nchunks, int sms, bool split, int64_t* rows, int64_t cap) {
   if (chains < 0 || nchunks < 0 || sms < 1) return -1;
-  const int64_t grid = sf_grid(chains, nchunks, sms), units = chains * nchunks;
+  const int64_t grid = sf_grid(chains, nchunks, sms, split), units = chains * nchunks;
   int64_t n = 0;
   for (int64_t k = 0; k < grid; ++k) {
     const int64_t u0 = k * units / grid, u1 = (k + 1) * units / grid;
@@ -607,19 +775,44 @@ bool ssd_state_fused_possible(const SsdDims& d) {
          d.chunk % kSfKH == 0 && d.chunk <= 256;
 }
 
+namespace {
+int device_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return sms;
+}
+// The rule for split chains: few chains (at most half the SMs) of many chunks, but at most 16
+// pieces per chain, since the fix-up of a piece composes the end states of every earlier piece
+// of its chain (measured: 16 chains of 512 chunks 886 us against 943 us for chunk states +
+// look-back state passing, 16 of 128 chunks 250 against 259 us; 4 chains of 64 chunks 79
+// against 50 us, 2 of 256 138 against 91 us).
+bool sf_split_rule(int64_t chains, int64_t nchunks, int sms) {
+  return 2 * chains <= sms && 16 * chains >= sms && nchunks >= SSM_SF_SPLIT_MIN_CHUNKS;
+}
+}  // namespace
+
 // Whether the fused kernel is the faster state path: the plan's choice, else either more
 // chains than SMs (ranges split across CTAs: b4 L8192 nh80, 160 chains, 158 us against 207 us
-// for chunk states + state passing), or one wave of short chains (a long chain is one CTA's
-// serial work).
+// for chunk states + state passing), one wave of short chains (a long chain is one CTA's
+// serial work), or few long chains, split into pieces (see ssd_state_fused_split).
 bool ssd_state_fused_supported(const SsdDims& d) {
   if (!ssd_state_fused_possible(d)) return false;
   if (d.plan_fused >= 0) return d.plan_fused != 0;
-  int dev = 0, sms = 148;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return false;
+  const int sms = device_sms();
+  if (sms < 1) return false;
   const int64_t chains = d.batch * (int64_t)(d.nheads / 2);
-  return chains > sms || d.nchunks <= 16;
+  return chains > sms || d.nchunks <= 16 || sf_split_rule(chains, d.nchunks, sms);
+}
+
+// Whether the fused pass splits its chains into independent pieces (one range per SM, every
+// piece after a chain's first from a zero state) and ssd_state_fixup then adds the state each
+// piece enters with: the plan's choice (fused = 2), else the rule above.
+bool ssd_state_fused_split(const SsdDims& d) {
+  if (!ssd_state_fused_possible(d) || d.nchunks == 0) return false;
+  if (d.plan_fused >= 0) return d.plan_fused == 2;
+  const int sms = device_sms();
+  return sms > 0 && sf_split_rule(d.batch * (int64_t)(d.nheads / 2), d.nchunks, sms);
 }
 
 cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float* h0, float* h_final,
@@ -664,14 +857,17 @@ cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float*
   p.b_keep = (uint64_t)d.batch * (uint64_t)d.seqlen * (uint64_t)d.ngroups * 128u * 2u <= (32ull << 20);
   const int64_t chains = d.batch * (int64_t)(d.nheads / 2);
   p.units = chains * d.nchunks;
-  int dev = 0, sms = 148;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int sms = device_sms();
+  if (sms < 1) return cudaErrorInvalidDevice;
+  const bool split = ssd_state_fused_split(d);
+  p.split = split ? 1 : 0;
   // one chain per CTA, or one CTA per SM with ranges of at least one chain (chains > SMs), so
   // that a range never lies inside one chain; the CTAs claim their ranges in order, so the CTA
-  // whose published state a range waits for is already running
-  const int64_t grid = sf_grid(chains, d.nchunks, sms);
-  if (grid > chains || ws.sp_tiles < chains) return cudaErrorInvalidValue;
+  // whose published state a range waits for is already running.  With split chains one range
+  // per SM, each publishing into its own slot of the (otherwise unused) chunk-state buffer,
+  // which holds a 128 x 128 state per unit.
+  const int64_t grid = sf_grid(chains, d.nchunks, sms, split);
+  if (split ? grid > p.units : (grid > chains || ws.sp_tiles < chains)) return cudaErrorInvalidValue;
   // the plan's ring split (X slots + B slots); the rule is 4 + 3
   auto go = [&](auto kernel, size_t total) -> cudaError_t {
     const size_t smem = total + 1024;
@@ -684,6 +880,27 @@ cudaError_t launch_ssd_state_fused_tc(const void* x, const void* B, const float*
     case 3: return go(ssd_state_fused_tc_kernel<5, 2>, SfLayout<5, 2>().total);
     default: return go(ssd_state_fused_tc_kernel<4, 3>, SfLayout<4, 3>().total);
   }
+}
+
+cudaError_t launch_ssd_state_fixup(float* h_final, const SsdDims& d, const SsdWorkspace& ws, cudaStream_t s) {
+  const int64_t chains = d.batch * (int64_t)(d.nheads / 2);
+  const int sms = device_sms();
+  if (sms < 1) return cudaErrorInvalidDevice;
+  FxParams p;
+  p.G = ws.G;
+  p.hin = static_cast<__nv_bfloat16*>(ws.hin);
+  p.h_final = h_final;
+  p.carry = ws.Sc;
+  p.units = chains * d.nchunks;
+  p.ranges = sf_grid(chains, d.nchunks, sms, true);  // as the fused pass split them
+  p.nchunks = d.nchunks;
+  p.lpad = d.lpad;
+  p.nheads = d.nheads;
+  p.chunk = d.chunk;
+  const int64_t grid = (p.ranges - 1) * (128 / kFxRows);
+  if (grid <= 0) return cudaSuccess;  // one range: every chain ran whole
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  return launch_pdl(ssd_state_fixup_kernel, dim3((unsigned)grid), dim3(kFxThreads), 0, s, p);
 }
 
 }  // namespace ssm

@@ -185,3 +185,4 @@ def test_plan_id_packing():
     assert ssm.plan_id() == 0 | (0 << 2)                    # all rules of thumb
     assert ssm.plan_id(1, -1, 0) == 2
     assert ssm.plan_id(0, 1, 20) == 1 | (2 << 2) | (20 << 4)
+    assert ssm.plan_id(2, -1, 0) == 3                        # the fused pass with split chains

@@ -37,6 +37,7 @@ def test_every_plan_is_correct(cuda_lib, dtype, hpg):
     if dtype == "bf16":
         plans += [ssm.plan_id(1, -1, 0)] + [ssm.plan_id(f, 1 - f, h) for f in (0, 1) for h in (1, 2, hpg)]
         plans += [ssm.plan_id(1, -1, h, ring) for ring in (1, 2, 3) for h in (0, 1)]  # the fused pass's ring splits
+        plans += [ssm.plan_id(2, -1, h, ring) for ring in (0, 2) for h in (0, 1)]  # split chains
     try:
         for plan in plans:
             ssm.set_ssd_fwd_plan(d["x"], d["B"], shape.chunk, plan)
@@ -77,7 +78,7 @@ def test_invalid_plan_rejected(cuda_lib):
     x = torch.zeros((1, 256, 2, 64), device="cuda", dtype=torch.bfloat16)
     B = torch.zeros((1, 256, 1, 128), device="cuda", dtype=torch.bfloat16)
     with pytest.raises(ssm.SsmError) as e:
-        ssm.set_ssd_fwd_plan(x, B, 256, 3)   # fused field 3 is not a choice
+        ssm.set_ssd_fwd_plan(x, B, 256, 3 << 2)   # sequential field 3 is not a choice
     assert e.value.status == _lib.SSM_ERR_INVALID_ARG
     with pytest.raises(ssm.SsmError) as e:
         ssm.set_ssd_fwd_plan(x, B, 256, 4 << 20)  # ring field 4 is not a choice

@@ -115,7 +115,7 @@ def test_headline_workload_every_plan_every_unit(cuda_lib):
     inp = synth.ssd_inputs(shape)
     x_dev, b_dev = P.to_dev(inp["x"], shape.dtype), P.to_dev(inp["B"], shape.dtype)
     plans = [ssm.plan_id(1, -1, 0), ssm.plan_id(1, -1, 16, 2), ssm.plan_id(1, -1, 0, 3), ssm.plan_id(0, 1, 0),
-             ssm.plan_id(0, 0, 0), ssm.plan_id(0, 1, 40)]
+             ssm.plan_id(0, 0, 0), ssm.plan_id(0, 1, 40), ssm.plan_id(2, -1, 0)]
     outs = {}
     try:
         for plan in plans:
@@ -146,15 +146,67 @@ def test_small_shapes_all_outputs(cuda_lib, shape):
     P.assert_ssd_close(shape.dtype, y, y_ref, hf, hf_ref, shape.name)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_long_state_chain(cuda_lib, dtype):
-    """Many chunks through the look-back state passing (nc = 200 chunks -> 13 chunk tiles)."""
+@pytest.mark.parametrize("dtype,fused", [("f32", -1), ("bf16", 0), ("bf16", 2)])
+def test_long_state_chain(cuda_lib, dtype, fused):
+    """Many chunks of one chain (nc = 200): through the look-back state passing (13 chunk tiles),
+    and for bf16 also through the fused pass with the chain split into pieces."""
+    import selective_state_space_mamba_gb300 as ssm
     shape = synth.SSDShape(f"chain_{dtype}", 1, 200 * 64 - 5, 2, 64, 128, 1, 64, dtype, dt_shift=4.0, h0=True)
     inp = synth.ssd_inputs(shape, seed=77)
-    y, hf = gpu_ssd(inp, shape)
+    x_dev, b_dev = P.to_dev(inp["x"], dtype), P.to_dev(inp["B"], dtype)
+    try:
+        if fused >= 0:
+            ssm.set_ssd_fwd_plan(x_dev, b_dev, shape.chunk, ssm.plan_id(fused, 0 if fused == 0 else -1, 0))
+        y, hf = gpu_ssd(inp, shape)
+    finally:
+        ssm.clear_ssd_fwd_plans()
     y_ref, hf_ref = native.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"])
     y_ref = y_ref.reshape(1, 2, -1, 64).transpose(0, 2, 1, 3)
     P.assert_ssd_close(dtype, y, y_ref, hf, hf_ref.reshape(hf.shape), shape.name)
+
+
+# Split chains (the fused pass in pieces, then the fix-up of each piece's entering state):
+# pieces of one chunk with fix-up walks back over up to 64 pieces; pieces that cross chain
+# boundaries; a ragged last chunk; every chunk size; grouped B/C; with and without h0.
+SPLIT = [synth.SSDShape("split_b1_nc65_T256", 1, 65 * 256 - 37, 4, 64, 128, 1, 256, "bf16", h0=True),
+         synth.SSDShape("split_b3_nc100_T64", 3, 100 * 64, 2, 64, 128, 1, 64, "bf16", h0=True),
+         synth.SSDShape("split_b1_nc41_T128_G2", 1, 40 * 128 + 5, 8, 64, 128, 2, 128, "bf16", h0=True),
+         synth.SSDShape("split_b2_nc300_T64_G1", 2, 300 * 64 - 1, 4, 64, 128, 1, 64, "bf16", dt_shift=4.0, h0=True)]
+
+
+@pytest.mark.parametrize("shape", SPLIT, ids=lambda s: s.name)
+@pytest.mark.parametrize("with_h0", [True, False])
+def test_split_chains_all_outputs(cuda_lib, shape, with_h0):
+    import selective_state_space_mamba_gb300 as ssm
+    inp = synth.ssd_inputs(shape, seed=zlib.crc32(shape.name.encode()))
+    x_dev, b_dev = P.to_dev(inp["x"], shape.dtype), P.to_dev(inp["B"], shape.dtype)
+    try:
+        ssm.set_ssd_fwd_plan(x_dev, b_dev, shape.chunk, ssm.plan_id(2, -1, 0))
+        y, hf = gpu_ssd(inp, shape, h0=with_h0)
+    finally:
+        ssm.clear_ssd_fwd_plans()
+    nh = shape.nheads
+    units = np.arange(shape.batch * nh)
+    y_ref, hf_ref = oracle_units(inp, units, h0=with_h0)
+    P.assert_ssd_close(shape.dtype, np.stack([y[u // nh, :, u % nh] for u in units]), y_ref,
+                       np.stack([hf[u // nh, u % nh] for u in units]), hf_ref, shape.name)
+
+
+def test_long_sequence_workload_both_state_paths(cuda_lib):
+    """b1 L131072 nh32 G8 (16 chains of 512 chunks) through the two state kernels (look-back
+    state passing) and through the fused pass with split chains, every unit."""
+    import selective_state_space_mamba_gb300 as ssm
+    shape = synth.SSD_B1_L131072
+    inp = synth.ssd_inputs(shape)
+    x_dev, b_dev = P.to_dev(inp["x"], shape.dtype), P.to_dev(inp["B"], shape.dtype)
+    outs = {}
+    try:
+        for plan in (ssm.plan_id(0, 0, 0), ssm.plan_id(2, -1, 0)):
+            ssm.set_ssd_fwd_plan(x_dev, b_dev, shape.chunk, plan)
+            outs[f"plan {plan}"] = gpu_ssd_f32(inp, shape)
+    finally:
+        ssm.clear_ssd_fwd_plans()
+    compare_all_units(shape, inp, outs)
 
 
 def test_no_h0_and_no_final_state(cuda_lib):
