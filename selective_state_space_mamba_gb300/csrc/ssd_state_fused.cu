@@ -731,10 +731,19 @@ __global__ void __launch_bounds__(kFxThreads, 3) ssd_state_fixup_kernel(FxParams
 }
 
 // CTAs of a launch: one per chain, or one per SM (ranges of at least one chain) when there are
-// more chains than SMs; with split chains one per SM (at most one per unit)
+// more chains than SMs.  With split chains, as many equal pieces of every chain as fit the SMs
+// (at most one per chunk), so that the pieces of the two head pairs that share a group's B run
+// the same chunks at the same time and read B once from DRAM; with more chains than SMs, one
+// range per SM.
 __host__ __forceinline__ int64_t sf_grid(int64_t chains, int64_t nchunks, int sms, bool split) {
   if (nchunks == 0) return chains;
-  if (split) return chains * nchunks < sms ? chains * nchunks : sms;
+  if (split) {
+    if (chains <= sms) {
+      const int64_t per = (int64_t)sms / chains;
+      return chains * (per < nchunks ? per : nchunks);
+    }
+    return sms;
+  }
   return chains <= sms ? chains : sms;
 }
 

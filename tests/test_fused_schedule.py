@@ -69,18 +69,26 @@ def test_carry_published_before_it_is_needed(chains, nchunks, sms):
         assert t_pub <= t_need, f"chain {chain}: published after {t_pub} units, needed after {t_need}"
 
 
+def split_grid(chains, nchunks, sms):
+    """Split chains: the same number of equal pieces for every chain, as many as fit the SMs (at
+    most one per chunk), so that pieces of different chains line up; one range per SM when
+    there are more chains than SMs."""
+    return chains * min(sms // chains, nchunks) if chains <= sms else sms
+
+
 SPLIT_SHAPES = [(16, 512, 152), (2, 64, 152), (1, 4, 152), (1, 1000, 152), (7, 9, 4), (76, 64, 152), (3, 152, 152),
                 (160, 32, 152), (5, 30, 148)]
 
 
 @pytest.mark.parametrize("chains,nchunks,sms", SPLIT_SHAPES)
 def test_split_chains_every_unit_once(chains, nchunks, sms):
-    """Split chains: one range per SM (at most one per unit), each of equal length; a segment
+    """Split chains: ranges of equal length (see split_grid); a segment
     starts from zero exactly when it starts inside its chain and publishes (into its CTA's slot)
     exactly when it ends inside it, so every range publishes at most once."""
     rows = schedule(chains, nchunks, sms, split=True)
     units = chains * nchunks
-    grid = min(sms, units)
+    grid = split_grid(chains, nchunks, sms)
+    assert int(rows[:, 0].max()) + 1 == grid
     seen = np.zeros((chains, nchunks), dtype=np.int64)
     for cta, chain, c0, c1, from_zero, publish in rows:
         assert 0 <= cta < grid and 0 <= chain < chains and 0 <= c0 < c1 <= nchunks
@@ -101,7 +109,7 @@ def test_split_chains_compose_to_the_recurrence(chains, nchunks, sms):
     rng = np.random.default_rng(7)
     rows = schedule(chains, nchunks, sms, split=True)
     units = chains * nchunks
-    grid = min(sms, units)
+    grid = split_grid(chains, nchunks, sms)
     lg = -rng.random((chains, nchunks)) * 0.5  # log2 decays
     inc = rng.standard_normal((chains, nchunks))
     h0 = rng.standard_normal(chains)
