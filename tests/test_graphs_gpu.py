@@ -147,3 +147,38 @@ def test_fused_split_chains_graph_replays(cuda_lib):
             P.assert_ssd_close("bf16", yu, y_ref, hu, hf_ref, f"{shape.name} replay {rep}")
     finally:
         ssm.clear_ssd_fwd_plans()
+
+
+def test_split_chains_graph_replays(cuda_lib):
+    """The fused pass with split chains (every piece from a zero state, then the fix-up kernel
+    adds the state each piece enters with) inside a CUDA graph: 2 chains of 65 chunks, so the
+    pieces are single chunks and each fix-up composes up to 64 earlier pieces' end states."""
+    import torch
+    import selective_state_space_mamba_gb300 as ssm
+    shape = synth.SSDShape("graph_split_chains", 1, 65 * 64 - 3, 4, 64, 128, 1, 64, "bf16", h0=True)
+    inp0 = synth.ssd_inputs(shape, seed=95)
+    d = {k: P.to_dev(v, "bf16" if k in ("x", "dt", "B", "C") else "f32") for k, v in inp0.items()}
+    y = torch.empty_like(d["x"])
+    hf = torch.empty((1, shape.nheads, 64, 128), device="cuda")
+
+    def call():
+        ssm.ssd_fwd(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["h0"], chunk=shape.chunk, y=y, h_final=hf)
+
+    try:
+        ssm.set_ssd_fwd_plan(d["x"], d["B"], shape.chunk, ssm.plan_id(2, -1, 0))
+        call()  # warm-up outside the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call()
+        for rep in range(3):
+            inp = synth.ssd_inputs(shape, seed=96 + rep)
+            for k, v in inp.items():
+                d[k].copy_(P.to_dev(v, "bf16" if k in ("x", "dt", "B", "C") else "f32"))
+            g.replay()
+            torch.cuda.synchronize()
+            assert ssm.check_device_status(kind="ssd") == 0
+            y_ref, hf_ref = ossd.ssd_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"], inp["h0"])
+            P.assert_ssd_close("bf16", P.to_np(y), y_ref, P.to_np(hf), hf_ref, f"{shape.name} replay {rep}")
+    finally:
+        ssm.clear_ssd_fwd_plans()
