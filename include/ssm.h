@@ -152,7 +152,7 @@ SSM_API ssm_status ssm_ssd_fwd(const void *x, const void *dt, const float *A, co
  * (fused + 1) | (sequential + 1) << 2 | heads_per_cta << 4 | ring << 20, where fused and
  * sequential are 1 (yes), 0 (no) or -1 (rule of thumb), fused may also be 2 (the one-kernel
  * pass with split chains; the rule takes it for between a sixteenth and a half as many chains
- * as SMs, with at least 64 chunks each), heads_per_cta (0 .. 65535) n > 0 gives
+ * as SMs, with at least 32 chunks each), heads_per_cta (0 .. 65535) n > 0 gives
  * every chunk-scan CTA a run of at most n heads (a tile's heads split evenly) and 0 means the
  * split a model of the hardware's CTA dispatch finds fastest (large runs first, small runs
  * last; ssm_debug_scan_schedule shows it; the first call of a shape on a device spends up to

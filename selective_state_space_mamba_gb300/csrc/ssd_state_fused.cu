@@ -47,7 +47,7 @@
 #include "tc_common.cuh"
 
 #ifndef SSM_SF_SPLIT_MIN_CHUNKS  // the rule splits chains of at least this many chunks
-#define SSM_SF_SPLIT_MIN_CHUNKS 64
+#define SSM_SF_SPLIT_MIN_CHUNKS 32
 #endif
 
 namespace ssm {
@@ -791,11 +791,12 @@ int device_sms() {
     return 0;
   return sms;
 }
-// The rule for split chains: few chains (at most half the SMs) of many chunks, but at most 16
-// pieces per chain, since the fix-up of a piece composes the end states of every earlier piece
-// of its chain (measured: 16 chains of 512 chunks 886 us against 943 us for chunk states +
-// look-back state passing, 16 of 128 chunks 250 against 259 us; 4 chains of 64 chunks 79
-// against 50 us, 2 of 256 138 against 91 us).
+// The rule for split chains: few chains (at most half the SMs) of at least 32 chunks, but at
+// most 16 pieces per chain, since the fix-up of a piece composes the end states of every
+// earlier piece of its chain (measured, forward: 16 chains of 512 chunks 855 us against 943 us
+// for chunk states + look-back state passing, 16 of 128 chunks 243 against 259 us, 20 of 128
+// 247 against 272 us, 32 of 32 114 against 120 us; 8 chains of 64 chunks 87 against 77 us, 4
+// of 64 79 against 50 us, 2 of 256 138 against 91 us).
 bool sf_split_rule(int64_t chains, int64_t nchunks, int sms) {
   return 2 * chains <= sms && 16 * chains >= sms && nchunks >= SSM_SF_SPLIT_MIN_CHUNKS;
 }
