@@ -48,8 +48,9 @@
  *     synchronized; the look-back flags carry an epoch kept in the workspace that each launch
  *     advances).  Make one ordinary call per device and shape before capturing, so that
  *     one-time set-up (kernel attributes, the no-alloc scratch address) happens outside the
- *     capture.  ssm_ssd_fwd_tune and ssm_check_device_status synchronize and cannot be
- *     captured.
+ *     capture.  ssm_ssd_fwd_tune, ssm_linscan_fwd_tune (the two also allocate, for the
+ *     duration of the call, the temporary buffer they flush L2 with) and
+ *     ssm_check_device_status synchronize and cannot be captured.
  */
 #ifndef SSM_GB300_H
 #define SSM_GB300_H
