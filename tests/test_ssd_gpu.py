@@ -175,21 +175,23 @@ SPLIT = [synth.SSDShape("split_b1_nc65_T256", 1, 65 * 256 - 37, 4, 64, 128, 1, 2
 
 
 @pytest.mark.parametrize("shape", SPLIT, ids=lambda s: s.name)
-@pytest.mark.parametrize("with_h0", [True, False])
-def test_split_chains_all_outputs(cuda_lib, shape, with_h0):
+@pytest.mark.parametrize("with_h0,with_final", [(True, True), (False, True), (True, False)])
+def test_split_chains_all_outputs(cuda_lib, shape, with_h0, with_final):
     import selective_state_space_mamba_gb300 as ssm
     inp = synth.ssd_inputs(shape, seed=zlib.crc32(shape.name.encode()))
     x_dev, b_dev = P.to_dev(inp["x"], shape.dtype), P.to_dev(inp["B"], shape.dtype)
     try:
         ssm.set_ssd_fwd_plan(x_dev, b_dev, shape.chunk, ssm.plan_id(2, -1, 0))
-        y, hf = gpu_ssd(inp, shape, h0=with_h0)
+        y, hf = gpu_ssd(inp, shape, h0=with_h0, final=with_final)
     finally:
         ssm.clear_ssd_fwd_plans()
+    assert (hf is None) == (not with_final)
     nh = shape.nheads
     units = np.arange(shape.batch * nh)
     y_ref, hf_ref = oracle_units(inp, units, h0=with_h0)
     P.assert_ssd_close(shape.dtype, np.stack([y[u // nh, :, u % nh] for u in units]), y_ref,
-                       np.stack([hf[u // nh, u % nh] for u in units]), hf_ref, shape.name)
+                       np.stack([hf[u // nh, u % nh] for u in units]) if with_final else None,
+                       hf_ref if with_final else None, shape.name)
 
 
 def test_long_sequence_workload_both_state_paths(cuda_lib):
